@@ -1,0 +1,194 @@
+"""CPU oracle of the MiniMax Sparse Attention forward pass (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use this package.  The product library never imports it, and it
+imports nothing from the product.  The arithmetic lives in ``msa_oracle.c``
+(plain C, one loop nest per step of the method); this module only marshals
+numpy arrays into it.
+
+Steps and their sources ("MiniMax Sparse Attention: let each query pick its own
+blocks", section "The mechanism, precisely", and its Figure 1):
+  * ``pooled``    -- index scores Q_idx . K_idx^T, max-pooled per block, causal;
+  * ``select``    -- top-k blocks by (score desc, index asc), local block forced;
+  * ``attention`` -- exact softmax attention over the selected blocks' tokens;
+  * ``forward``   -- the three chained.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libmsa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+def build() -> str:
+    """Compile ``msa_oracle.c`` (gcc + OpenMP) if the library is missing or stale."""
+    src = os.path.join(_HERE, "msa_oracle.c")
+    if (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(src):
+        subprocess.run(["make", "-s", "-C", _HERE], check=True)
+    return _LIB_PATH
+
+
+def _load(path: str | None = None):
+    """Load the oracle library (``path`` overrides the default build, for mutation tests)."""
+    global _lib
+    with _lock:
+        if path is not None:
+            _lib = None
+        if _lib is None:
+            lib = ctypes.CDLL(path or build())
+            lib.msa_oracle_pooled.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u16p, _u16p, ctypes.c_int, _i32p, ctypes.c_int, _f32p]
+            lib.msa_oracle_select.argtypes = [ctypes.c_int, _f32p, ctypes.c_int, _i32p, _f64p]
+            lib.msa_oracle_attention.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_double, _u16p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p,
+                _f64p, _f64p]
+            lib.msa_oracle_forward.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, ctypes.c_double, _u16p, _u16p, _u16p, _u16p, _u16p,
+                ctypes.c_int, _i32p, _i32p, _f64p, _f64p, _f64p]
+            for fn in (lib.msa_oracle_pooled, lib.msa_oracle_select, lib.msa_oracle_attention,
+                       lib.msa_oracle_forward):
+                fn.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def use_library(path: str | None):
+    """Switch to another build of ``msa_oracle.c`` (None: back to the default one)."""
+    global _lib
+    with _lock:
+        _lib = None
+    if path is not None:
+        _load(path)
+
+
+def _ptr(a: np.ndarray | None, ctype):
+    if a is None:
+        return ctypes.cast(None, ctype)
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctype)
+
+
+def _bits(a) -> np.ndarray:
+    """bf16 data as raw uint16 bits.  Accepts a torch bf16 tensor or a uint16 array."""
+    if isinstance(a, np.ndarray):
+        assert a.dtype == np.uint16
+        return np.ascontiguousarray(a)
+    import torch  # local: only needed when a torch tensor is passed
+    assert a.dtype == torch.bfloat16, a.dtype
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    a = np.asarray(a)
+    return np.ascontiguousarray(a.astype(np.int32, copy=False))
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (code {rc})")
+
+
+def max_blocks(cu_k: np.ndarray, block: int) -> int:
+    kv = np.diff(_i32(cu_k))
+    return int(max(1, ((kv.max() - 1) // block + 1) if kv.size and kv.max() > 0 else 1))
+
+
+def pooled(cu_q, cu_k, q_idx, k_idx, block: int, rows=None, nb_stride: int | None = None) -> np.ndarray:
+    """Block max-pooled causal index scores, fp32 [n_rows, Hkv, nb_stride] (-inf past the causal end)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    qb, kb = _bits(q_idx), _bits(k_idx)
+    total_q, hkv, d_idx = qb.shape
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    nb_stride = nb_stride or max_blocks(cu_k, block)
+    out = np.empty((n_rows, hkv, nb_stride), np.float32)
+    rc = _load().msa_oracle_pooled(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hkv, d_idx,
+                                   block, _ptr(qb, _u16p), _ptr(kb, _u16p), n_rows,
+                                   _ptr(rows_a, _i32p), nb_stride, _ptr(out, _f32p))
+    _check(rc, "pooled")
+    return out
+
+
+def select(pooled_row: np.ndarray, nb: int, k: int):
+    """Top-k of one pooled row (local block nb-1 forced).  Returns (idx[k] int32, gap float)."""
+    row = np.ascontiguousarray(pooled_row, dtype=np.float32)
+    assert row.size >= nb
+    sel = np.empty(max(k, 1), np.int32)
+    gap = ctypes.c_double(0.0)
+    rc = _load().msa_oracle_select(nb, _ptr(row, _f32p), k, _ptr(sel, _i32p), ctypes.byref(gap))
+    _check(rc, "select")
+    return sel[:k], gap.value
+
+
+def attention(cu_q, cu_k, q, k, v, idx, block: int, scale: float | None = None, rows=None):
+    """Main Branch over given block indices.  Returns (o [n, Hq, D] f64, lse [n, Hq] f64)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    qb, kb, vb = _bits(q), _bits(k), _bits(v)
+    total_q, hq, head_dim = qb.shape
+    hkv = kb.shape[1]
+    idx_a = _i32(idx)
+    topk = idx_a.shape[-1]
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    assert idx_a.shape == (n_rows, hkv, topk)
+    scale = float(head_dim ** -0.5 if scale is None else scale)
+    o = np.empty((n_rows, hq, head_dim), np.float64)
+    lse = np.empty((n_rows, hq), np.float64)
+    rc = _load().msa_oracle_attention(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hq, hkv,
+                                      head_dim, block, topk, scale, _ptr(qb, _u16p), _ptr(kb, _u16p),
+                                      _ptr(vb, _u16p), _ptr(idx_a, _i32p), n_rows,
+                                      _ptr(rows_a, _i32p), _ptr(o, _f64p), _ptr(lse, _f64p))
+    _check(rc, "attention")
+    return o, lse
+
+
+def forward(cu_q, cu_k, q, k, v, q_idx, k_idx, block: int, topk: int, scale: float | None = None,
+            rows=None):
+    """All three steps.  Returns dict(idx [n,Hkv,k] i32, gap [n,Hkv] f64, o [n,Hq,D] f64, lse [n,Hq] f64)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    qb, kb, vb, qib, kib = _bits(q), _bits(k), _bits(v), _bits(q_idx), _bits(k_idx)
+    total_q, hq, head_dim = qb.shape
+    hkv = kb.shape[1]
+    d_idx = qib.shape[2]
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    scale = float(head_dim ** -0.5 if scale is None else scale)
+    idx = np.empty((n_rows, hkv, topk), np.int32)
+    gap = np.empty((n_rows, hkv), np.float64)
+    o = np.empty((n_rows, hq, head_dim), np.float64)
+    lse = np.empty((n_rows, hq), np.float64)
+    rc = _load().msa_oracle_forward(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hq, hkv,
+                                    head_dim, d_idx, block, topk, scale, _ptr(qb, _u16p),
+                                    _ptr(kb, _u16p), _ptr(vb, _u16p), _ptr(qib, _u16p),
+                                    _ptr(kib, _u16p), n_rows, _ptr(rows_a, _i32p), _ptr(idx, _i32p),
+                                    _ptr(gap, _f64p), _ptr(o, _f64p), _ptr(lse, _f64p))
+    _check(rc, "forward")
+    return {"idx": idx, "gap": gap, "o": o, "lse": lse}
+
+
+def query_positions(cu_q, cu_k) -> np.ndarray:
+    """Key position of every packed query row (bottom-right alignment)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    out = np.empty(int(cu_q[-1]), np.int64)
+    for s in range(len(cu_q) - 1):
+        ql, kl = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+        out[cu_q[s]:cu_q[s + 1]] = kl - ql + np.arange(ql)
+    return out

@@ -1,0 +1,309 @@
+/*
+ * msa_oracle.c -- plain CPU reference of the MiniMax Sparse Attention (MSA)
+ * forward pass.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * benchmark's CPU-baseline leg are the only callers.  The product library
+ * never links, loads or calls this file, and this file shares no code, header
+ * or constant with the CUDA path.
+ *
+ * What it computes (one function per step, in the order the method runs):
+ *
+ *  1. msa_oracle_pooled -- Index Branch scores and block max-pool.
+ *     "MiniMax Sparse Attention: let each query pick its own blocks",
+ *     section "The mechanism, precisely", first bullet: one index-query head
+ *     per GQA group, one shared index-key head, token scores Q_idx . K_idx^T,
+ *     max-pooled to 128-token blocks.  The same page's Figure 1 (architecture
+ *     diagram) shows the order: score matrix -> block max pooling -> top-k.
+ *     Only keys at or before the query's own position enter a pool.
+ *
+ *  2. msa_oracle_select -- top-k block selection with the local block forced
+ *     in.  Same section: keep the top-k blocks (k = 16 deployed), the block
+ *     the query sits in is always kept; the atlas record of the report
+ *     ("MiniMax M3 428B" architecture page, summary paragraph) states the
+ *     local block is forced in and that selection is per query and per group.
+ *     Ranking: pooled score descending, ties to the lower block index.
+ *
+ *  3. msa_oracle_attention -- Main Branch: exact softmax attention of every
+ *     query head over only the tokens of its group's selected blocks.  Same
+ *     section, second bullet ("exact attention over only those blocks",
+ *     "every head in a group reuses the same block set").
+ *
+ * Precision.  The pages fix no precision.  Token index scores are formed in
+ * double from the exact bf16 inputs and rounded once to fp32; pooling and
+ * ranking then run in fp32, because a float comparison there decides an
+ * integer (which blocks are kept) and the GPU path takes that decision in
+ * fp32.  The Main Branch runs entirely in double.
+ *
+ * Layout (packed variable-length batch, row-major, contiguous):
+ *   q      [total_q][hq][head_dim]      bf16 bits (uint16)
+ *   k, v   [total_k][hkv][head_dim]     bf16 bits
+ *   q_idx  [total_q][hkv][d_idx]        bf16 bits
+ *   k_idx  [total_k][d_idx]             bf16 bits
+ *   cu_q, cu_k  [num_seqs + 1] prefix sums of per-sequence query / key counts.
+ * Query t of sequence s sits at key position pos = kv_len - q_len + t
+ * (queries are the last q_len positions of the sequence; a decode step is
+ * q_len = 1).  Head h belongs to group h / (hq / hkv).
+ *
+ * Every function returns 0 on success and a negative code on bad arguments.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+#define ORACLE_ENOMEM (-2)
+
+static double bf16_bits_to_double(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Checks the two prefix-sum arrays: nondecreasing, start at 0, and every
+ * sequence has at least as many keys as queries. */
+static int check_seqlens(int num_seqs, const int32_t *cu_q, const int32_t *cu_k) {
+  if (num_seqs < 0 || !cu_q || !cu_k) return ORACLE_EINVAL;
+  if (cu_q[0] != 0 || cu_k[0] != 0) return ORACLE_EINVAL;
+  for (int s = 0; s < num_seqs; ++s) {
+    int q_len = cu_q[s + 1] - cu_q[s];
+    int kv_len = cu_k[s + 1] - cu_k[s];
+    if (q_len < 0 || kv_len < 0 || kv_len < q_len) return ORACLE_EINVAL;
+  }
+  return ORACLE_OK;
+}
+
+/* Sequence that owns packed query row i (linear scan: plain, not fast). */
+static int seq_of_query(int num_seqs, const int32_t *cu_q, int i) {
+  for (int s = 0; s < num_seqs; ++s)
+    if (i >= cu_q[s] && i < cu_q[s + 1]) return s;
+  return -1;
+}
+
+int msa_oracle_num_blocks(int pos, int block) { return pos / block + 1; }
+
+/*
+ * Step 1.  pooled[r][g][b] for query row rows[r] (all rows when rows == NULL,
+ * then n_rows must equal total_q) and group g:
+ *     s_j      = fp32( sum_d q_idx[i][g][d] * k_idx[key j][d] )   (sum in double)
+ *     pooled_b = max over keys j of block b with j <= pos of s_j  (fp32)
+ * for b = 0 .. pos / block.  Entries b > pos / block are set to -INFINITY.
+ */
+int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                      int hkv, int d_idx, int block,
+                      const uint16_t *q_idx, const uint16_t *k_idx,
+                      int n_rows, const int32_t *rows,
+                      int nb_stride, float *pooled) {
+  if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
+  if (hkv <= 0 || d_idx <= 0 || block <= 0 || n_rows < 0 || !pooled) return ORACLE_EINVAL;
+  const int total_q = cu_q[num_seqs];
+  if (!rows && n_rows != total_q) return ORACLE_EINVAL;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int r = 0; r < n_rows; ++r) {
+    const int i = rows ? rows[r] : r;
+    const int s = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
+    if (s < 0) { bad = 1; continue; }
+    const int q_len = cu_q[s + 1] - cu_q[s];
+    const int kv_len = cu_k[s + 1] - cu_k[s];
+    const int pos = kv_len - q_len + (i - cu_q[s]);
+    const int nb = msa_oracle_num_blocks(pos, block);
+    if (nb > nb_stride) { bad = 1; continue; }
+    for (int g = 0; g < hkv; ++g) {
+      float *out = pooled + ((size_t)r * hkv + g) * nb_stride;
+      for (int b = 0; b < nb_stride; ++b) out[b] = -INFINITY;
+      const uint16_t *qv = q_idx + ((size_t)i * hkv + g) * d_idx;
+      for (int b = 0; b < nb; ++b) {
+        float best = -INFINITY;
+        for (int j = b * block; j < (b + 1) * block && j <= pos; ++j) {
+          const uint16_t *kv = k_idx + (size_t)(cu_k[s] + j) * d_idx;
+          double acc = 0.0;
+          for (int d = 0; d < d_idx; ++d)
+            acc += bf16_bits_to_double(qv[d]) * bf16_bits_to_double(kv[d]);
+          float sj = (float)acc;
+          if (sj > best) best = sj;
+        }
+        out[b] = best;
+      }
+    }
+  }
+  return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/*
+ * Step 2.  For one pooled row of nb valid blocks whose local block is
+ * local = nb - 1 (the query's own block is the last causal one):
+ *   take the min(k - 1, nb - 1) best non-local blocks, best meaning larger
+ *   pooled score, equal scores going to the lower block index; add the local
+ *   block; write the set in ascending block order to sel[0..k), padding with
+ *   -1.  (When k <= 0 nothing is selected.)
+ * *gap receives the relative gap between the last selected non-local block
+ * and the best unselected non-local block, |a - b| / max(|a|, |b|, 1e-30),
+ * or +INFINITY when every non-local block is selected or none is (no float
+ * comparison decides the set).  Scores are compared as fp32 values; +0 and -0
+ * compare equal.
+ */
+int msa_oracle_select(int nb, const float *pooled_row, int k, int32_t *sel, double *gap) {
+  if (nb <= 0 || k < 0 || !pooled_row || (k > 0 && !sel)) return ORACLE_EINVAL;
+  const int local = nb - 1;
+  const int want = (k - 1 < nb - 1) ? k - 1 : nb - 1;
+  char *taken = (char *)calloc((size_t)nb, 1);
+  int32_t *chosen = (int32_t *)malloc(sizeof(int32_t) * (size_t)(want > 0 ? want : 1));
+  if (!taken || !chosen) { free(taken); free(chosen); return ORACLE_ENOMEM; }
+  if (k > 0) taken[local] = 1;
+  float last_val = 0.f;
+  for (int r = 0; r < want; ++r) {
+    int best = -1;
+    for (int b = 0; b < nb; ++b) {
+      if (taken[b]) continue;
+      /* scanning b upward with a strict '>' keeps the lower index on ties */
+      if (best < 0 || pooled_row[b] > pooled_row[best]) best = b;
+    }
+    taken[best] = 1;
+    chosen[r] = best;
+    last_val = pooled_row[best];
+  }
+  if (gap) {
+    *gap = INFINITY;
+    if (want >= 1 && want < nb - 1) {
+      int next = -1;
+      for (int b = 0; b < nb; ++b) {
+        if (taken[b]) continue;
+        if (next < 0 || pooled_row[b] > pooled_row[next]) next = b;
+      }
+      double a = last_val, c = pooled_row[next];
+      double den = fabs(a) > fabs(c) ? fabs(a) : fabs(c);
+      if (den < 1e-30) den = 1e-30;
+      *gap = fabs(a - c) / den;
+    }
+  }
+  /* ascending block order, -1 padding at the tail */
+  int n = 0;
+  for (int b = 0; b < nb && n < k; ++b)
+    if (taken[b]) sel[n++] = b;
+  for (; n < k; ++n) sel[n] = -1;
+  free(taken);
+  free(chosen);
+  return ORACLE_OK;
+}
+
+/*
+ * Step 3.  For query row rows[r] and every head h (group g = h / (hq/hkv)),
+ * with the group's selected blocks idx[r][g][0..topk) (-1 entries ignored):
+ *   x_j  = scale * sum_d q[i][h][d] * k[key j][g][d]   over tokens j of the
+ *          selected blocks with j <= pos
+ *   m    = max_j x_j,  l = sum_j exp(x_j - m)
+ *   o[r][h][:] = sum_j exp(x_j - m) v[key j][g][:] / l,  lse[r][h] = m + ln l
+ * all in double.  A row with no token (impossible when the local block is
+ * selected) gets o = 0 and lse = -INFINITY.
+ */
+int msa_oracle_attention(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                         int hq, int hkv, int head_dim, int block, int topk, double scale,
+                         const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const int32_t *idx, int n_rows, const int32_t *rows,
+                         double *o, double *lse) {
+  if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || head_dim <= 0 || block <= 0 || topk <= 0) return ORACLE_EINVAL;
+  if (!q || !k || !v || !idx || !o || !lse || n_rows < 0) return ORACLE_EINVAL;
+  const int total_q = cu_q[num_seqs];
+  if (!rows && n_rows != total_q) return ORACLE_EINVAL;
+  const int G = hq / hkv;
+  int bad = 0;
+#pragma omp parallel reduction(| : bad)
+  {
+    double *x = (double *)malloc(sizeof(double) * (size_t)topk * block);
+    int32_t *key = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk * block);
+    if (!x || !key) bad = 1;
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < n_rows; ++r) {
+      if (!x || !key) continue;
+      const int i = rows ? rows[r] : r;
+      const int s = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
+      if (s < 0) { bad = 1; continue; }
+      const int q_len = cu_q[s + 1] - cu_q[s];
+      const int kv_len = cu_k[s + 1] - cu_k[s];
+      const int pos = kv_len - q_len + (i - cu_q[s]);
+      for (int h = 0; h < hq; ++h) {
+        const int g = h / G;
+        const int32_t *sel = idx + ((size_t)r * hkv + g) * topk;
+        /* gather the attended token positions */
+        int n = 0;
+        for (int e = 0; e < topk; ++e) {
+          const int b = sel[e];
+          if (b < 0) continue;
+          for (int j = b * block; j < (b + 1) * block && j <= pos; ++j) key[n++] = j;
+        }
+        const uint16_t *qh = q + ((size_t)i * hq + h) * head_dim;
+        double *oh = o + ((size_t)r * hq + h) * head_dim;
+        for (int d = 0; d < head_dim; ++d) oh[d] = 0.0;
+        if (n == 0) { lse[(size_t)r * hq + h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+          const uint16_t *kj = k + ((size_t)(cu_k[s] + key[t]) * hkv + g) * head_dim;
+          double acc = 0.0;
+          for (int d = 0; d < head_dim; ++d) acc += bf16_bits_to_double(qh[d]) * bf16_bits_to_double(kj[d]);
+          x[t] = scale * acc;
+          if (x[t] > m) m = x[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < n; ++t) {
+          const double p = exp(x[t] - m);
+          l += p;
+          const uint16_t *vj = v + ((size_t)(cu_k[s] + key[t]) * hkv + g) * head_dim;
+          for (int d = 0; d < head_dim; ++d) oh[d] += p * bf16_bits_to_double(vj[d]);
+        }
+        for (int d = 0; d < head_dim; ++d) oh[d] /= l;
+        lse[(size_t)r * hq + h] = m + log(l);
+      }
+    }
+    free(x);
+    free(key);
+  }
+  return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/*
+ * Steps 1-3 chained for the query rows listed in rows (all when NULL).
+ * Outputs: idx [n_rows][hkv][topk] (ascending, -1 padded), gap
+ * [n_rows][hkv] (see msa_oracle_select), o [n_rows][hq][head_dim] and
+ * lse [n_rows][hq] in double.
+ */
+int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                       int hq, int hkv, int head_dim, int d_idx, int block, int topk, double scale,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const uint16_t *q_idx, const uint16_t *k_idx,
+                       int n_rows, const int32_t *rows,
+                       int32_t *idx, double *gap, double *o, double *lse) {
+  if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
+  if (hkv <= 0 || block <= 0 || topk <= 0 || !idx) return ORACLE_EINVAL;
+  int max_nb = 1;
+  for (int s = 0; s < num_seqs; ++s) {
+    int kv_len = cu_k[s + 1] - cu_k[s];
+    if (kv_len > 0) {
+      int nb = msa_oracle_num_blocks(kv_len - 1, block);
+      if (nb > max_nb) max_nb = nb;
+    }
+  }
+  float *pooled = (float *)malloc(sizeof(float) * (size_t)(n_rows > 0 ? n_rows : 1) * hkv * max_nb);
+  if (!pooled) return ORACLE_ENOMEM;
+  int rc = msa_oracle_pooled(num_seqs, cu_q, cu_k, hkv, d_idx, block, q_idx, k_idx,
+                             n_rows, rows, max_nb, pooled);
+  if (rc) { free(pooled); return rc; }
+  const int total_q = cu_q[num_seqs];
+  for (int r = 0; r < n_rows && !rc; ++r) {
+    const int i = rows ? rows[r] : r;
+    const int s = seq_of_query(num_seqs, cu_q, i);
+    const int pos = (cu_k[s + 1] - cu_k[s]) - (cu_q[s + 1] - cu_q[s]) + (i - cu_q[s]);
+    const int nb = msa_oracle_num_blocks(pos, block);
+    (void)total_q;
+    for (int g = 0; g < hkv && !rc; ++g)
+      rc = msa_oracle_select(nb, pooled + ((size_t)r * hkv + g) * max_nb, topk,
+                             idx + ((size_t)r * hkv + g) * topk,
+                             gap ? gap + (size_t)r * hkv + g : NULL);
+  }
+  free(pooled);
+  if (rc) return rc;
+  return msa_oracle_attention(num_seqs, cu_q, cu_k, hq, hkv, head_dim, block, topk, scale,
+                              q, k, v, idx, n_rows, rows, o, lse);
+}

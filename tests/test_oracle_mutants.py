@@ -1,0 +1,69 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies ``oracle/msa_oracle.c``, plants one mistake in the copy (on
+the CPU, in a temporary directory), compiles it and runs the pins from
+``test_oracle_pins`` against it: at least one pin has to fail.  The real oracle
+is restored afterwards.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                   "msa_oracle.c")
+
+MUTANTS = {
+    "pool_ignores_causality": ("j < (b + 1) * block && j <= pos; ++j) {", "j < (b + 1) * block; ++j) {"),
+    "ties_go_to_higher_index": ("pooled_row[b] > pooled_row[best]) best = b;",
+                                "pooled_row[b] >= pooled_row[best]) best = b;"),
+    "local_block_not_forced": ("if (k > 0) taken[local] = 1;", ""),
+    "attention_ignores_causality": ("j <= pos; ++j) key[n++] = j;", "1; ++j) key[n++] = j;"),
+    "scale_dropped": ("x[t] = scale * acc;", "x[t] = acc;"),
+    "wrong_group_of_head": ("const int g = h / G;", "const int g = h % hkv;"),
+    "top_left_alignment": ("const int pos = kv_len - q_len + (i - cu_q[s]);",
+                           "const int pos = (i - cu_q[s]);"),
+    "lse_without_max": ("lse[(size_t)r * hq + h] = m + log(l);", "lse[(size_t)r * hq + h] = log(l);"),
+    "index_dot_skips_last_dim": ("for (int d = 0; d < d_idx; ++d)", "for (int d = 0; d + 1 < d_idx; ++d)"),
+    "value_from_wrong_row": ("const uint16_t *vj = v + ((size_t)(cu_k[s] + key[t]) * hkv + g)",
+                             "const uint16_t *vj = v + ((size_t)(key[t]) * hkv + g)"),
+}
+
+PIN_TESTS = [
+    lambda: pins.test_golden_three_block_example(),
+    lambda: pins.test_pooled_matches_torch_matmul(0),
+    lambda: pins.test_select_matches_full_sort_with_ties(0),
+    lambda: pins.test_attention_matches_masked_sdpa(0),
+    lambda: pins.test_forward_equals_dense_causal_when_k_covers_all_blocks(),
+    lambda: pins.test_invariants_on_tiny_workload(),
+    lambda: pins.test_token_budget_and_closed_forms(),
+]
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = text.replace(old, new)
+    src = tmp_path / "mutant.c"
+    src.write_text(mutated)
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-fopenmp", "-shared", "-o", str(lib), str(src),
+                    "-lm"], check=True)
+    failures = 0
+    oracle.use_library(str(lib))
+    try:
+        for t in PIN_TESTS:
+            try:
+                t()
+            except (AssertionError, ValueError):
+                failures += 1
+    finally:
+        oracle.use_library(None)
+    assert failures > 0, f"no pin caught the mutant {name}"
