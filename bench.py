@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the MSA forward pass (index selection + sparse attention).
+
+One step = one msa_forward call (every stage of the hot path: plan, index
+scores with fused top-k, schedule, Main Branch, combine -- or, for decode
+workloads, the index scan, top-k, split attention and combine) over one batch
+of seeded synthetic inputs already resident in HBM.
+
+Default workload: prefill_32k (one causal sequence of 32768 queries, 64/4
+heads, head dim 128, d_idx 128, block 128, k 16).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl msa|reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own
+GPU (weak scaling, no data-path collective); the reported time is the max over
+ranks.  ``--impl reference`` times the CPU oracle (the plain reference
+implementation of the method) on the host cores, on a bounded sample of the
+same workload, and reports the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MSA prefill query-tok/s & decode tok/s at 128K/1M ctx; % of TC/HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ algorithmic work
+def algorithmic_work(x, idx: torch.Tensor):
+    """Per-stage algorithmic FLOPs / bytes of one step (from the actual selection)."""
+    cfg = x.cfg
+    G = cfg.hq // cfg.hkv
+    dev = idx.device
+    cu_q = x.cu_q.long().to(dev)
+    cu_k = x.cu_k.long().to(dev)
+    seq = torch.repeat_interleave(torch.arange(len(x.seqs), device=dev), (cu_q[1:] - cu_q[:-1]))
+    t = torch.arange(x.total_q, device=dev) - cu_q[seq]
+    pos = (cu_k[seq + 1] - cu_k[seq]) - (cu_q[seq + 1] - cu_q[seq]) + t          # [T]
+    # index: 2 * d_idx FLOPs per (query, group, causal key)
+    index_flops = float(2 * cfg.d_idx * cfg.hkv * (pos + 1).double().sum().item())
+    # Main Branch: tokens attended per (query, group)
+    b = idx.long()
+    valid = b >= 0
+    start = b * 128
+    ntok_blk = torch.clamp(pos[:, None, None] - start + 1, min=0, max=128) * valid
+    ntok = ntok_blk.sum(dim=2)                                                     # [T, Hkv]
+    attn_flops = float(4 * cfg.head_dim * G * ntok.double().sum().item())
+    n_slots = int(valid.sum().item())
+    # K/V bytes the Main Branch must read at least once: each selected block's K and V rows
+    kv_bytes_selected = float(2 * 2 * cfg.head_dim * ntok.double().sum().item())  # per (query,group) reads
+    k_idx_bytes = float(2 * cfg.d_idx * (pos + 1).double().sum().item()) if cfg.is_decode else None
+    # combine: read every valid partial (G x 128 bf16 + G fp32), write O and LSE
+    combine_bytes = float(n_slots * G * (cfg.head_dim * 2 + 4) + x.total_q * cfg.hq * (cfg.head_dim * 2 + 4) +
+                          x.total_q * cfg.hkv * cfg.topk * 4)
+    return {"index_flops": index_flops, "attn_flops": attn_flops, "n_slots": n_slots,
+            "kv_bytes_selected": kv_bytes_selected, "k_idx_bytes": k_idx_bytes,
+            "combine_bytes": combine_bytes, "ntok_total": float(ntok.double().sum().item())}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"msa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ traffic record from ncu
+def kernel_source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "block_sparse_attention_05_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "block_sparse_attention_05_gb300", "csrc", "common.cuh")):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel_file: str, units_now: float):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu record, scaled to this launch
+    by the units processed; None when absent or taken on a different version of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p)).get(workload)
+    except (ValueError, OSError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel_file):
+        return None
+    per_unit = rec["dram_bytes"] / rec["units"]
+    return per_unit * units_now
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+def host_copy(x):
+    return dict(cu_q=x.cu_q.cpu(), cu_k=x.cu_k.cpu(), q=x.q.cpu(), k=x.k.cpu(), v=x.v.cpu(),
+                q_idx=x.q_idx.cpu(), k_idx=x.k_idx.cpu())
+
+
+def oracle_rate(x, budget_s: float, max_rows: int = 100000, seed: int = 0, host=None):
+    """Query rows per second of the CPU oracle on a position-uniform sample of the workload's rows."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    host = host or host_copy(x)
+    cfg = x.cfg
+    ncores = os.cpu_count() or 1
+
+    def run(rows):
+        t0 = time.perf_counter()
+        oracle.forward(host["cu_q"], host["cu_k"], host["q"], host["k"], host["v"], host["q_idx"],
+                       host["k_idx"], block=cfg.block, topk=cfg.topk, rows=rows)
+        return time.perf_counter() - t0
+
+    n0 = min(x.total_q, max(ncores, 8))
+    rows = np.sort(rng.choice(x.total_q, size=n0, replace=False)).astype(np.int32)
+    t = run(rows)
+    n = int(min(x.total_q, max_rows, max(n0, n0 * budget_s / max(t, 1e-6))))
+    if n > n0:
+        rows = np.sort(rng.choice(x.total_q, size=n, replace=False)).astype(np.int32)
+        t = run(rows)
+    return n / t, n, t, ncores
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefill_32k", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="msa", choices=["msa", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    cfg = workloads.get(args.workload)
+    unit = "tok/s" if cfg.is_decode else "query tok/s"
+    higher = True
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        # inputs are drawn on the GPU when there is one (only to make them; the timed work is the oracle's)
+        x = workloads.generate(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+        host = host_copy(x)
+        per_step = []
+        rows_done = 0
+        budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+        for i in range(args.warmup + args.steps):
+            rate, n, t, cores = oracle_rate(x, budget_s=budget, seed=i, host=host)
+            if i >= args.warmup:
+                per_step.append((n, t))
+                rows_done += n
+        tot_t = sum(t for _, t in per_step)
+        value = rows_done / tot_t
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / len(per_step),
+                "higher_is_better": higher, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": f"{cfg.name}: {cfg.description}", "sample": "rows per step, position-uniform"},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows_done} query rows of {cfg.name} over {args.steps} steps"},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import block_sparse_attention_05_gb300 as msa
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    x = workloads.generate(cfg, device=dev)
+    prob = msa.Problem(x.cu_q, x.cu_k, x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq, cfg.hkv, cfg.d_idx,
+                       cfg.topk)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx = torch.empty((x.total_q, cfg.hkv, cfg.topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((x.total_q, cfg.hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(max(2 * L2_BYTES, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    timer = msa.StageTimer()
+
+    def step():
+        msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, idx=idx, o=o, lse=lse, ws=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    flags = msa.msa_read_device_status(ws)
+    if flags:
+        raise RuntimeError(f"device status flags {flags} after warm-up")
+
+    # ---------------- timed region (device-resident inputs)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = {s: [] for s in msa.STAGES}
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = msa.kernel_launch_count()
+    with ClockSampler(dev.index) as clk:
+        with timer:
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record()
+                step()
+                ends[i].record()
+                ends[i].synchronize()
+                for k, v in timer.elapsed_ms().items():
+                    stage_ms[k].append(v)
+        torch.cuda.synchronize()
+    launches = msa.kernel_launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    units_per_gpu = x.total_q
+    value = units_per_gpu * world / (ms / 1000.0)
+
+    # ---------------- roofline of the dominant kernel
+    peaks = measured_peaks()
+    work = algorithmic_work(x, idx)
+    stage_mean = {k: sum(v) / len(v) for k, v in stage_ms.items() if v}
+    dominant = max(stage_mean, key=stage_mean.get)
+    kernel_file = {"index": "decode.cu" if cfg.is_decode else "index_score.cu",
+                   "attn": "decode.cu" if cfg.is_decode else "sparse_attn.cu",
+                   "combine": "combine.cu", "topk": "topk.cu", "schedule": "schedule.cu", "plan": "plan.cu"}
+    if dominant == "attn" and not cfg.is_decode:
+        bound, unit_r, amount = "tensor", "TFLOP/s", work["attn_flops"]
+        achieved = amount / (stage_mean["attn"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+    elif dominant == "index" and not cfg.is_decode:
+        bound, unit_r, amount = "tensor", "TFLOP/s", work["index_flops"]
+        achieved = amount / (stage_mean["index"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+    elif dominant == "index":
+        bound, unit_r, amount = "hbm", "GB/s", work["k_idx_bytes"]
+        achieved = amount / (stage_mean["index"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+    elif dominant == "combine":
+        bound, unit_r, amount = "hbm", "GB/s", work["combine_bytes"]
+        achieved = amount / (stage_mean["combine"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+    else:
+        bound, unit_r, amount = "hbm", "GB/s", work["kv_bytes_selected"]
+        achieved = amount / (stage_mean[dominant] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+    traffic = ncu_traffic(cfg.name, kernel_file[dominant], units_per_gpu)
+    roofline = {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak, "unit": unit_r,
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peaks['source']} ({'bf16 burst' if bound == 'tensor' else 'HBM copy'})"}
+    stages = {}
+    for k, v in stage_mean.items():
+        e = {"ms": v, "share": v / ms}
+        if k == "index" and not cfg.is_decode:
+            e["tflops"] = work["index_flops"] / (v * 1e-3) / 1e12
+            e["frac_of_tc_peak"] = e["tflops"] / peaks["bf16_tflops"]
+        if k == "index" and cfg.is_decode:
+            e["gbs"] = work["k_idx_bytes"] / (v * 1e-3) / 1e9
+            e["frac_of_hbm_peak"] = e["gbs"] / peaks["hbm_gbs"]
+        if k == "attn" and not cfg.is_decode:
+            e["tflops"] = work["attn_flops"] / (v * 1e-3) / 1e12
+            e["frac_of_tc_peak"] = e["tflops"] / peaks["bf16_tflops"]
+        if k == "attn" and cfg.is_decode:
+            e["gbs"] = work["kv_bytes_selected"] / (v * 1e-3) / 1e9
+        if k == "combine":
+            e["gbs"] = work["combine_bytes"] / (v * 1e-3) / 1e9
+            e["frac_of_hbm_peak"] = e["gbs"] / peaks["hbm_gbs"]
+        stages[k] = e
+
+    # ---------------- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: getattr(x, n).cpu().pin_memory() for n in ("q", "k", "v", "q_idx", "k_idx", "cu_q", "cu_k")}
+        dev_in = {n: torch.empty_like(getattr(x, n)) for n in host_in}
+        host_out = {"idx": torch.empty(idx.shape, dtype=idx.dtype).pin_memory(),
+                    "o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
+        prob_e = msa.Problem(dev_in["cu_q"], dev_in["cu_k"], x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq,
+                             cfg.hkv, cfg.d_idx, cfg.topk)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for n, t in host_in.items():
+                dev_in[n].copy_(t, non_blocking=True)
+            msa.msa_forward(prob_e, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_idx"], dev_in["k_idx"],
+                            idx=idx, o=o, lse=lse, ws=ws)
+            host_out["idx"].copy_(idx, non_blocking=True)
+            host_out["o"].copy_(o, non_blocking=True)
+            host_out["lse"].copy_(lse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            e2e_step()
+        t1.record()
+        t1.synchronize()
+        e2e_ms = t0.elapsed_time(t1) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, t, cores = oracle_rate(x, budget_s=args.cpu_budget)
+        cpu = {"value": rate, "unit": unit, "cores": cores, "kind": "oracle",
+               "sample": f"{n} position-uniform query rows of {cfg.name} (all groups and heads), {t:.1f} s"}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": higher, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: {cfg.description}", "seqs": len(x.seqs),
+                       "total_q": x.total_q, "total_k": x.total_k,
+                       "l2": "inputs larger than L2; a 258 MB buffer is written between timed steps",
+                       "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roofline,
+            "stages": stages,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
+                     "selected_slots": work["n_slots"], "attended_tokens": work["ntok_total"]},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

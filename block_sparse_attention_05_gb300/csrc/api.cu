@@ -1,0 +1,633 @@
+// api.cu -- the C ABI declared in include/msa.h: argument validation (all on
+// the host, before any CUDA call), workspace layout, TMA tensor maps and the
+// launch sequence of each entry point.  The library never allocates, frees or
+// synchronises (except msa_read_device_status, which is documented to).
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "msa.h"
+
+namespace msa {
+
+namespace {
+std::atomic<int64_t> g_launches{0};
+thread_local cudaEvent_t t_stage_events[2 * MSA_NUM_STAGES];
+thread_local bool t_stage_events_on = false;
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+// Records the caller's stage events (if any) around one stage of a call.
+struct StageScope {
+  int stage;
+  cudaStream_t stream;
+  StageScope(int s, cudaStream_t st) : stage(s), stream(st) {
+    if (t_stage_events_on) cudaEventRecord(t_stage_events[2 * stage], stream);
+  }
+  ~StageScope() {
+    if (t_stage_events_on) cudaEventRecord(t_stage_events[2 * stage + 1], stream);
+  }
+};
+
+constexpr size_t kAlign = 256;
+constexpr int kWindow = 4096;       // queries per scheduling window
+constexpr int kTilesPerChunk = 16;  // Main Branch tiles per work item
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+struct Derived {
+  int S, T, N, hq, hkv, G, d_idx, topk, max_q, max_k, max_nb, qt, qpt, qpc, total_blocks, n_windows;
+  long long max_tiles, n_buckets, max_chunks, n_inc;
+  bool decode;
+  float scale;
+};
+
+struct Layout {
+  size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, count, bstart, bcursor, nchunk, cstart,
+      entries, chunks, scan_tmp, part_o, part_lse, total;
+};
+
+msa_status_t derive(const msa_problem_t* p, Derived& d) {
+  if (!p) return MSA_ERR_INVALID_ARG;
+  if (p->num_seqs < 1 || !p->cu_seqlens_q || !p->cu_seqlens_k) return MSA_ERR_INVALID_ARG;
+  if (p->total_q < 0 || p->total_k < 0 || p->max_seqlen_q < 0 || p->max_seqlen_k < 0) return MSA_ERR_INVALID_ARG;
+  if (p->max_seqlen_q > p->total_q || p->max_seqlen_k > p->total_k) return MSA_ERR_INVALID_ARG;
+  if (p->num_q_heads <= 0 || p->num_kv_heads <= 0 || p->num_q_heads % p->num_kv_heads) return MSA_ERR_INVALID_ARG;
+  if (p->topk <= 0 || p->head_dim <= 0 || p->index_dim <= 0 || p->block_size <= 0) return MSA_ERR_INVALID_ARG;
+  if (!(p->softmax_scale == p->softmax_scale)) return MSA_ERR_INVALID_ARG;  // NaN
+  if (p->head_dim != 128 || p->block_size != 128) return MSA_ERR_UNSUPPORTED;
+  if (p->index_dim != 64 && p->index_dim != 128) return MSA_ERR_UNSUPPORTED;
+  if (p->topk > 16) return MSA_ERR_UNSUPPORTED;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  if (!is_pow2(G) || G < 8 || G > 128) return MSA_ERR_UNSUPPORTED;
+  if (128 % p->num_kv_heads) return MSA_ERR_UNSUPPORTED;
+  d.S = p->num_seqs;
+  d.T = p->total_q;
+  d.N = p->total_k;
+  d.hq = p->num_q_heads;
+  d.hkv = p->num_kv_heads;
+  d.G = G;
+  d.d_idx = p->index_dim;
+  d.topk = p->topk;
+  d.max_q = p->max_seqlen_q;
+  d.max_k = p->max_seqlen_k;
+  d.max_nb = (p->max_seqlen_k + 127) / 128;
+  if (d.max_nb < 1) d.max_nb = 1;
+  d.qt = 128 / d.hkv;
+  d.qpt = 128 / G;
+  d.qpc = d.qpt * kTilesPerChunk;
+  d.total_blocks = (p->total_k + 127) / 128 + d.S;
+  d.n_windows = (p->total_q + kWindow - 1) / kWindow;
+  if (d.n_windows < 1) d.n_windows = 1;
+  d.max_tiles = static_cast<long long>(p->total_q) / d.qt + d.S;
+  d.n_inc = static_cast<long long>(p->total_q) * d.hkv * d.topk;
+  d.n_buckets = static_cast<long long>(d.n_windows) * d.total_blocks * d.hkv;
+  d.max_chunks = (d.n_inc + d.qpc - 1) / d.qpc + d.n_buckets;
+  d.decode = (p->max_seqlen_q <= 1);
+  d.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
+  if (d.n_buckets > 0x7FFFFFFFLL || d.n_inc > (1LL << 31) || p->total_q >= (1 << 26)) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+bool op_uses_index_prefill(msa_op_t op, const Derived& d) {
+  return op == MSA_OP_INDEX_POOL || ((op == MSA_OP_INDEX_TOPK || op == MSA_OP_FORWARD) && !d.decode);
+}
+bool op_uses_decode_index(msa_op_t op, const Derived& d) {
+  return (op == MSA_OP_INDEX_TOPK || op == MSA_OP_FORWARD) && d.decode;
+}
+bool op_uses_prefill_attn(msa_op_t op, const Derived& d) {
+  return op == MSA_OP_SPARSE_ATTN_PREFILL || (op == MSA_OP_FORWARD && !d.decode);
+}
+bool op_uses_decode_attn(msa_op_t op, const Derived& d) {
+  return op == MSA_OP_SPARSE_ATTN_DECODE || (op == MSA_OP_FORWARD && d.decode);
+}
+
+Layout layout(const Derived& d, msa_op_t op) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align_up(bytes);
+    return at;
+  };
+  L.hdr = take(sizeof(WsHeader));
+  L.seq = take(sizeof(SeqInfo) * d.S);
+  L.blk_off = take(sizeof(int32_t) * (d.S + 1));
+  L.tile_base = take(sizeof(int32_t) * (d.S + 1));
+  L.hist = take(sizeof(int32_t) * (d.max_nb + 2));
+  L.cursor = take(sizeof(int32_t) * (d.max_nb + 2));
+  if (op_uses_index_prefill(op, d)) L.tiles = take(sizeof(int2) * d.max_tiles);
+  if (op_uses_decode_index(op, d)) L.pooled = take(sizeof(float) * static_cast<size_t>(d.T) * d.hkv * d.max_nb);
+  if (op_uses_prefill_attn(op, d)) {
+    L.count = take(sizeof(int32_t) * d.n_buckets);
+    L.bstart = take(sizeof(int32_t) * (d.n_buckets + 1));
+    L.bcursor = take(sizeof(int32_t) * d.n_buckets);
+    L.nchunk = take(sizeof(int32_t) * d.n_buckets);
+    L.cstart = take(sizeof(int32_t) * (d.n_buckets + 1));
+    L.entries = take(sizeof(int32_t) * (d.n_inc > 0 ? d.n_inc : 1));
+    L.chunks = take(sizeof(int4) * (d.max_chunks > 0 ? d.max_chunks : 1));
+    L.scan_tmp = take(sizeof(int32_t) * scan_tmp_ints(static_cast<int>(d.n_buckets)));
+  }
+  if (op_uses_prefill_attn(op, d) || op_uses_decode_attn(op, d)) {
+    L.part_o = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.n_inc) * d.G * kHeadDim);
+    L.part_lse = take(sizeof(float) * static_cast<size_t>(d.n_inc) * d.G);
+  }
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- device facts
+struct DeviceFacts {
+  int sms = 0;
+  bool ok = false;
+};
+
+msa_status_t device_facts(DeviceFacts& f) {
+  static std::mutex mu;
+  static DeviceFacts cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev].ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MSA_ERR_DEVICE;
+    if (major != 10 || minor != 3) return MSA_ERR_DEVICE;
+    cache[dev].sms = sms;
+    cache[dev].ok = true;
+  }
+  f = cache[dev];
+  return MSA_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap& m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+              const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides_bytes, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// [rows, cols] row-major, box = 64 columns x box_rows rows
+bool map_2d(CUtensorMap& m, const void* ptr, long long rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  return make_map(m, ptr, 2, dims, strides, box);
+}
+
+// [n, heads, 128] row-major, box = 64 dims x box_heads heads x box_rows rows
+bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_heads, int box_rows) {
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(n > 0 ? n : 1)};
+  cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+  return make_map(m, ptr, 3, dims, strides, box);
+}
+
+// ---------------------------------------------------------------- common prologue
+struct Ctx {
+  Derived d;
+  Layout L;
+  DeviceFacts dev;
+  WsHeader* hdr;
+  SeqInfo* seq;
+  cudaStream_t stream;
+  void* ws;
+};
+
+msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_bytes, msa_stream_t stream,
+                   Ctx& c) {
+  msa_status_t st = derive(p, c.d);
+  if (st != MSA_OK) return st;
+  if ((op == MSA_OP_SPARSE_ATTN_DECODE) && !c.d.decode) return MSA_ERR_INVALID_ARG;
+  // decode batches: exactly one query per sequence
+  if ((op_uses_decode_index(op, c.d) || op_uses_decode_attn(op, c.d)) && c.d.T != c.d.S) return MSA_ERR_INVALID_ARG;
+  if (op_uses_decode_index(op, c.d) && c.d.hkv > 8) return MSA_ERR_UNSUPPORTED;
+  if (op_uses_decode_attn(op, c.d) && c.d.G != 16) return MSA_ERR_UNSUPPORTED;
+  c.L = layout(c.d, op);
+  if (!ws || ws_bytes < c.L.total) return MSA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MSA_ERR_ALIGNMENT;
+  st = device_facts(c.dev);
+  if (st != MSA_OK) return st;
+  c.ws = ws;
+  c.hdr = at<WsHeader>(ws, c.L.hdr);
+  c.seq = at<SeqInfo>(ws, c.L.seq);
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  return MSA_OK;
+}
+
+msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+msa_status_t run_plan(const msa_problem_t* p, Ctx& c, int qt) {
+  StageScope scope(MSA_STAGE_PLAN, c.stream);
+  note_launches(1);
+  if (cudaMemsetAsync(c.hdr, 0, sizeof(WsHeader), c.stream) != cudaSuccess) return MSA_ERR_CUDA;
+  PlanParams pp{};
+  pp.num_seqs = c.d.S;
+  pp.cu_q = p->cu_seqlens_q;
+  pp.cu_k = p->cu_seqlens_k;
+  pp.total_q = c.d.T;
+  pp.total_k = c.d.N;
+  pp.max_q = c.d.max_q;
+  pp.max_k = c.d.max_k;
+  pp.qt = qt;
+  pp.max_nb = c.d.max_nb;
+  pp.seq = c.seq;
+  pp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
+  pp.tile_base = at<int32_t>(c.ws, c.L.tile_base);
+  pp.hist = at<int32_t>(c.ws, c.L.hist);
+  pp.cursor = at<int32_t>(c.ws, c.L.cursor);
+  pp.tiles = qt > 0 ? at<int2>(c.ws, c.L.tiles) : nullptr;
+  pp.hdr = c.hdr;
+  return cuda_status(launch_plan(pp, c.stream));
+}
+
+msa_status_t run_index_prefill(const msa_problem_t* p, Ctx& c, const void* q_idx, const void* k_idx, bool fused,
+                               float* pooled, int64_t pooled_stride, int32_t* idx) {
+  if (c.d.T == 0) return MSA_OK;
+  CUtensorMap tq, tk;
+  if (!map_2d(tq, q_idx, static_cast<long long>(c.d.T) * c.d.hkv, c.d.d_idx, 128) ||
+      !map_2d(tk, k_idx, c.d.N, c.d.d_idx, 128))
+    return MSA_ERR_CUDA;
+  IndexParams ip{};
+  ip.seq = c.seq;
+  ip.tiles = at<int2>(c.ws, c.L.tiles);
+  ip.hdr = c.hdr;
+  ip.hkv = c.d.hkv;
+  ip.d_idx = c.d.d_idx;
+  ip.topk = c.d.topk;
+  ip.qt = c.d.qt;
+  ip.pooled = pooled;
+  ip.pooled_stride = pooled_stride;
+  ip.idx = idx;
+  long long grid = c.d.max_tiles;
+  if (grid > c.dev.sms) grid = c.dev.sms;
+  if (grid < 1) grid = 1;
+  StageScope scope(MSA_STAGE_INDEX, c.stream);
+  return cuda_status(launch_index_score(tq, tk, ip, fused, static_cast<int>(grid), c.stream));
+  (void)p;
+}
+
+msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled, int64_t stride, int32_t* idx) {
+  TopkParams tp{};
+  tp.num_seqs = c.d.S;
+  tp.total_q = c.d.T;
+  tp.hkv = c.d.hkv;
+  tp.topk = c.d.topk;
+  tp.cu_q = p->cu_seqlens_q;
+  tp.seq = c.seq;
+  tp.pooled = pooled;
+  tp.pooled_stride = stride;
+  tp.idx = idx;
+  tp.hdr = c.hdr;
+  StageScope scope(MSA_STAGE_TOPK, c.stream);
+  return cuda_status(launch_topk_pooled(tp, c.d.max_nb, c.stream));
+}
+
+msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx, const void* k_idx, int32_t* idx) {
+  if (c.d.T == 0) return MSA_OK;
+  CUtensorMap tk;
+  if (!map_2d(tk, k_idx, c.d.N, c.d.d_idx, 128)) return MSA_ERR_CUDA;
+  float* pooled = at<float>(c.ws, c.L.pooled);
+  DecodeScanParams sp{};
+  sp.num_seqs = c.d.S;
+  sp.hkv = c.d.hkv;
+  sp.d_idx = c.d.d_idx;
+  sp.seq = c.seq;
+  sp.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  sp.pooled = pooled;
+  sp.pooled_stride = c.d.max_nb;
+  // about 4 work units per SM in total, at least 16 blocks each
+  long long want_units = 4LL * c.dev.sms;
+  int ups = static_cast<int>((want_units + c.d.S - 1) / c.d.S);
+  if (ups < 1) ups = 1;
+  int bpu = (c.d.max_nb + ups - 1) / ups;
+  if (bpu < 16) bpu = 16;
+  ups = (c.d.max_nb + bpu - 1) / bpu;
+  sp.units_per_seq = ups;
+  sp.blocks_per_unit = bpu;
+  sp.hdr = c.hdr;
+  long long units = static_cast<long long>(c.d.S) * ups;
+  int grid = static_cast<int>(units < c.dev.sms ? units : c.dev.sms);
+  if (grid < 1) grid = 1;
+  msa_status_t st;
+  {
+    StageScope scope(MSA_STAGE_INDEX, c.stream);
+    st = cuda_status(launch_decode_scan(tk, sp, grid, c.stream));
+  }
+  if (st != MSA_OK) return st;
+  return run_topk_pooled(p, c, pooled, c.d.max_nb, idx);
+}
+
+PartialBuffers partials(Ctx& c) {
+  PartialBuffers pb;
+  pb.o = at<__nv_bfloat16>(c.ws, c.L.part_o);
+  pb.lse = at<float>(c.ws, c.L.part_lse);
+  return pb;
+}
+
+msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, void* o, float* lse) {
+  CombineParams cp{};
+  cp.total_q = c.d.T;
+  cp.hq = c.d.hq;
+  cp.hkv = c.d.hkv;
+  cp.group = c.d.G;
+  cp.topk = c.d.topk;
+  cp.num_seqs = c.d.S;
+  cp.cu_q = p->cu_seqlens_q;
+  cp.seq = c.seq;
+  cp.idx = idx;
+  cp.part = partials(c);
+  cp.o = static_cast<__nv_bfloat16*>(o);
+  cp.lse = lse;
+  cp.hdr = c.hdr;
+  StageScope scope(MSA_STAGE_COMBINE, c.stream);
+  return cuda_status(launch_combine(cp, c.stream));
+}
+
+msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, const void* k, const void* v,
+                              const int32_t* idx, void* o, float* lse) {
+  if (c.d.T == 0) return MSA_OK;
+  ScheduleParams sp{};
+  sp.num_seqs = c.d.S;
+  sp.total_q = c.d.T;
+  sp.hkv = c.d.hkv;
+  sp.topk = c.d.topk;
+  sp.window = kWindow;
+  sp.total_blocks = c.d.total_blocks;
+  sp.n_windows = c.d.n_windows;
+  sp.qpc = c.d.qpc;
+  sp.cu_q = p->cu_seqlens_q;
+  sp.seq = c.seq;
+  sp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
+  sp.idx = idx;
+  sp.count = at<int32_t>(c.ws, c.L.count);
+  sp.bucket_start = at<int32_t>(c.ws, c.L.bstart);
+  sp.cursor = at<int32_t>(c.ws, c.L.bcursor);
+  sp.nchunk = at<int32_t>(c.ws, c.L.nchunk);
+  sp.chunk_start = at<int32_t>(c.ws, c.L.cstart);
+  sp.entries = at<int32_t>(c.ws, c.L.entries);
+  sp.chunks = at<int4>(c.ws, c.L.chunks);
+  sp.scan_tmp = at<int32_t>(c.ws, c.L.scan_tmp);
+  sp.hdr = c.hdr;
+  sp.n_buckets = c.d.n_buckets;
+  msa_status_t st;
+  {
+    StageScope scope(MSA_STAGE_SCHEDULE, c.stream);
+    st = cuda_status(launch_schedule(sp, c.stream));
+  }
+  if (st != MSA_OK) return st;
+
+  CUtensorMap tq, tk, tv;
+  if (!map_3d(tq, q, c.d.T, c.d.hq, c.d.G, 1) || !map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) ||
+      !map_3d(tv, v, c.d.N, c.d.hkv, 1, 128))
+    return MSA_ERR_CUDA;
+  AttnParams ap{};
+  ap.seq = c.seq;
+  ap.blk_off = at<int32_t>(c.ws, c.L.blk_off);
+  ap.cu_q = p->cu_seqlens_q;
+  ap.chunks = sp.chunks;
+  ap.entries = sp.entries;
+  ap.part = partials(c);
+  ap.hdr = c.hdr;
+  ap.num_seqs = c.d.S;
+  ap.hkv = c.d.hkv;
+  ap.group = c.d.G;
+  ap.topk = c.d.topk;
+  ap.total_blocks = c.d.total_blocks;
+  ap.qpt = c.d.qpt;
+  ap.scale_log2 = c.d.scale * 1.4426950408889634f;
+  {
+    StageScope scope(MSA_STAGE_ATTN, c.stream);
+    st = cuda_status(launch_sparse_attn(tq, tk, tv, ap, c.dev.sms, c.stream));
+  }
+  if (st != MSA_OK) return st;
+  return run_combine(p, c, idx, o, lse);
+}
+
+msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, const void* k, const void* v,
+                             const int32_t* idx, void* o, float* lse) {
+  if (c.d.T == 0) return MSA_OK;
+  CUtensorMap tk, tv;
+  if (!map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) || !map_3d(tv, v, c.d.N, c.d.hkv, 1, 128)) return MSA_ERR_CUDA;
+  DecodeAttnParams dp{};
+  dp.num_seqs = c.d.S;
+  dp.hkv = c.d.hkv;
+  dp.group = c.d.G;
+  dp.topk = c.d.topk;
+  dp.seq = c.seq;
+  dp.q = static_cast<const __nv_bfloat16*>(q);
+  dp.idx = idx;
+  dp.part = partials(c);
+  dp.scale_log2 = c.d.scale * 1.4426950408889634f;
+  dp.hdr = c.hdr;
+  msa_status_t st;
+  {
+    StageScope scope(MSA_STAGE_ATTN, c.stream);
+    st = cuda_status(launch_decode_attn(tk, tv, dp, c.stream));
+  }
+  if (st != MSA_OK) return st;
+  return run_combine(p, c, idx, o, lse);
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+int32_t msa_abi_version(void) { return 1; }
+
+msa_status_t msa_set_stage_events(void* const* events) {
+  if (!events) {
+    t_stage_events_on = false;
+    return MSA_OK;
+  }
+  for (int i = 0; i < 2 * MSA_NUM_STAGES; ++i) {
+    if (!events[i]) return MSA_ERR_INVALID_ARG;
+    t_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  t_stage_events_on = true;
+  return MSA_OK;
+}
+
+int64_t msa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case MSA_ERR_ALIGNMENT: return "misaligned pointer";
+    case MSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MSA_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case MSA_ERR_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+msa_status_t msa_workspace_size(const msa_problem_t* problem, msa_op_t op, size_t* bytes) {
+  if (!bytes) return MSA_ERR_INVALID_ARG;
+  if (op < MSA_OP_INDEX_POOL || op > MSA_OP_TOPK_POOLED) return MSA_ERR_INVALID_ARG;
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  *bytes = layout(d, op).total;
+  return MSA_OK;
+}
+
+msa_status_t msa_index_pool(const msa_problem_t* problem, const void* q_idx, const void* k_idx, float* pooled,
+                            int64_t pooled_stride, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!q_idx || !k_idx || !pooled) return MSA_ERR_INVALID_ARG;
+  if (pooled_stride < d.max_nb) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(pooled)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_INDEX_POOL, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  return run_index_prefill(problem, c, q_idx, k_idx, false, pooled, pooled_stride, nullptr);
+}
+
+msa_status_t msa_topk_pooled(const msa_problem_t* problem, const float* pooled, int64_t pooled_stride,
+                             int32_t* idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!pooled || !idx) return MSA_ERR_INVALID_ARG;
+  if (pooled_stride < d.max_nb) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(pooled) || !aligned16(idx)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_TOPK_POOLED, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  if (c.d.T == 0) return MSA_OK;
+  return run_topk_pooled(problem, c, pooled, pooled_stride, idx);
+}
+
+msa_status_t msa_index_topk(const msa_problem_t* problem, const void* q_idx, const void* k_idx, int32_t* idx,
+                            void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!q_idx || !k_idx || !idx) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(idx)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_INDEX_TOPK, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if (c.d.decode) {
+    if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+    return run_index_decode(problem, c, q_idx, k_idx, idx);
+  }
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  return run_index_prefill(problem, c, q_idx, k_idx, true, nullptr, 0, idx);
+}
+
+static msa_status_t check_attn_args(const void* q, const void* k, const void* v, const int32_t* idx,
+                                    const void* o, const float* lse) {
+  if (!q || !k || !v || !idx || !o || !lse) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(idx) || !aligned16(o) || !aligned16(lse))
+    return MSA_ERR_ALIGNMENT;
+  return MSA_OK;
+}
+
+msa_status_t msa_sparse_attn_prefill(const msa_problem_t* problem, const void* q, const void* k, const void* v,
+                                     const int32_t* idx, void* o, float* lse, void* workspace,
+                                     size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k, v, idx, o, lse)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_SPARSE_ATTN_PREFILL, workspace, workspace_bytes, stream, c)) != MSA_OK)
+    return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  return run_attn_prefill(problem, c, q, k, v, idx, o, lse);
+}
+
+msa_status_t msa_sparse_attn_decode(const msa_problem_t* problem, const void* q, const void* k, const void* v,
+                                    const int32_t* idx, void* o, float* lse, void* workspace,
+                                    size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k, v, idx, o, lse)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_SPARSE_ATTN_DECODE, workspace, workspace_bytes, stream, c)) != MSA_OK)
+    return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  return run_attn_decode(problem, c, q, k, v, idx, o, lse);
+}
+
+msa_status_t msa_forward(const msa_problem_t* problem, const void* q, const void* k, const void* v,
+                         const void* q_idx, const void* k_idx, int32_t* idx, void* o, float* lse,
+                         void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k, v, idx, o, lse)) != MSA_OK) return st;
+  if (!q_idx || !k_idx) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_FORWARD, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if (c.d.decode) {
+    if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+    if ((st = run_index_decode(problem, c, q_idx, k_idx, idx)) != MSA_OK) return st;
+    return run_attn_decode(problem, c, q, k, v, idx, o, lse);
+  }
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  if ((st = run_index_prefill(problem, c, q_idx, k_idx, true, nullptr, 0, idx)) != MSA_OK) return st;
+  return run_attn_prefill(problem, c, q, k, v, idx, o, lse);
+}
+
+msa_status_t msa_read_device_status(const void* workspace, uint32_t* flags, msa_stream_t stream) {
+  if (!workspace || !flags) return MSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return MSA_ERR_ALIGNMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MSA_ERR_CUDA;
+  *flags = v;
+  return MSA_OK;
+}
+
+}  // extern "C"

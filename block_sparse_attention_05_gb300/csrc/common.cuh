@@ -1,0 +1,293 @@
+// common.cuh -- device primitives shared by the sm_103a kernels: bounded
+// mbarrier waits, TMA tile loads, tcgen05 (UMMA) issue / commit / TMEM loads,
+// shared-memory matrix descriptors, and the top-k key order.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace msa {
+
+// ----------------------------------------------------------------------------
+// Workspace header: first 256 bytes of every workspace.
+// ----------------------------------------------------------------------------
+enum : uint32_t { kFlagTimeout = 1u, kFlagBadSeqlens = 2u };
+
+struct WsHeader {
+  uint32_t status;          // MSA_DEVICE_* bits
+  uint32_t n_qtiles;        // index-scoring work items
+  uint32_t n_chunks;        // sparse-attention work items
+  uint32_t n_entries;       // (query, group, slot) incidences
+  uint32_t counter[8];      // persistent-kernel claim counters
+  uint32_t timeout_site;    // where a wait gave up (debug)
+};
+
+// Per-sequence facts derived once from cu_seqlens.
+struct SeqInfo {
+  int32_t q_start, q_len, k_start, kv_len;
+};
+
+constexpr int kBlock = 128;       // key block size (tokens)
+constexpr int kHeadDim = 128;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
+
+// ----------------------------------------------------------------------------
+// mbarrier
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) when *abort becomes nonzero or after kWaitLimitNs; the
+// caller then records the failure and leaves its loop.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+// Records a failed wait: sets the CTA abort flag and the workspace status.
+__device__ __forceinline__ void report_timeout(volatile int* abort_flag, WsHeader* hdr, uint32_t site) {
+  *abort_flag = 1;
+  atomicOr(&hdr->status, kFlagTimeout);
+  atomicExch(&hdr->timeout_site, site);
+}
+
+// ----------------------------------------------------------------------------
+// TMA (tiled bulk tensor copies global -> shared, completion on an mbarrier)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy (tensor core / TMA) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
+// tcgen05: TMEM allocation, MMA issue, commit, TMEM -> register loads
+// ----------------------------------------------------------------------------
+// Whole warp.  Writes the allocated TMEM base address to *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Each thread of the warp reads 32 consecutive 32-bit columns of its TMEM
+// lane (lane = (warp % 4) * 32 + laneid, encoded in taddr bits 31..16).
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format) for a tile stored in the
+// 128-byte swizzled layout that TMA writes with CU_TENSOR_MAP_SWIZZLE_128B:
+// rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset).
+// For K-major operands the leading byte offset is unused; for MN-major
+// operands it is the distance between 64-element column chunks.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N tile.
+// b_mn_major: B stored with N contiguous (else K contiguous).  A is K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4)                                  // D format: f32
+         | (1u << 7)                                // A format: bf16
+         | (1u << 10)                               // B format: bf16
+         | ((b_mn_major ? 1u : 0u) << 16)           // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// ----------------------------------------------------------------------------
+// Top-k key order: larger key = better block.  Score descending first, then
+// block index ascending.  +0 and -0 map to the same key (they compare equal).
+// Key 0 is "empty" (below every real key).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t topk_key(float score, int block) {
+  float s = (score == 0.0f) ? 0.0f : score;
+  uint32_t u = __float_as_uint(s);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(block));
+}
+__device__ __forceinline__ int topk_key_block(uint64_t key) {
+  return static_cast<int>(~static_cast<uint32_t>(key & 0xFFFFFFFFu));
+}
+
+// Sorted (descending) register list of the CAP best keys seen so far.
+// Keys must be distinct (they embed the block index), so the order is total.
+template <int CAP>
+struct TopkList {
+  uint64_t k[CAP];
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int j = 0; j < CAP; ++j) k[j] = 0ull;
+  }
+  __device__ __forceinline__ void insert(uint64_t x) {
+    if (x > k[CAP - 1]) {
+      k[CAP - 1] = x;
+#pragma unroll
+      for (int j = CAP - 1; j > 0; --j) {
+        const uint64_t a = k[j - 1], b = k[j];
+        const bool sw = b > a;
+        k[j - 1] = sw ? b : a;
+        k[j] = sw ? a : b;
+      }
+    }
+  }
+  // Removes the head (the best key).
+  __device__ __forceinline__ void pop() {
+#pragma unroll
+    for (int j = 0; j + 1 < CAP; ++j) k[j] = k[j + 1];
+    k[CAP - 1] = 0ull;
+  }
+};
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const uint64_t y = __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    x = y > x ? y : x;
+  }
+  return x;
+}
+
+// Writes the ascending selection {chosen blocks} U {local}, -1 padded, to
+// out[0..k).  chosen[] holds up to CAP block indices (-1 = none), all < local.
+template <int CAP>
+__device__ __forceinline__ void write_selection(int32_t* out, int k, const int (&chosen)[CAP], int local) {
+  int v[CAP + 1];
+#pragma unroll
+  for (int j = 0; j < CAP; ++j) v[j] = chosen[j] < 0 ? 0x7FFFFFFF : chosen[j];
+  v[CAP] = local;
+  // odd-even transposition sort, ascending
+#pragma unroll
+  for (int pass = 0; pass < CAP + 1; ++pass) {
+#pragma unroll
+    for (int j = (pass & 1); j + 1 < CAP + 1; j += 2) {
+      const int a = v[j], b = v[j + 1];
+      v[j] = a < b ? a : b;
+      v[j + 1] = a < b ? b : a;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < CAP + 1; ++j)
+    if (j < k) out[j] = (v[j] == 0x7FFFFFFF) ? -1 : v[j];
+}
+
+// Largest s in [0, num_seqs) with cu[s] <= row (the sequence owning `row`;
+// empty sequences are skipped because they share their prefix value).
+__device__ __forceinline__ int find_seq(const int32_t* cu, int num_seqs, int row) {
+  int lo = 0, hi = num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+}  // namespace msa

@@ -1,0 +1,444 @@
+// decode.cu -- decode batches (one new query per sequence).
+//
+// Index scan: for each sequence, the index scores of its single query against
+// every cached index key, max-pooled per 128-token block ("MiniMax Sparse
+// Attention: let each query pick its own blocks", section "The mechanism,
+// precisely"; the groundtruth.day article on the llama.cpp merge notes that
+// selection runs in decode too and that decode then reads about 2,048 KV
+// tokens whatever the context length).  The scan streams K_idx once and is
+// bound by HBM bandwidth, so it is built for bytes in flight: a persistent
+// grid, a TMA producer keeping a 6-stage ring of 128-key tiles full, and four
+// consumer warps.  The 4 group queries against 16 keys are one small
+// mma.sync (m16n8k16: keys x d_idx times d_idx x groups) -- it keeps the
+// instruction count per byte low so the issue slots never limit the stream.
+//
+// Attention: one CTA per (sequence, group, selected block): the block's K and
+// V by TMA, the group's 16 heads as the M = 16 rows of mma.sync tiles, four
+// warps over 32 keys each merged in shared memory, then a normalised partial
+// output and its LSE per slot.  combine.cu merges the slots (split-KV with a
+// log-sum-exp combine).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kScanStages = 6;
+constexpr int kScanConsumers = 4;
+constexpr int kScanThreads = 32 * (kScanConsumers + 1);
+constexpr int kScanTile = 128 * 128 * 2;  // 128 keys x up to 128 dims, bf16
+constexpr size_t kScanSmemBytes = 1024 + kScanStages * kScanTile + 256;
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Byte offset of (row, 8-element chunk) in a TMA 128-byte-swizzled tile whose
+// 64-column halves are 16 KB apart.
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+  return (chunk >> 3) * 16384 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+struct ScanSmem {
+  uint64_t full[kScanStages], empty[kScanStages];
+  int abort_flag;
+};
+
+// The work of one CTA: units u = blockIdx.x + j * gridDim.x; unit u covers
+// blocks [c * bpu, min((c + 1) * bpu, nb)) of sequence u / ups.
+struct ScanCursor {
+  int u, b, b_end, s;
+};
+
+__device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor& c) {
+  while (true) {
+    if (c.b < c.b_end) return true;
+    c.u += gridDim.x;
+    if (c.u >= p.num_seqs * p.units_per_seq) return false;
+    c.s = c.u / p.units_per_seq;
+    const int unit = c.u % p.units_per_seq;
+    const SeqInfo si = p.seq[c.s];
+    const int nb = (si.kv_len + kBlock - 1) / kBlock;
+    c.b = unit * p.blocks_per_unit;
+    c.b_end = min(nb, c.b + p.blocks_per_unit);
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kScanThreads, 1)
+    decode_scan_kernel(const __grid_constant__ CUtensorMap tm_k, DecodeScanParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  WsHeader* hdr = p.hdr;
+  if (hdr->status & kFlagBadSeqlens) return;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  ScanSmem& sm = *reinterpret_cast<ScanSmem*>(base + kScanStages * kScanTile);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kchunks = p.d_idx >> 6;
+  const uint32_t tile_tx = 128u * p.d_idx * 2u;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kScanStages; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+  }
+  __syncthreads();
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == kScanConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0};
+      uint32_t it = 0;
+      while (scan_next(p, c)) {
+        const int st = it % kScanStages;
+        if (it >= kScanStages && !mbar_wait(&sm.empty[st], ((it / kScanStages) - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 301);
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.full[st], tile_tx);
+        const int row = p.seq[c.s].k_start + c.b * kBlock;
+        for (int ch = 0; ch < kchunks; ++ch)
+          tma_load_2d(base + st * kScanTile + ch * 16384, &tm_k, &sm.full[st], ch * 64, row);
+        ++c.b;
+        ++it;
+      }
+      for (int s = 0; s < kScanStages; ++s)
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t last = ((it - 1 - s) / kScanStages) * kScanStages + s;
+          mbar_wait(&sm.full[s], (last / kScanStages) & 1, nullptr);
+        }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0};
+    uint32_t it = 0;
+    int cur_s = -1;
+    uint32_t qf[8][2];
+    int pos = 0;
+    const int gq = lane >> 2;                 // B-fragment column = group
+    while (scan_next(p, c)) {
+      const int st = it % kScanStages;
+      const int b = c.b;
+      ++c.b;
+      const uint32_t my = it;
+      ++it;
+      if ((my % kScanConsumers) != static_cast<uint32_t>(warp)) continue;
+      if (c.s != cur_s) {
+        cur_s = c.s;
+        const SeqInfo si = p.seq[cur_s];
+        pos = si.kv_len - 1;
+        const __nv_bfloat16* qrow = p.q_idx + (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          qf[ks][0] = qf[ks][1] = 0u;
+          if (gq < p.hkv && ks * 16 < p.d_idx) {
+            const int d0 = ks * 16 + (lane & 3) * 2;
+            qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + d0);
+            qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + d0 + 8);
+          }
+        }
+      }
+      if (!mbar_wait(&sm.full[st], (my / kScanStages) & 1, abort_flag)) {
+        report_timeout(abort_flag, hdr, 311);
+        break;
+      }
+      const uint32_t tile = smem_u32(base + st * kScanTile);
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+      const int key_base = b * kBlock;
+      const int mtx = lane >> 3, mr = lane & 7;
+#pragma unroll
+      for (int sub = 0; sub < 8; ++sub) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int arow = sub * 16 + (mtx & 1) * 8 + mr;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          if (ks * 16 < p.d_idx) {
+            uint32_t a[4];
+            ldmatrix_x4(tile + sw128_off(arow, ks * 2 + (mtx >> 1)), a[0], a[1], a[2], a[3]);
+            mma_16816(acc, a, qf[ks][0], qf[ks][1]);
+          }
+        }
+        const int k0 = key_base + sub * 16 + (lane >> 2);
+        if (k0 <= pos) {
+          mx0 = fmaxf(mx0, acc[0]);
+          mx1 = fmaxf(mx1, acc[1]);
+        }
+        if (k0 + 8 <= pos) {
+          mx0 = fmaxf(mx0, acc[2]);
+          mx1 = fmaxf(mx1, acc[3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[st]);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+      }
+      if (lane < 4) {
+        const int g0 = lane * 2;
+        float* out = p.pooled + static_cast<int64_t>(cur_s) * p.hkv * p.pooled_stride + b;
+        if (g0 < p.hkv) out[static_cast<int64_t>(g0) * p.pooled_stride] = mx0;
+        if (g0 + 1 < p.hkv) out[static_cast<int64_t>(g0 + 1) * p.pooled_stride] = mx1;
+      }
+    }
+  }
+  __syncthreads();
+}
+
+size_t decode_scan_smem_bytes() { return kScanSmemBytes; }
+
+cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kScanSmemBytes));
+  if (e != cudaSuccess) return e;
+  decode_scan_kernel<<<grid, kScanThreads, kScanSmemBytes, stream>>>(tk, p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// decode attention
+// ----------------------------------------------------------------------------
+namespace {
+
+constexpr int kDecThreads = 128;
+constexpr size_t kDecSmemBytes = 1024 + 2 * 32768 + 4 * 16 * 2 * sizeof(float) + 64;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kDecThreads)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       DecodeAttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  WsHeader* hdr = p.hdr;
+  if (hdr->status & kFlagBadSeqlens) return;
+  const int bid = blockIdx.x;
+  const int slot = bid % p.topk;
+  const int g = (bid / p.topk) % p.hkv;
+  const int s = bid / (p.topk * p.hkv);
+  const int64_t sel = (static_cast<int64_t>(s) * p.hkv + g) * p.topk + slot;
+  const int b = p.idx[sel];
+  const SeqInfo si = p.seq[s];
+  const int pos = si.kv_len - 1;
+  if (b < 0 || b > (pos >> 7)) return;  // empty slot: no partial, the combine skips it
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ks = base;            // K tile, 2 x 16 KB halves
+  uint8_t* vs = base + 32768;    // V tile
+  float* red = reinterpret_cast<float*>(base + 65536);          // [4 warps][16 heads][m, l]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 4 * 16 * 2);
+  int* abort_flag = reinterpret_cast<int*>(bar + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int krow = si.k_start + b * kBlock;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, 65536);
+    tma_load_3d(ks, &tm_k, bar, 0, g, krow);
+    tma_load_3d(ks + 16384, &tm_k, bar, 64, g, krow);
+    tma_load_3d(vs, &tm_v, bar, 0, g, krow);
+    tma_load_3d(vs + 16384, &tm_v, bar, 64, g, krow);
+  }
+  // Q fragments (16 heads x 128 dims) straight from global memory
+  const int G = p.group;  // 16
+  const __nv_bfloat16* qg = p.q + (static_cast<int64_t>(s) * p.hkv * G + g * G) * kHeadDim;
+  uint32_t qa[8][4];
+  {
+    const int h0 = lane >> 2, d0 = (lane & 3) * 2;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      qa[k][0] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0);
+      qa[k][1] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0);
+      qa[k][2] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0 + 8);
+      qa[k][3] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0 + 8);
+    }
+  }
+  __syncthreads();
+  if (!mbar_wait(bar, 0, abort_flag)) {
+    report_timeout(abort_flag, hdr, 321);
+  }
+  __syncthreads();
+  if (*reinterpret_cast<volatile int*>(abort_flag)) {
+    // the copies may still be in flight: wait once more (bounded) before leaving
+    mbar_wait(bar, 0, nullptr);
+    return;
+  }
+  const uint32_t kt = smem_u32(ks), vt = smem_u32(vs);
+  const int mtx = lane >> 3, mr = lane & 7;
+
+  // S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
+  float sacc[4][4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+#pragma unroll
+    for (int ntp = 0; ntp < 2; ++ntp) {
+      // matrices: (keys nt, d lo), (keys nt, d hi), (keys nt+1, d lo), (keys nt+1, d hi)
+      const int key = warp * 32 + (ntp * 2 + (mtx >> 1)) * 8 + mr;
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(kt + sw128_off(key, k * 2 + (mtx & 1)), b0, b1, b2, b3);
+      mma_16816(sacc[ntp * 2], qa[k], b0, b1);
+      mma_16816(sacc[ntp * 2 + 1], qa[k], b2, b3);
+    }
+  }
+  // masked, scaled logits; per-head max and sum over this warp's keys
+  const int lim = pos - b * kBlock;
+  float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int c0 = warp * 32 + nt * 8 + (lane & 3) * 2;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = c0 + (j & 1);
+      const float x = (c <= lim) ? sacc[nt][j] * p.scale_log2 : -INFINITY;
+      sacc[nt][j] = x;
+    }
+    m0 = fmaxf(m0, fmaxf(sacc[nt][0], sacc[nt][1]));
+    m1 = fmaxf(m1, fmaxf(sacc[nt][2], sacc[nt][3]));
+  }
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, o));
+  }
+  const float r0 = (m0 == -INFINITY) ? 0.f : m0, r1 = (m1 == -INFINITY) ? 0.f : m1;
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    sacc[nt][0] = exp2f(sacc[nt][0] - r0);
+    sacc[nt][1] = exp2f(sacc[nt][1] - r0);
+    sacc[nt][2] = exp2f(sacc[nt][2] - r1);
+    sacc[nt][3] = exp2f(sacc[nt][3] - r1);
+    l0 += sacc[nt][0] + sacc[nt][1];
+    l1 += sacc[nt][2] + sacc[nt][3];
+  }
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+  }
+  // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
+  float oacc[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) oacc[nt][j] = 0.f;
+#pragma unroll
+  for (int kj = 0; kj < 2; ++kj) {
+    uint32_t pa[4];
+    pa[0] = pack_bf16x2(sacc[2 * kj][0], sacc[2 * kj][1]);
+    pa[1] = pack_bf16x2(sacc[2 * kj][2], sacc[2 * kj][3]);
+    pa[2] = pack_bf16x2(sacc[2 * kj + 1][0], sacc[2 * kj + 1][1]);
+    pa[3] = pack_bf16x2(sacc[2 * kj + 1][2], sacc[2 * kj + 1][3]);
+#pragma unroll
+    for (int dp = 0; dp < 8; ++dp) {
+      // matrices: (keys lo, d 16dp..+7), (keys hi, same d), (keys lo, d +8..15), (keys hi, d +8..15)
+      const int key = warp * 32 + kj * 16 + (mtx & 1) * 8 + mr;
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(vt + sw128_off(key, dp * 2 + (mtx >> 1)), b0, b1, b2, b3);
+      mma_16816(oacc[2 * dp], pa, b0, b1);
+      mma_16816(oacc[2 * dp + 1], pa, b2, b3);
+    }
+  }
+  // merge the four warps: rescale to the common max, sum, normalise
+  const int h0 = lane >> 2;
+  if ((lane & 3) == 0) {
+    red[(warp * 16 + h0) * 2 + 0] = m0;
+    red[(warp * 16 + h0) * 2 + 1] = l0;
+    red[(warp * 16 + h0 + 8) * 2 + 0] = m1;
+    red[(warp * 16 + h0 + 8) * 2 + 1] = l1;
+  }
+  __syncthreads();  // all warps are done with K and V from here on
+  float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    M0 = fmaxf(M0, red[(w * 16 + h0) * 2]);
+    M1 = fmaxf(M1, red[(w * 16 + h0 + 8) * 2]);
+  }
+  const float R0 = (M0 == -INFINITY) ? 0.f : M0, R1 = (M1 == -INFINITY) ? 0.f : M1;
+  float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float mw0 = red[(w * 16 + h0) * 2], mw1 = red[(w * 16 + h0 + 8) * 2];
+    L0 += (mw0 == -INFINITY) ? 0.f : red[(w * 16 + h0) * 2 + 1] * exp2f(mw0 - R0);
+    L1 += (mw1 == -INFINITY) ? 0.f : red[(w * 16 + h0 + 8) * 2 + 1] * exp2f(mw1 - R1);
+  }
+  const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0;
+  const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1;
+  // sum of the four warps' scaled partial outputs, through shared memory (reuses the K tile)
+  float* osum = reinterpret_cast<float*>(base);  // [16 heads][128] fp32 = 8 KB
+  for (int i = threadIdx.x; i < 16 * 128; i += kDecThreads) osum[i] = 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) {
+    const int d = nt * 8 + (lane & 3) * 2;
+    atomicAdd(&osum[h0 * 128 + d], oacc[nt][0] * f0);
+    atomicAdd(&osum[h0 * 128 + d + 1], oacc[nt][1] * f0);
+    atomicAdd(&osum[(h0 + 8) * 128 + d], oacc[nt][2] * f1);
+    atomicAdd(&osum[(h0 + 8) * 128 + d + 1], oacc[nt][3] * f1);
+  }
+  __syncthreads();
+  __nv_bfloat16* out = p.part.o + sel * G * kHeadDim;
+  for (int i = threadIdx.x * 2; i < 16 * 128; i += kDecThreads * 2)
+    *reinterpret_cast<uint32_t*>(out + i) = pack_bf16x2(osum[i], osum[i + 1]);
+  if (threadIdx.x < 16) {
+    const int h = threadIdx.x;
+    float M = -INFINITY;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * 2]);
+    float L = 0.f;
+    for (int w = 0; w < 4; ++w) {
+      const float mw = red[(w * 16 + h) * 2];
+      if (mw != -INFINITY) L += red[(w * 16 + h) * 2 + 1] * exp2f(mw - M);
+    }
+    p.part.lse[sel * G + h] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+  }
+}
+
+size_t decode_attn_smem_bytes() { return kDecSmemBytes; }
+
+cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeAttnParams& p,
+                               cudaStream_t stream) {
+  const long long grid = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
+  if (grid == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kDecSmemBytes));
+  if (e != cudaSuccess) return e;
+  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads, kDecSmemBytes, stream>>>(tk, tv, p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,330 @@
+// index_score.cu -- Index Branch scoring on the tensor cores.
+//
+// "MiniMax Sparse Attention: let each query pick its own blocks", section
+// "The mechanism, precisely" (first bullet) and Figure 1: token scores
+// Q_idx . K_idx^T, max-pooled over 128-token key blocks, then top-k blocks
+// with the query's own (local) block always kept.
+//
+// Work item: a tile of 128 rows of Q_idx viewed as [T * Hkv, d_idx]; with
+// Hkv = 4 that is 32 consecutive queries x 4 groups, so one K_idx tile (the
+// shared index-key head) serves every group at once.  The CTA walks the key
+// blocks 0..L_max of the tile in order; each block is one 128 x 128 x d_idx
+// tcgen05 MMA (bf16 in, fp32 accumulate in TMEM, double-buffered), and the
+// epilogue warps reduce each accumulator row (one TMEM lane per thread) to the
+// block's pooled score with the causal limit of that row.  In the fused mode
+// the epilogue keeps a running top-(k-1) of the non-local blocks per row in
+// registers and writes the final selection; otherwise it writes pooled scores.
+//
+// Warp roles (256 threads): warp 0 = TMA producer and work claiming, warp 1 =
+// MMA issuer, warp 2 = TMEM allocator, warp 3 idle, warps 4..7 = epilogue.
+// Work items are claimed dynamically (atomic counter) from a list sorted by
+// descending cost, so the persistent grid balances itself.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+
+namespace {
+
+constexpr int kIdxStagesK = 4;            // K_idx ring depth
+constexpr int kTileBytes = 128 * 128 * 2; // one 128-row tile of 128 bf16 columns
+constexpr int kIdxThreads = 256;
+
+struct IdxSmem {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kIdxStagesK], k_empty[kIdxStagesK];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t work_full[2], work_empty[2];
+  uint64_t mma_done;
+  int work[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t kIdxSmemBytes = 1024 /*align slack*/ + (2 + kIdxStagesK) * kTileBytes + sizeof(IdxSmem);
+
+__device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt, int& nq, int& lmax) {
+  nq = min(qt, si.q_len - t0);
+  const int last_pos = si.kv_len - si.q_len + t0 + nq - 1;
+  lmax = last_pos >> 7;
+}
+
+}  // namespace
+
+template <int CAP, bool FUSED>
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       IndexParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  WsHeader* hdr = p.hdr;
+  if (hdr->status & kFlagBadSeqlens) return;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_buf = base;                          // 2 tiles
+  uint8_t* k_buf = base + 2 * kTileBytes;         // kIdxStagesK tiles
+  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(base + (2 + kIdxStagesK) * kTileBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tiles = static_cast<int>(hdr->n_qtiles);
+  const int kchunks = p.d_idx >> 6;                // 64-column chunks per row
+  const int ksteps = p.d_idx >> 4;                 // UMMA K = 16 steps
+  const uint32_t tile_tx = 128u * p.d_idx * 2u;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1);
+      mbar_init(&sm.acc_full[i], 1);
+      mbar_init(&sm.acc_empty[i], 128);
+      mbar_init(&sm.work_full[i], 1);
+      mbar_init(&sm.work_empty[i], 5);
+    }
+    for (int i = 0; i < kIdxStagesK; ++i) {
+      mbar_init(&sm.k_full[i], 1);
+      mbar_init(&sm.k_empty[i], 1);
+    }
+    mbar_init(&sm.mma_done, 1);
+    sm.abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 2) {
+    tmem_alloc(&sm.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t q_iter = 0, k_iter = 0;
+      for (uint32_t w = 0;; ++w) {
+        const int slot = w & 1;
+        if (w >= 2 && !mbar_wait(&sm.work_empty[slot], ((w >> 1) - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 101);
+          break;
+        }
+        const int u = static_cast<int>(atomicAdd(&hdr->counter[0], 1u));
+        const int item = (u < n_tiles && !*abort_flag) ? u : -1;
+        sm.work[slot] = item;
+        mbar_arrive(&sm.work_full[slot]);
+        if (item < 0) break;
+        const int2 tile = p.tiles[item];
+        const SeqInfo si = p.seq[tile.x];
+        int nq, lmax;
+        tile_geometry(si, tile.y, p.qt, nq, lmax);
+        const int row0 = (si.q_start + tile.y) * p.hkv;
+        const int qb = q_iter & 1;
+        if (q_iter >= 2 && !mbar_wait(&sm.q_empty[qb], ((q_iter >> 1) - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 102);
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.q_full[qb], tile_tx);
+        for (int c = 0; c < kchunks; ++c)
+          tma_load_2d(q_buf + qb * kTileBytes + c * 16384, &tm_q, &sm.q_full[qb], c * 64, row0);
+        ++q_iter;
+        bool ok = true;
+        for (int b = 0; b <= lmax; ++b) {
+          const int ks = k_iter % kIdxStagesK;
+          if (k_iter >= kIdxStagesK &&
+              !mbar_wait(&sm.k_empty[ks], ((k_iter / kIdxStagesK) - 1) & 1, abort_flag)) {
+            report_timeout(abort_flag, hdr, 103);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&sm.k_full[ks], tile_tx);
+          for (int c = 0; c < kchunks; ++c)
+            tma_load_2d(k_buf + ks * kTileBytes + c * 16384, &tm_k, &sm.k_full[ks], c * 64,
+                        si.k_start + b * kBlock);
+          ++k_iter;
+        }
+        if (!ok) break;
+      }
+      // Let every issued copy land before the CTA can exit (matters only
+      // after an abort; in a normal run the MMA warp consumed them all).
+      for (int s = 0; s < 2; ++s)
+        if (q_iter > static_cast<uint32_t>(s)) {
+          const uint32_t last = ((q_iter - 1 - s) / 2) * 2 + s;
+          mbar_wait(&sm.q_full[s], (last >> 1) & 1, nullptr);
+        }
+      for (int s = 0; s < kIdxStagesK; ++s)
+        if (k_iter > static_cast<uint32_t>(s)) {
+          const uint32_t last = ((k_iter - 1 - s) / kIdxStagesK) * kIdxStagesK + s;
+          mbar_wait(&sm.k_full[s], (last / kIdxStagesK) & 1, nullptr);
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(128, 128, false);
+      uint32_t q_iter = 0, k_iter = 0, a_iter = 0;
+      for (uint32_t w = 0;; ++w) {
+        const int slot = w & 1;
+        if (!mbar_wait(&sm.work_full[slot], (w >> 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 111);
+          break;
+        }
+        const int item = sm.work[slot];
+        mbar_arrive(&sm.work_empty[slot]);
+        if (item < 0) break;
+        const int2 tile = p.tiles[item];
+        const SeqInfo si = p.seq[tile.x];
+        int nq, lmax;
+        tile_geometry(si, tile.y, p.qt, nq, lmax);
+        const int qb = q_iter & 1;
+        if (!mbar_wait(&sm.q_full[qb], (q_iter >> 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 112);
+          break;
+        }
+        const uint32_t qa = smem_u32(q_buf + qb * kTileBytes);
+        bool ok = true;
+        for (int b = 0; b <= lmax; ++b) {
+          const int ks = k_iter % kIdxStagesK;
+          const int ab = a_iter & 1;
+          if (!mbar_wait(&sm.k_full[ks], (k_iter / kIdxStagesK) & 1, abort_flag) ||
+              (a_iter >= 2 && !mbar_wait(&sm.acc_empty[ab], ((a_iter >> 1) - 1) & 1, abort_flag))) {
+            report_timeout(abort_flag, hdr, 113);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ka = smem_u32(k_buf + ks * kTileBytes);
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            umma_bf16(tmem + ab * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc,
+                      kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&sm.k_empty[ks]);
+          umma_commit(&sm.acc_full[ab]);
+          ++k_iter;
+          ++a_iter;
+        }
+        if (!ok) break;
+        umma_commit(&sm.q_empty[qb]);
+        ++q_iter;
+      }
+      // all MMAs retired before TMEM can be released
+      umma_commit(&sm.mma_done);
+      mbar_wait(&sm.mma_done, 0, nullptr);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int row = (warp - 4) * 32 + lane;  // TMEM lane == tile row
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    uint32_t a_iter = 0;
+    for (uint32_t w = 0;; ++w) {
+      const int slot = w & 1;
+      if (!mbar_wait(&sm.work_full[slot], (w >> 1) & 1, abort_flag)) {
+        report_timeout(abort_flag, hdr, 121);
+        break;
+      }
+      const int item = sm.work[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.work_empty[slot]);
+      if (item < 0) break;
+      const int2 tile = p.tiles[item];
+      const SeqInfo si = p.seq[tile.x];
+      int nq, lmax;
+      tile_geometry(si, tile.y, p.qt, nq, lmax);
+      const int tq = row / p.hkv;               // query offset inside the tile
+      const bool valid = tq < nq;
+      const int t = tile.y + tq;
+      const int pos = si.kv_len - si.q_len + t;
+      const int local = pos >> 7;
+      const int64_t grow = static_cast<int64_t>(si.q_start + tile.y) * p.hkv + row;  // global Q_idx row
+      TopkList<CAP> list;
+      list.clear();
+      bool ok = true;
+      for (int b = 0; b <= lmax; ++b) {
+        const int ab = a_iter & 1;
+        if (!mbar_wait(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 122);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32cols(lane_addr + ab * 128 + c * 32, r[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.acc_empty[ab]);
+        ++a_iter;
+        if (valid && b <= local) {
+          const int lim = (b == local) ? (pos & 127) : 127;
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+          if (lim == 127) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              m0 = fmaxf(m0, __uint_as_float(r[0][c]));
+              m1 = fmaxf(m1, __uint_as_float(r[1][c]));
+              m2 = fmaxf(m2, __uint_as_float(r[2][c]));
+              m3 = fmaxf(m3, __uint_as_float(r[3][c]));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              m0 = fmaxf(m0, c <= lim ? __uint_as_float(r[0][c]) : -INFINITY);
+              m1 = fmaxf(m1, c + 32 <= lim ? __uint_as_float(r[1][c]) : -INFINITY);
+              m2 = fmaxf(m2, c + 64 <= lim ? __uint_as_float(r[2][c]) : -INFINITY);
+              m3 = fmaxf(m3, c + 96 <= lim ? __uint_as_float(r[3][c]) : -INFINITY);
+            }
+          }
+          const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+          if constexpr (FUSED) {
+            if (b < local) list.insert(topk_key(m, b));
+          } else {
+            p.pooled[grow * p.pooled_stride + b] = m;
+          }
+        }
+      }
+      if (!ok) break;
+      if constexpr (FUSED) {
+        if (valid) {
+          int chosen[CAP];
+#pragma unroll
+          for (int j = 0; j < CAP; ++j)
+            chosen[j] = (j < p.topk - 1 && list.k[j] != 0ull) ? topk_key_block(list.k[j]) : -1;
+          write_selection<CAP>(p.idx + grow * p.topk, p.topk, chosen, local);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+size_t index_score_smem_bytes() { return kIdxSmemBytes; }
+
+template <int CAP, bool FUSED>
+static cudaError_t launch_index(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p, int grid,
+                                cudaStream_t stream) {
+  auto* fn = index_score_kernel<CAP, FUSED>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kIdxSmemBytes));
+  if (e != cudaSuccess) return e;
+  fn<<<grid, kIdxThreads, kIdxSmemBytes, stream>>>(tq, tk, p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_index_score(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p, bool fused,
+                               int grid, cudaStream_t stream) {
+  if (!fused) return launch_index<1, false>(tq, tk, p, grid, stream);
+  if (p.topk <= 4) return launch_index<3, true>(tq, tk, p, grid, stream);
+  if (p.topk <= 8) return launch_index<7, true>(tq, tk, p, grid, stream);
+  return launch_index<15, true>(tq, tk, p, grid, stream);
+}
+
+}  // namespace msa

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Small cases are checked on every row and span several tiles with ragged
+tails; the named workloads are checked at full size on sampled rows, in the
+launch configuration the benchmark times.  Each step is also tested on its
+own: pooled index scores, top-k over given pooled rows, the Main Branch on
+the oracle's own indices.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from workloads.configs import small
+
+from parity import (NEAR_TIE, assert_attention_close, compare_indices, problem_for, sample_rows, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msa():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_attention_05_gb300 as m
+    torch.cuda.set_device(0)
+    return m
+
+
+SMALL_CASES = {
+    # several index tiles, ragged query tails, kv_len not a multiple of 128, chunked (q_len < kv_len)
+    "varlen_g16": dict(seqs=((300, 300), (1000, 1777), (1, 129), (129, 900), (0, 77), (640, 640)),
+                       hq=64, hkv=4, d_idx=128, topk=16, n_topics=16),
+    "tiny_shape_short": dict(seqs=((700, 700), (257, 1500)), hq=16, hkv=2, d_idx=64, topk=4, n_topics=8),
+    "k_covers_all": dict(seqs=((200, 200), (64, 1000)), hq=64, hkv=4, d_idx=128, topk=16, n_topics=4),
+    "k_small": dict(seqs=((1100, 1100),), hq=32, hkv=4, d_idx=128, topk=2, n_topics=8),
+    "k_one": dict(seqs=((520, 520),), hq=64, hkv=4, d_idx=64, topk=1, n_topics=8),
+}
+
+
+def make_small(name, seed=3):
+    kw = dict(SMALL_CASES[name])
+    seqs = kw.pop("seqs")
+    return small(name, seqs, seed=seed, **kw)
+
+
+# ------------------------------------------------------------------ a1: pooled scores
+@pytest.mark.parametrize("name", ["varlen_g16", "tiny_shape_short"])
+def test_index_pool_matches_oracle(msa, name):
+    cfg = make_small(name)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    pooled = msa.msa_index_pool(prob, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    got = to_np(pooled).reshape(x.total_q, cfg.hkv, -1)
+    ref = oracle.pooled(x.cu_q, x.cu_k, x.q_idx, x.k_idx, block=cfg.block, nb_stride=got.shape[2])
+    valid = np.isfinite(ref)
+    assert np.all(np.isnan(got[~valid])), "entries past the causal end must be left untouched"
+    np.testing.assert_allclose(got[valid], ref[valid], rtol=1e-5, atol=1e-4)
+
+
+# ------------------------------------------------------------------ a2: top-k over given pooled rows
+@pytest.mark.parametrize("nb_max,topk,seed", [(40, 4, 0), (600, 16, 1), (1024, 16, 2), (5000, 8, 3),
+                                              (8192, 16, 4), (3, 16, 5)])
+def test_topk_pooled_matches_oracle_select(msa, nb_max, topk, seed):
+    rng = np.random.default_rng(seed)
+    # one sequence whose queries sit at positions spread over the whole context
+    kv = nb_max * 128
+    q_len = 64 if kv >= 64 else kv
+    prob = msa.problem_from_seqlens([q_len], [kv], hq=64, hkv=4, d_idx=128, topk=topk)
+    rows = q_len * 4
+    vals = rng.standard_normal((rows, nb_max)).astype(np.float32)
+    tied = rng.random(rows) < 0.5           # half the rows: few distinct values, many exact ties
+    vals[tied] = rng.choice(np.array([-1.0, -0.0, 0.0, 2.0, 2.0, 5.0], np.float32), size=(tied.sum(), nb_max))
+    pooled = torch.from_numpy(vals).cuda()
+    idx = to_np(msa.msa_topk_pooled(prob, pooled))
+    pos = kv - q_len + np.arange(q_len)
+    for r in range(rows):
+        nb = int(pos[r // 4]) // 128 + 1
+        sel, _ = oracle.select(vals[r], nb, topk)
+        assert idx[r // 4, r % 4].tolist() == sel.tolist(), f"row {r} (nb {nb})"
+
+
+# ------------------------------------------------------------------ a1+a2 fused: selection
+@pytest.mark.parametrize("name", sorted(SMALL_CASES))
+def test_index_topk_matches_oracle(msa, name):
+    cfg = make_small(name)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    idx = to_np(msa.msa_index_topk(prob, x.q_idx, x.k_idx))
+    torch.cuda.synchronize()
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(idx, ref)
+    assert mism == 0, f"{mism} rows select differently from the oracle"
+    assert tie.mean() < 1e-3 or tie.sum() <= 1, f"near-tie rate {tie.mean():.2e}"
+
+
+# ------------------------------------------------------------------ a3-a5: Main Branch on oracle indices
+@pytest.mark.parametrize("name", sorted(SMALL_CASES))
+def test_sparse_attn_prefill_on_oracle_indices(msa, name):
+    cfg = make_small(name)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    idx = torch.from_numpy(ref["idx"]).cuda()
+    o, lse = msa.msa_sparse_attn_prefill(prob, x.q, x.k, x.v, idx)
+    torch.cuda.synchronize()
+    if x.total_q:
+        assert_attention_close(to_np(o), to_np(lse), ref, cfg.hq // cfg.hkv, what=name)
+
+
+def test_sparse_attn_prefill_random_selections(msa):
+    """Arbitrary valid selections (not top-k), including fewer than k blocks and repeated hot blocks."""
+    cfg = small("rand_sel", ((900, 900), (333, 2000)), hq=64, hkv=4, d_idx=128, topk=8, n_topics=4, seed=11)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    rng = np.random.default_rng(5)
+    pos = oracle.query_positions(x.cu_q, x.cu_k)
+    idx = np.full((x.total_q, cfg.hkv, cfg.topk), -1, np.int32)
+    for i in range(x.total_q):
+        nb = int(pos[i]) // 128 + 1
+        for g in range(cfg.hkv):
+            m = int(rng.integers(1, min(cfg.topk, nb) + 1))
+            pick = set([nb - 1, 0] if nb > 1 and m > 1 else [nb - 1])  # block 0: a hot block
+            while len(pick) < m:
+                pick.add(int(rng.integers(0, nb)))
+            s = sorted(pick)
+            idx[i, g, :len(s)] = s
+    o, lse = msa.msa_sparse_attn_prefill(prob, x.q, x.k, x.v, torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(x.cu_q, x.cu_k, x.q, x.k, x.v, idx, block=128)
+    assert_attention_close(to_np(o), to_np(lse), {"o": o_ref, "lse": lse_ref}, 16, what="random selections")
+
+
+# ------------------------------------------------------------------ end to end (prefill)
+@pytest.mark.parametrize("name", ["varlen_g16", "tiny_shape_short", "k_covers_all"])
+def test_forward_prefill_end_to_end(msa, name):
+    cfg = make_small(name, seed=21)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(to_np(idx), ref)
+    assert mism == 0
+    assert_attention_close(to_np(o), to_np(lse), ref, cfg.hq // cfg.hkv, exempt=tie, what=name)
+
+
+def test_forward_tiny_workload_all_rows(msa):
+    cfg = workloads.get("tiny")
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(to_np(idx), ref)
+    assert mism == 0
+    assert tie.mean() < 1e-3
+    assert_attention_close(to_np(o), to_np(lse), ref, cfg.hq // cfg.hkv, exempt=tie, what="tiny")
+    # Main Branch in isolation on the oracle's indices: every row, no exemption
+    o2, lse2 = msa.msa_sparse_attn_prefill(prob, x.q, x.k, x.v, torch.from_numpy(ref["idx"]).cuda())
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(o2), to_np(lse2), ref, cfg.hq // cfg.hkv, what="tiny, oracle indices")
+
+
+# ------------------------------------------------------------------ decode
+def decode_case(n, ctx, seed, topk=16, d_idx=128):
+    return workloads.configs.Workload("dec_small", None, seed=seed, decode_batch=n, decode_ctx=ctx,
+                                      topk=topk, d_idx=d_idx, n_topics=16)
+
+
+@pytest.mark.parametrize("n,ctx,topk,d_idx", [(8, 3000, 16, 128), (5, 700, 16, 64), (3, 128, 4, 128),
+                                              (16, 20000, 16, 128)])
+def test_forward_decode_end_to_end(msa, n, ctx, topk, d_idx):
+    cfg = decode_case(n, ctx, seed=n + ctx, topk=topk, d_idx=d_idx)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(to_np(idx), ref)
+    assert mism == 0
+    assert_attention_close(to_np(o), to_np(lse), ref, 16, exempt=tie, what="decode")
+    # the decode Main Branch on the oracle's indices
+    o2, lse2 = msa.msa_sparse_attn_decode(prob, x.q, x.k, x.v, torch.from_numpy(ref["idx"]).cuda())
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(o2), to_np(lse2), ref, 16, what="decode, oracle indices")
+
+
+# ------------------------------------------------------------------ device-side validation
+def test_inconsistent_seqlens_raise_a_device_flag(msa):
+    cfg = make_small("varlen_g16")
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    bad = x.cu_k.clone()
+    bad[2] = bad[1] + 5  # sequence 1 now has fewer keys than queries
+    prob.cu_k = bad
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    o = torch.full_like(x.q, 7.0)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, o=o, ws=ws)
+    flags = msa.msa_read_device_status(ws)
+    assert flags & msa.DEVICE_BAD_SEQLENS
+    assert torch.all(o == 7.0), "no kernel may write output after a bad-seqlens flag"
+    # a good call on the same workspace clears it
+    prob.cu_k = x.cu_k
+    msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, ws=ws)
+    assert msa.msa_read_device_status(ws) == 0
+
+
+def test_outputs_do_not_depend_on_the_stream_or_repeat(msa):
+    cfg = make_small("varlen_g16", seed=9)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    a = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    s.synchronize()
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v), "two runs must agree bit for bit"
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled rows
+FULL = ["prefill_32k", "varlen", "decode_128k", "chunked_1m", "decode_1m", "prefill_128k"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(msa, name):
+    cfg = workloads.get(name)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
+    rows = sample_rows(x, n_random=24 if x.total_q > 10000 else 16)
+    ref = _oracle_rows(x, cfg, rows)
+    rows_t = torch.from_numpy(rows).long().cuda()
+    tie, mism = compare_indices(to_np(idx[rows_t]), ref)
+    assert mism == 0, f"{mism} sampled rows select differently"
+    assert_attention_close(to_np(o[rows_t]), to_np(lse[rows_t]), ref, cfg.hq // cfg.hkv, exempt=tie, what=name)
+    # properties over every row: the local block is selected, the budget is full, order ascending
+    idx_all = idx.cpu().numpy()
+    pos = oracle.query_positions(x.cu_q, x.cu_k)
+    local = (pos // 128).astype(np.int32)
+    nb = local + 1
+    valid = idx_all >= 0
+    n_valid = valid.sum(axis=2)
+    assert np.all(n_valid == np.minimum(cfg.topk, nb)[:, None])
+    last = np.take_along_axis(idx_all, (n_valid - 1)[:, :, None], axis=2)[:, :, 0]
+    assert np.all(last == local[:, None]), "the local block must be the largest selected index"
+    d = np.diff(np.where(valid, idx_all, np.iinfo(np.int32).max), axis=2)
+    assert np.all(d[valid[:, :, 1:]] > 0)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
+def _oracle_rows(x, cfg, rows):
+    """The oracle on the sampled query rows (it reads the full K, V, K_idx; Q rows by index)."""
+    return oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk,
+                          rows=rows)
