@@ -56,6 +56,15 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks (the slowest replica's time); identity without a process group."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ algorithmic work
 def algorithmic_work(x, idx: torch.Tensor):
     """Per-stage algorithmic FLOPs / bytes of one step (from the actual selection)."""
@@ -299,10 +308,7 @@ def main():
         torch.distributed.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     units_per_gpu = x.total_q
     value = units_per_gpu * world / (ms / 1000.0)
 
@@ -390,10 +396,7 @@ def main():
         t1.record()
         t1.synchronize()
         e2e_ms = t0.elapsed_time(t1) / args.steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 

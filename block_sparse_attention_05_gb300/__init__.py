@@ -34,7 +34,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 class MsaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {_lib.msa_status_string(status).decode()} (status {status})")
+        detail = _lib.msa_last_error_detail().decode() if status == -5 else ""
+        super().__init__(f"{where}: {_lib.msa_status_string(status).decode()} (status {status})"
+                         + (f" [{detail}]" if detail else ""))
 
 
 class Op(enum.IntEnum):
@@ -48,6 +50,7 @@ class Op(enum.IntEnum):
 
 DEVICE_TIMEOUT = 1
 DEVICE_BAD_SEQLENS = 2
+DEVICE_BAD_INDEX = 4
 
 
 class MsaProblem(ctypes.Structure):
@@ -95,11 +98,12 @@ _lib.msa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _v
 _lib.msa_set_stage_events.restype = ctypes.c_int
 _lib.msa_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
 _lib.msa_kernel_launch_count.restype = ctypes.c_int64
+_lib.msa_last_error_detail.restype = ctypes.c_char_p
 
 EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_index_topk",
             "msa_sparse_attn_prefill", "msa_sparse_attn_decode", "msa_forward",
             "msa_read_device_status", "msa_status_string", "msa_abi_version", "msa_set_stage_events",
-            "msa_kernel_launch_count")
+            "msa_kernel_launch_count", "msa_last_error_detail")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 

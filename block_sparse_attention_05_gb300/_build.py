@@ -48,6 +48,16 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     hdrs = _headers()
     exe = nvcc()
     flags = FLAGS + list(extra_flags or [])
+    # objects built with other flags are stale
+    stamp = os.path.join(LIB_DIR, "obj", "flags.txt")
+    key = " ".join(ARCH + flags)
+    if not os.path.exists(stamp) or open(stamp).read() != key:
+        for o in glob.glob(os.path.join(LIB_DIR, "obj", "*.o")):
+            os.remove(o)
+        if os.path.exists(LIB):
+            os.remove(LIB)
+        with open(stamp, "w") as f:
+            f.write(key)
 
     def compile_one(src):
         obj = os.path.join(LIB_DIR, "obj", os.path.basename(src) + ".o")

@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -19,6 +20,9 @@ namespace {
 std::atomic<int64_t> g_launches{0};
 thread_local cudaEvent_t t_stage_events[2 * MSA_NUM_STAGES];
 thread_local bool t_stage_events_on = false;
+thread_local int t_stage = -1;
+thread_local char t_error_detail[256] = "";
+const char* const kStageNames[MSA_NUM_STAGES] = {"plan", "index", "topk", "schedule", "attn", "combine"};
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -30,6 +34,7 @@ struct StageScope {
   int stage;
   cudaStream_t stream;
   StageScope(int s, cudaStream_t st) : stage(s), stream(st) {
+    t_stage = s;
     if (t_stage_events_on) cudaEventRecord(t_stage_events[2 * stage], stream);
   }
   ~StageScope() {
@@ -203,6 +208,9 @@ bool make_map(CUtensorMap& m, const void* ptr, int rank, const cuuint64_t* dims,
   CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides_bytes, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    std::snprintf(t_error_detail, sizeof t_error_detail, "tensor map encode failed (CUresult %d, rank %d)",
+                  static_cast<int>(r), rank);
   return r == CUDA_SUCCESS;
 }
 
@@ -235,6 +243,8 @@ struct Ctx {
 
 msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_bytes, msa_stream_t stream,
                    Ctx& c) {
+  t_stage = -1;
+  t_error_detail[0] = 0;
   msa_status_t st = derive(p, c.d);
   if (st != MSA_OK) return st;
   if ((op == MSA_OP_SPARSE_ATTN_DECODE) && !c.d.decode) return MSA_ERR_INVALID_ARG;
@@ -254,7 +264,12 @@ msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_byte
   return MSA_OK;
 }
 
-msa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+msa_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MSA_OK;
+  std::snprintf(t_error_detail, sizeof t_error_detail, "stage %s: %s (%d)",
+                t_stage >= 0 ? kStageNames[t_stage] : "setup", cudaGetErrorName(e), static_cast<int>(e));
+  return MSA_ERR_CUDA;
+}
 
 msa_status_t run_plan(const msa_problem_t* p, Ctx& c, int qt) {
   StageScope scope(MSA_STAGE_PLAN, c.stream);
@@ -312,6 +327,7 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
   tp.total_q = c.d.T;
   tp.hkv = c.d.hkv;
   tp.topk = c.d.topk;
+  tp.max_nb = static_cast<int>(stride < c.d.max_nb ? stride : c.d.max_nb);
   tp.cu_q = p->cu_seqlens_q;
   tp.seq = c.seq;
   tp.pooled = pooled;
@@ -344,6 +360,7 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   ups = (c.d.max_nb + bpu - 1) / bpu;
   sp.units_per_seq = ups;
   sp.blocks_per_unit = bpu;
+  sp.total_k = c.d.N;
   sp.hdr = c.hdr;
   long long units = static_cast<long long>(c.d.S) * ups;
   int grid = static_cast<int>(units < c.dev.sms ? units : c.dev.sms);
@@ -491,6 +508,8 @@ msa_status_t msa_set_stage_events(void* const* events) {
 }
 
 int64_t msa_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* msa_last_error_detail(void) { return t_error_detail; }
 
 const char* msa_status_string(msa_status_t s) {
   switch (s) {

@@ -13,7 +13,15 @@ namespace msa {
 // ----------------------------------------------------------------------------
 // Workspace header: first 256 bytes of every workspace.
 // ----------------------------------------------------------------------------
-enum : uint32_t { kFlagTimeout = 1u, kFlagBadSeqlens = 2u };
+enum : uint32_t { kFlagTimeout = 1u, kFlagBadSeqlens = 2u, kFlagBadIndex = 4u };
+
+// Compile with -DMSA_CHECKED=1 to make the kernels verify their computed
+// indices before each global or shared access they are not certain of; a
+// failed check records (site, index, bound) in the workspace header, raises
+// kFlagBadIndex and skips the access.
+#ifndef MSA_CHECKED
+#define MSA_CHECKED 0
+#endif
 
 struct WsHeader {
   uint32_t status;          // MSA_DEVICE_* bits
@@ -22,6 +30,8 @@ struct WsHeader {
   uint32_t n_entries;       // (query, group, slot) incidences
   uint32_t counter[8];      // persistent-kernel claim counters
   uint32_t timeout_site;    // where a wait gave up (debug)
+  uint32_t bad_site;        // first failed index check: site
+  long long bad_index, bad_bound;
 };
 
 // Per-sequence facts derived once from cu_seqlens.
@@ -88,11 +98,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Warp-wide wait.  try_wait may release the lanes of a warp at different
+// times, so a plain per-lane spin can leave the warp diverged; the code after
+// a wait executes warp-collective .sync.aligned instructions (ldmatrix,
+// mma.sync, tcgen05.ld/st) that need every lane converged.  __all_sync
+// reconverges the warp and makes the outcome uniform.  Every lane must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xFFFFFFFFu, ok) != 0;
+}
+
 // Records a failed wait: sets the CTA abort flag and the workspace status.
 __device__ __forceinline__ void report_timeout(volatile int* abort_flag, WsHeader* hdr, uint32_t site) {
   *abort_flag = 1;
   atomicOr(&hdr->status, kFlagTimeout);
   atomicExch(&hdr->timeout_site, site);
+}
+
+// True when 0 <= i < n; otherwise (in checked builds) records the failure.
+__device__ __forceinline__ bool index_ok(WsHeader* hdr, long long i, long long n, uint32_t site) {
+#if MSA_CHECKED
+  if (i < 0 || i >= n) {
+    if (atomicCAS(&hdr->bad_site, 0u, site) == 0u) {
+      hdr->bad_index = i;
+      hdr->bad_bound = n;
+    }
+    atomicOr(&hdr->status, kFlagBadIndex);
+    return false;
+  }
+#else
+  (void)hdr; (void)i; (void)n; (void)site;
+#endif
+  return true;
 }
 
 // ----------------------------------------------------------------------------
@@ -154,6 +191,17 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Same with A read from tensor memory (columns a_tmem.., one row per lane, two
+// 16-bit elements per 32-bit column along K).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -176,6 +224,17 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Each thread of the warp writes 16 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (tcgen05 format) for a tile stored in the
 // 128-byte swizzled layout that TMA writes with CU_TENSOR_MAP_SWIZZLE_128B:

@@ -7,8 +7,8 @@
 // selection runs in decode too and that decode then reads about 2,048 KV
 // tokens whatever the context length).  The scan streams K_idx once and is
 // bound by HBM bandwidth, so it is built for bytes in flight: a persistent
-// grid, a TMA producer keeping a 6-stage ring of 128-key tiles full, and four
-// consumer warps.  The 4 group queries against 16 keys are one small
+// grid, a TMA producer keeping a 6-stage ring of 128-key tiles full, and one
+// consumer warp per stage.  The 4 group queries against 16 keys are one small
 // mma.sync (m16n8k16: keys x d_idx times d_idx x groups) -- it keeps the
 // instruction count per byte low so the issue slots never limit the stream.
 //
@@ -24,8 +24,12 @@ namespace msa {
 
 namespace {
 
+// One consumer warp per ring stage: block j of a CTA's stream goes to stage
+// j % kScanStages and is consumed by warp j % kScanStages, so every stage has a
+// single consumer that takes its fills in order (a parity wait is only sound
+// when the waiter already consumed the stage's previous fill).
 constexpr int kScanStages = 6;
-constexpr int kScanConsumers = 4;
+constexpr int kScanConsumers = kScanStages;
 constexpr int kScanThreads = 32 * (kScanConsumers + 1);
 constexpr int kScanTile = 128 * 128 * 2;  // 128 keys x up to 128 dims, bf16
 constexpr size_t kScanSmemBytes = 1024 + kScanStages * kScanTile + 256;
@@ -117,8 +121,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           report_timeout(abort_flag, hdr, 301);
           break;
         }
-        mbar_arrive_expect_tx(&sm.full[st], tile_tx);
         const int row = p.seq[c.s].k_start + c.b * kBlock;
+        index_ok(hdr, c.s, p.num_seqs, 401);
+        index_ok(hdr, row, p.total_k, 402);
+        mbar_arrive_expect_tx(&sm.full[st], tile_tx);
         for (int ch = 0; ch < kchunks; ++ch)
           tma_load_2d(base + st * kScanTile + ch * 16384, &tm_k, &sm.full[st], ch * 64, row);
         ++c.b;
@@ -150,17 +156,19 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const SeqInfo si = p.seq[cur_s];
         pos = si.kv_len - 1;
         const __nv_bfloat16* qrow = p.q_idx + (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx;
+        const bool q_ok = gq >= p.hkv || index_ok(hdr, (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx +
+                                                             p.d_idx - 1, static_cast<long long>(p.num_seqs) * p.hkv * p.d_idx, 403);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           qf[ks][0] = qf[ks][1] = 0u;
-          if (gq < p.hkv && ks * 16 < p.d_idx) {
+          if (q_ok && gq < p.hkv && ks * 16 < p.d_idx) {
             const int d0 = ks * 16 + (lane & 3) * 2;
             qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + d0);
             qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + d0 + 8);
           }
         }
       }
-      if (!mbar_wait(&sm.full[st], (my / kScanStages) & 1, abort_flag)) {
+      if (!mbar_wait_warp(&sm.full[st], (my / kScanStages) & 1, abort_flag)) {
         report_timeout(abort_flag, hdr, 311);
         break;
       }
@@ -199,9 +207,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       }
       if (lane < 4) {
         const int g0 = lane * 2;
+        const long long rows = static_cast<long long>(p.num_seqs) * p.hkv;
+        const long long at0 = (static_cast<long long>(cur_s) * p.hkv + g0) * p.pooled_stride + b;
         float* out = p.pooled + static_cast<int64_t>(cur_s) * p.hkv * p.pooled_stride + b;
-        if (g0 < p.hkv) out[static_cast<int64_t>(g0) * p.pooled_stride] = mx0;
-        if (g0 + 1 < p.hkv) out[static_cast<int64_t>(g0 + 1) * p.pooled_stride] = mx1;
+        if (g0 < p.hkv && index_ok(hdr, at0, rows * p.pooled_stride, 404) && index_ok(hdr, b, p.pooled_stride, 405))
+          out[static_cast<int64_t>(g0) * p.pooled_stride] = mx0;
+        if (g0 + 1 < p.hkv && index_ok(hdr, at0 + p.pooled_stride, rows * p.pooled_stride, 406))
+          out[static_cast<int64_t>(g0 + 1) * p.pooled_stride] = mx1;
       }
     }
   }
@@ -231,6 +243,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// (a, b) -> bf16 pair hi and bf16 pair lo with a ~= hi.x + lo.x, b ~= hi.y + lo.y
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_bf16x2(a - __low2float(h), b - __high2float(h));
 }
 
 }  // namespace
@@ -358,11 +377,12 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int j = 0; j < 4; ++j) oacc[nt][j] = 0.f;
 #pragma unroll
   for (int kj = 0; kj < 2; ++kj) {
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(sacc[2 * kj][0], sacc[2 * kj][1]);
-    pa[1] = pack_bf16x2(sacc[2 * kj][2], sacc[2 * kj][3]);
-    pa[2] = pack_bf16x2(sacc[2 * kj + 1][0], sacc[2 * kj + 1][1]);
-    pa[3] = pack_bf16x2(sacc[2 * kj + 1][2], sacc[2 * kj + 1][3]);
+    // P = hi + lo (both bf16): ~16 significant bits for the PV product
+    uint32_t pa[4], pl[4];
+    split_bf16x2(sacc[2 * kj][0], sacc[2 * kj][1], pa[0], pl[0]);
+    split_bf16x2(sacc[2 * kj][2], sacc[2 * kj][3], pa[1], pl[1]);
+    split_bf16x2(sacc[2 * kj + 1][0], sacc[2 * kj + 1][1], pa[2], pl[2]);
+    split_bf16x2(sacc[2 * kj + 1][2], sacc[2 * kj + 1][3], pa[3], pl[3]);
 #pragma unroll
     for (int dp = 0; dp < 8; ++dp) {
       // matrices: (keys lo, d 16dp..+7), (keys hi, same d), (keys lo, d +8..15), (keys hi, d +8..15)
@@ -371,6 +391,8 @@ __global__ void __launch_bounds__(kDecThreads)
       ldmatrix_x4_trans(vt + sw128_off(key, dp * 2 + (mtx >> 1)), b0, b1, b2, b3);
       mma_16816(oacc[2 * dp], pa, b0, b1);
       mma_16816(oacc[2 * dp + 1], pa, b2, b3);
+      mma_16816(oacc[2 * dp], pl, b0, b1);
+      mma_16816(oacc[2 * dp + 1], pl, b2, b3);
     }
   }
   // merge the four warps: rescale to the common max, sum, normalise

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     uint32_t a_iter = 0;
     for (uint32_t w = 0;; ++w) {
       const int slot = w & 1;
-      if (!mbar_wait(&sm.work_full[slot], (w >> 1) & 1, abort_flag)) {
+      if (!mbar_wait_warp(&sm.work_full[slot], (w >> 1) & 1, abort_flag)) {
         report_timeout(abort_flag, hdr, 121);
         break;
       }
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       bool ok = true;
       for (int b = 0; b <= lmax; ++b) {
         const int ab = a_iter & 1;
-        if (!mbar_wait(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
+        if (!mbar_wait_warp(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 122);
           ok = false;
           break;

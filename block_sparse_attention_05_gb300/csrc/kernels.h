@@ -57,7 +57,7 @@ cudaError_t launch_index_score(const CUtensorMap& tq, const CUtensorMap& tk, con
 // Top-k over pooled rows r = i * hkv + g (rows of queries, or of decode
 // sequences when every q_len is 1).
 struct TopkParams {
-  int num_seqs, total_q, hkv, topk;
+  int num_seqs, total_q, hkv, topk, max_nb;
   const int32_t* cu_q;
   const SeqInfo* seq;
   const float* pooled;
@@ -76,6 +76,7 @@ struct DecodeScanParams {
   int64_t pooled_stride;
   int units_per_seq;            // work units per sequence
   int blocks_per_unit;
+  long long total_k;            // rows of K_idx (for checked builds)
   WsHeader* hdr;
 };
 size_t decode_scan_smem_bytes();

@@ -16,8 +16,10 @@
 // their Q rows gathered by TMA.  Per tile:
 //   S = Q K^T                 tcgen05, 128 x 128 x 128, fp32 in TMEM
 //   P = exp2(S*c - max)       softmax warpgroup, one TMEM lane (row) per thread,
-//                             causal limit per row (only the local block is cut)
-//   O = P V                   tcgen05, P (bf16) from shared memory, V MN-major
+//                             causal limit per row (only the local block is cut);
+//                             P is split into bf16 hi + lo parts written back
+//                             over S in TMEM
+//   O = P_hi V + P_lo V       tcgen05 with A read from TMEM, V MN-major in smem
 //   partial O / l and LSE     written per (query, group, slot, head)
 // The tile covers exactly one key block, so no running rescale is needed.
 //
@@ -25,8 +27,8 @@
 // MMA issuer, warp 2 = TMEM allocator, warp 3 idle, warps 4..7 and 8..11 = two
 // softmax/epilogue warpgroups taking alternate tiles (each owns an S and an O
 // accumulator in TMEM: 2 x (128 + 128) = 512 columns).  Q tiles live in a
-// 3-stage ring; a tile's P overwrites its own Q stage once QK^T has retired.
-// K/V are double-buffered across chunks.
+// 3-stage ring, freed as soon as QK^T retires; K/V are double-buffered across
+// chunks.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&sm.kv_full[i], 1);
       mbar_init(&sm.kv_empty[i], 1);
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_free[i], 128);
+      mbar_init(&sm.s_free[i], 1);
       mbar_init(&sm.p_full[i], 128);
       mbar_init(&sm.o_full[i], 1);
       mbar_init(&sm.o_free[i], 128);
@@ -269,10 +271,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.s_full[w]);
+          umma_commit(&sm.q_empty[qs]);  // the Q stage is free once QK^T has retired
           ++tt;
         }
         if (prev_valid) {
-          const int qs = prev_t % kQStages;
           const int w = prev_t & 1;
           const uint32_t n = prev_t >> 1;
           if (!mbar_wait(&sm.p_full[w], n & 1, abort_flag) ||
@@ -281,16 +283,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t pa = smem_u32(q_buf + qs * kQTileBytes);
+          // P sits in the S columns of TMEM as bf16 pairs: high parts in columns
+          // 0..63, low parts (p - bf16(p)) in 64..127; O = P_hi V + P_lo V.
+          const uint32_t pa = tmem + w * 256;
           const uint32_t va = smem_u32(kv_buf + prev_kvb * kKVBytes + 32768);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(tmem + w * 256 + 128, sdesc_sw128(pa + aoff, 16, 1024),
-                      sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, kk > 0 ? 1u : 0u);
-          }
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16_ts(tmem + w * 256 + 128, pa + part * 64 + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024),
+                           idesc_pv, (part | kk) ? 1u : 0u);
           umma_commit(&sm.o_full[w]);
-          umma_commit(&sm.q_empty[qs]);
+          umma_commit(&sm.s_free[w]);  // S/P columns reusable once PV has retired
           if (prev_last) umma_commit(&sm.kv_empty[prev_kvb]);
         }
         if (!next_valid) break;
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool ok = true;
     while (ok) {
       const int slot = w_iter % kWorkSlots;
-      if (!mbar_wait(&sm.work_full[slot], (w_iter / kWorkSlots) & 1, abort_flag)) {
+      if (!mbar_wait_warp(&sm.work_full[slot], (w_iter / kWorkSlots) & 1, abort_flag)) {
         report_timeout(abort_flag, hdr, 221);
         break;
       }
@@ -326,7 +330,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int tt = 0; tt < ci.ntile; ++tt, ++t) {
         if ((t & 1) != static_cast<uint32_t>(wg)) continue;
         const uint32_t n = t >> 1;
-        const int qs = t % kQStages;
         const int e = ci.begin + tt * p.qpt + q_local;
         const bool valid = e < ci.begin + ci.count;
         int qi = 0, slot_id = 0, lim = -1;
@@ -338,7 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const int pos = si.kv_len - si.q_len + (qi - si.q_start);
           lim = pos - ci.b * kBlock;               // keys 0..lim of this block are visible
         }
-        if (!mbar_wait(&sm.s_full[wg], n & 1, abort_flag)) {
+        if (!mbar_wait_warp(&sm.s_full[wg], n & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 222);
           ok = false;
           break;
@@ -348,8 +351,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld_32cols(lane_addr + c * 32, sr[c]);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.s_free[wg]);
 
         // softmax over the visible keys of this block (base-2, scale folded in)
         float mx = -INFINITY;
@@ -363,31 +364,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
         const float mref = (mx == -INFINITY) ? 0.f : mx;
         float l = 0.f;
+        // P = hi + lo, both bf16, written over the S columns: hi pairs to columns
+        // 0..63, lo pairs to 64..127 (two bf16 per 32-bit column, key 2c in the
+        // low half).  Splitting keeps P at ~16 significant bits for the PV product.
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float pv = exp2f(__uint_as_float(sr[c][j]) - mref);
-            sr[c][j] = __float_as_uint(pv);
-            l += pv;
+          for (int j = 0; j < 16; ++j) {
+            const float a = exp2f(__uint_as_float(sr[c][2 * j]) - mref);
+            const float b = exp2f(__uint_as_float(sr[c][2 * j + 1]) - mref);
+            l += a + b;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            hi[j] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[j] = pack_bf16(a - __low2float(h), b - __high2float(h));
           }
-        // P (bf16) into this tile's Q stage, K-major 128B-swizzled like the Q tile
-        uint8_t* prow = q_buf + qs * kQTileBytes + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {  // 8-key chunks
-          const int c = ch >> 2, j0 = (ch & 3) * 8;
-          uint4 v;
-          v.x = pack_bf16(__uint_as_float(sr[c][j0 + 0]), __uint_as_float(sr[c][j0 + 1]));
-          v.y = pack_bf16(__uint_as_float(sr[c][j0 + 2]), __uint_as_float(sr[c][j0 + 3]));
-          v.z = pack_bf16(__uint_as_float(sr[c][j0 + 4]), __uint_as_float(sr[c][j0 + 5]));
-          v.w = pack_bf16(__uint_as_float(sr[c][j0 + 6]), __uint_as_float(sr[c][j0 + 7]));
-          const int half = ch >> 3, phys = (ch & 7) ^ (r & 7);
-          *reinterpret_cast<uint4*>(prow + half * 16384 + phys * 16) = v;
+          tmem_st_16cols(lane_addr + c * 16, hi);
+          tmem_st_16cols(lane_addr + 64 + c * 16, lo);
         }
-        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
         mbar_arrive(&sm.p_full[wg]);
 
-        if (!mbar_wait(&sm.o_full[wg], n & 1, abort_flag)) {
+        if (!mbar_wait_warp(&sm.o_full[wg], n & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 223);
           ok = false;
           break;

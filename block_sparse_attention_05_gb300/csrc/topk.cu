@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 502)) return;
   const int nwarps = blockDim.x >> 5;
   const int i = row / p.hkv;
   const int s = find_seq(p.cu_q, p.num_seqs, i);
@@ -41,7 +42,8 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   const int lo = warp * per, hi = min(local, lo + per);
   TopkList<CAP> lst;
   lst.clear();
-  for (int b = lo + lane; b < hi; b += 32) lst.insert(topk_key(pr[b], b));
+  for (int b = lo + lane; b < hi; b += 32)
+    if (index_ok(p.hdr, b, p.max_nb, 501)) lst.insert(topk_key(pr[b], b));
 #pragma unroll
   for (int r = 0; r < CAP; ++r) {
     if (r < want) {
@@ -65,7 +67,8 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
       if (best != 0ull) chosen[r] = topk_key_block(best);
     }
   }
-  if (lane == 0) write_selection<CAP>(p.idx + static_cast<int64_t>(row) * p.topk, p.topk, chosen, local);
+  if (lane == 0 && index_ok(p.hdr, local, p.max_nb, 503))
+    write_selection<CAP>(p.idx + static_cast<int64_t>(row) * p.topk, p.topk, chosen, local);
 }
 
 }  // namespace

@@ -81,6 +81,7 @@ typedef enum msa_status {
 /* Device-side error flags (msa_read_device_status). */
 #define MSA_DEVICE_TIMEOUT 1u        /* a kernel wait exceeded its time limit */
 #define MSA_DEVICE_BAD_SEQLENS 2u    /* cu_seqlens disagree with the host sizes */
+#define MSA_DEVICE_BAD_INDEX 4u      /* a computed index failed its check (checked builds only) */
 
 typedef struct msa_problem {
   int32_t num_seqs;              /* >= 1 */
@@ -183,6 +184,10 @@ msa_status_t msa_set_stage_events(void *const *events);
 /* Number of kernels this library has enqueued since the process started
  * (all host threads; memsets included).  A diagnostic for launch accounting. */
 int64_t msa_kernel_launch_count(void);
+
+/* For the calling host thread: a description of the CUDA failure behind the
+ * last MSA_ERR_CUDA (stage and CUDA error name), or "" if none. */
+const char *msa_last_error_detail(void);
 
 /* Static description of a status code. */
 const char *msa_status_string(msa_status_t status);

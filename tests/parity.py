@@ -45,9 +45,12 @@ def sample_rows(x, n_random=48, seed=0):
 
 
 def compare_indices(idx_gpu: np.ndarray, ref: dict):
-    """Returns (tie mask [n, hkv], number of non-exempt mismatching rows)."""
+    """Returns (tie mask [n, hkv], number of non-exempt mismatching rows); prints the first mismatches."""
     tie = ref["gap"] < NEAR_TIE
     mism = (idx_gpu != ref["idx"]).any(axis=-1) & ~tie
+    for r, g in np.argwhere(mism)[:5]:
+        print(f"index mismatch row {r} group {g}: gpu {idx_gpu[r, g].tolist()} oracle {ref['idx'][r, g].tolist()} "
+              f"gap {ref['gap'][r, g]:.3e}")
     return tie, int(mism.sum())
 
 

@@ -141,8 +141,10 @@ def test_forward_prefill_end_to_end(msa, name):
     cfg = make_small(name, seed=21)
     x = workloads.generate(cfg, device="cuda")
     prob = problem_for(msa, x)
-    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, ws=ws)
     torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
     ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
     tie, mism = compare_indices(to_np(idx), ref)
     assert mism == 0
@@ -173,13 +175,15 @@ def decode_case(n, ctx, seed, topk=16, d_idx=128):
 
 
 @pytest.mark.parametrize("n,ctx,topk,d_idx", [(8, 3000, 16, 128), (5, 700, 16, 64), (3, 128, 4, 128),
-                                              (16, 20000, 16, 128)])
+                                              (16, 20000, 16, 128), (40, 60000, 16, 128)])
 def test_forward_decode_end_to_end(msa, n, ctx, topk, d_idx):
     cfg = decode_case(n, ctx, seed=n + ctx, topk=topk, d_idx=d_idx)
     x = workloads.generate(cfg, device="cuda")
     prob = problem_for(msa, x)
-    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, ws=ws)
     torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
     ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
     tie, mism = compare_indices(to_np(idx), ref)
     assert mism == 0
