@@ -439,17 +439,13 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
     return MSA_ERR_CUDA;
   AttnParams ap{};
   ap.seq = c.seq;
-  ap.blk_off = at<int32_t>(c.ws, c.L.blk_off);
-  ap.cu_q = p->cu_seqlens_q;
   ap.chunks = sp.chunks;
   ap.entries = sp.entries;
   ap.part = partials(c);
   ap.hdr = c.hdr;
-  ap.num_seqs = c.d.S;
   ap.hkv = c.d.hkv;
   ap.group = c.d.G;
   ap.topk = c.d.topk;
-  ap.total_blocks = c.d.total_blocks;
   ap.qpt = c.d.qpt;
   ap.scale_log2 = c.d.scale * 1.4426950408889634f;
   {

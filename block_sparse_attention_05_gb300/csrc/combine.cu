@@ -20,6 +20,7 @@ namespace msa {
 namespace {
 
 constexpr int kCombineWarps = 8;
+constexpr int kMaxTopk = 16;
 
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombineParams p) {
   if (p.hdr->status & kFlagBadSeqlens) return;
@@ -47,18 +48,27 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
 
+  // issue every slot's load before using any (memory-level parallelism)
+  const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + lane * 4;
+  const int64_t slot_stride = static_cast<int64_t>(p.group) * kHeadDim;
+  uint2 raw[kMaxTopk];
+  float wsl[kMaxTopk];
+#pragma unroll
+  for (int sl = 0; sl < kMaxTopk; ++sl) {
+    wsl[sl] = __shfl_sync(0xFFFFFFFFu, w, sl);
+    raw[sl] = make_uint2(0u, 0u);
+    if (sl < p.topk && wsl[sl] != 0.f) raw[sl] = __ldcs(reinterpret_cast<const uint2*>(base + sl * slot_stride));
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int sl = 0; sl < p.topk; ++sl) {
-    const float ws = __shfl_sync(0xFFFFFFFFu, w, sl);
-    if (ws == 0.f) continue;
-    const uint2 raw = *reinterpret_cast<const uint2*>(p.part.o + ((sel_base + sl) * p.group + hh) * kHeadDim +
-                                                       lane * 4);
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    acc[0] += ws * __low2float(a);
-    acc[1] += ws * __high2float(a);
-    acc[2] += ws * __low2float(b);
-    acc[3] += ws * __high2float(b);
+#pragma unroll
+  for (int sl = 0; sl < kMaxTopk; ++sl) {
+    const float ws = wsl[sl];
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw[sl].x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw[sl].y);
+    acc[0] = fmaf(ws, __low2float(a), acc[0]);
+    acc[1] = fmaf(ws, __high2float(a), acc[1]);
+    acc[2] = fmaf(ws, __low2float(b), acc[2]);
+    acc[3] = fmaf(ws, __high2float(b), acc[3]);
   }
   const bool empty = (m == -INFINITY);
   const float inv = empty ? 0.f : 1.f / sum;

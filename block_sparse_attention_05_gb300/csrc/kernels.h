@@ -101,7 +101,7 @@ struct ScheduleParams {
   int32_t* nchunk;        // [n_buckets]
   int32_t* chunk_start;   // [n_buckets + 1]
   int32_t* entries;       // [total_q * hkv * topk]
-  int4* chunks;           // [max_chunks] (bucket, begin, count, 0)
+  int4* chunks;           // [max_chunks] (begin, count, g | block << 8, seq)
   int32_t* scan_tmp;
   WsHeader* hdr;
   long long n_buckets;
@@ -110,13 +110,11 @@ cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t stream);
 
 struct AttnParams {
   const SeqInfo* seq;
-  const int32_t* blk_off;
-  const int32_t* cu_q;
   const int4* chunks;
   const int32_t* entries;
   PartialBuffers part;
   WsHeader* hdr;
-  int num_seqs, hkv, group, topk, total_blocks, qpt;
+  int hkv, group, topk, qpt;
   float scale_log2;       // softmax scale * log2(e)
 };
 size_t sparse_attn_smem_bytes();

@@ -1,13 +1,15 @@
 // schedule.cu -- inverts the block selection for the KV-outer Main Branch.
 //
 // For every incidence (query i, group g, slot) whose selected block b is
-// valid, the incidence goes to bucket (window(i), key block (s, b), g).  A
+// valid, the incidence goes to bucket (window(i), g, key block (s, b)).  A
 // counting sort (count, exclusive scan, scatter) gathers each bucket's queries
 // contiguously, and every bucket is cut into chunks of at most `qpc` queries
 // -- a block that many queries selected becomes several chunks, so no work item
-// is much larger than another.  Buckets are ordered window-major: the chunks
-// of one window of queries run together, which keeps that window's Q rows hot
-// in L2 while every key block they selected is visited.
+// is much larger than another.  Buckets are ordered window-major, then by
+// group: the chunks of one window and one group run together, so that group's
+// Q rows of the window and its K/V stay hot in L2 while every key block they
+// selected is visited.  Each chunk descriptor carries (begin, count,
+// g | b << 8, s) so the attention kernel needs no lookup.
 // (The atlas record of the report lists KV-outer sparse attention with query
 // gathering, pre-scheduled tile chunking for hot KV blocks and dynamic load
 // balancing; these kernels build that schedule on the device, with nothing
@@ -31,7 +33,7 @@ __device__ __forceinline__ bool incidence(const ScheduleParams& p, int64_t e, in
   const int pos = si.kv_len - si.q_len + (i - si.q_start);
   if (b > (pos >> 7)) return false;  // not a causal block of this query: ignored
   const long long w = i / p.window;
-  bucket = (w * p.total_blocks + p.blk_off[s] + b) * p.hkv + g;
+  bucket = (w * p.hkv + g) * p.total_blocks + p.blk_off[s] + b;
   return true;
 }
 
@@ -72,10 +74,15 @@ __global__ void sched_chunks_kernel(ScheduleParams p) {
   for (long long bk = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; bk < p.n_buckets;
        bk += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int cnt = p.count[bk];
+    if (cnt == 0) continue;
     const int begin = p.bucket_start[bk];
     const int c0 = p.chunk_start[bk];
+    const int g = static_cast<int>((bk / p.total_blocks) % p.hkv);
+    const int gb = static_cast<int>(bk % p.total_blocks);
+    const int s = find_seq(p.blk_off, p.num_seqs, gb);
+    const int b = gb - p.blk_off[s];
     for (int c = 0; c * p.qpc < cnt; ++c)
-      p.chunks[c0 + c] = make_int4(static_cast<int>(bk), begin + c * p.qpc, min(p.qpc, cnt - c * p.qpc), 0);
+      p.chunks[c0 + c] = make_int4(begin + c * p.qpc, min(p.qpc, cnt - c * p.qpc), g | (b << 8), s);
   }
 }
 

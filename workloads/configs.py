@@ -54,6 +54,9 @@ CONFIGS = {
     "decode_1m": Workload(
         "decode_1m", None, n_topics=256, seed=1014, decode_batch=8, decode_ctx=1048576,
         description="8 sequences x 1 query, KV cache 1048576-128+U{1..128}, k 16, 256 topics"),
+    "prefill_16k": Workload(
+        "prefill_16k", ((16384, 16384),), seed=1016,
+        description="T=N=16384 causal, Hq 64 / Hkv 4, d_idx 128, k 16, 64 topics (profiling size)"),
     "prefill_128k": Workload(
         "prefill_128k", ((131072, 131072),), seed=1010,
         description="T=N=131072 causal, Hq 64 / Hkv 4, d_idx 128, k 16, 64 topics"),
