@@ -91,6 +91,8 @@ _lib.msa_index_topk.argtypes = [_P, _vp, _vp, _vp, _vp, _sz, _vp]
 for _fn in (_lib.msa_sparse_attn_prefill, _lib.msa_sparse_attn_decode):
     _fn.restype = ctypes.c_int
     _fn.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.msa_sparse_attn_decode_static.restype = ctypes.c_int
+_lib.msa_sparse_attn_decode_static.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.msa_forward.restype = ctypes.c_int
 _lib.msa_forward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
@@ -103,7 +105,7 @@ _lib.msa_last_error_detail.restype = ctypes.c_char_p
 EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_index_topk",
             "msa_sparse_attn_prefill", "msa_sparse_attn_decode", "msa_forward",
             "msa_read_device_status", "msa_status_string", "msa_abi_version", "msa_set_stage_events",
-            "msa_kernel_launch_count", "msa_last_error_detail")
+            "msa_kernel_launch_count", "msa_last_error_detail", "msa_sparse_attn_decode_static")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 
@@ -250,6 +252,22 @@ def msa_sparse_attn_prefill(problem: Problem, q, k, v, idx, o=None, lse=None, ws
 def msa_sparse_attn_decode(problem: Problem, q, k, v, idx, o=None, lse=None, ws=None):
     return _attn(_lib.msa_sparse_attn_decode, Op.SPARSE_ATTN_DECODE, "msa_sparse_attn_decode", problem, q, k, v,
                  idx, o, lse, ws)
+
+
+def msa_sparse_attn_decode_static(problem: Problem, q, k, v, idx, o=None, lse=None):
+    """The decode Main Branch without a workspace: its scratch is a fixed device array inside the library
+    (for callers that cannot allocate device memory; see include/msa.h).  Calls share that array, so calls
+    that may overlap on the GPU must be serialised."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    _need(idx, torch.int32, "idx")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=q.device)
+    _check(_lib.msa_sparse_attn_decode_static(ctypes.byref(problem.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(idx),
+                                              _ptr(o), _ptr(lse), _stream()), "msa_sparse_attn_decode_static")
+    return o, lse
 
 
 def msa_forward(problem: Problem, q, k, v, q_idx, k_idx, idx=None, o=None, lse=None, ws=None):

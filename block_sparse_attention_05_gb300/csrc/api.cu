@@ -484,6 +484,42 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
 }  // namespace
 }  // namespace msa
 
+// ----------------------------------------------------------------------------
+// Fixed device scratch for msa_sparse_attn_decode_static: the workspace that
+// msa_sparse_attn_decode takes from its caller lives here instead.  Every GPU
+// that loads this library holds these bytes until the process exits.
+// ----------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t msa_static_scratch[MSA_STATIC_SCRATCH_BYTES];
+
+namespace msa {
+namespace {
+
+// Device address of msa_static_scratch on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is looked up
+// once per device with that device current, then cached.
+msa_status_t static_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, msa_static_scratch);
+    if (e != cudaSuccess || !ptr) {
+      std::snprintf(t_error_detail, sizeof t_error_detail, "cudaGetSymbolAddress of the static scratch: %s (%d)",
+                    cudaGetErrorName(e), static_cast<int>(e));
+      return MSA_ERR_CUDA;
+    }
+    addr[dev] = ptr;
+  }
+  *out = addr[dev];
+  return MSA_OK;
+}
+
+}  // namespace
+}  // namespace msa
+
 using namespace msa;
 
 extern "C" {
@@ -609,6 +645,32 @@ msa_status_t msa_sparse_attn_decode(const msa_problem_t* problem, const void* q,
   if ((st = begin(problem, MSA_OP_SPARSE_ATTN_DECODE, workspace, workspace_bytes, stream, c)) != MSA_OK)
     return st;
   if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  return run_attn_decode(problem, c, q, k, v, idx, o, lse);
+}
+
+msa_status_t msa_sparse_attn_decode_static(const msa_problem_t* problem, const void* q, const void* k,
+                                           const void* v, const int32_t* idx, void* o, float* lse,
+                                           msa_stream_t stream) {
+  t_error_detail[0] = 0;
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k, v, idx, o, lse)) != MSA_OK) return st;
+  const size_t need = layout(d, MSA_OP_SPARSE_ATTN_DECODE).total;
+  if (need > MSA_STATIC_SCRATCH_BYTES) {
+    std::snprintf(t_error_detail, sizeof t_error_detail,
+                  "this batch needs %zu bytes of scratch; the static buffer holds %zu", need,
+                  static_cast<size_t>(MSA_STATIC_SCRATCH_BYTES));
+    return MSA_ERR_WORKSPACE;
+  }
+  DeviceFacts dev;
+  if ((st = device_facts(dev)) != MSA_OK) return st;
+  void* scratch = nullptr;
+  if ((st = static_scratch_address(&scratch)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_SPARSE_ATTN_DECODE, scratch, MSA_STATIC_SCRATCH_BYTES, stream, c)) != MSA_OK)
+    return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;  // clears the scratch header first
   return run_attn_decode(problem, c, q, k, v, idx, o, lse);
 }
 

@@ -154,6 +154,33 @@ msa_status_t msa_sparse_attn_decode(const msa_problem_t *problem, const void *q,
                                     void *workspace, size_t workspace_bytes,
                                     msa_stream_t stream);
 
+/* Size of the device array behind msa_sparse_attn_decode_static (32 MiB). */
+#define MSA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* msa_sparse_attn_decode for callers that cannot allocate device memory: no
+ * workspace argument; the scratch lives in a fixed device array of
+ * MSA_STATIC_SCRATCH_BYTES that this library declares (every GPU that loads
+ * the library holds it until the process exits).  The method's pages have no
+ * counterpart to this call; it exists for code that runs where cudaMalloc is
+ * not available or not allowed -- a host framework that hands out only its
+ * own pre-allocated tensors, an allocator-free serving loop, a process whose
+ * memory pool is already fully reserved -- and that would otherwise have no
+ * way to provide the workspace.
+ * Arguments, layouts and results are those of msa_sparse_attn_decode.  The
+ * call allocates and frees nothing.  Batches whose scratch would exceed the
+ * array (about 120 decode sequences at 64 query / 4 KV heads and topk 16)
+ * return MSA_ERR_WORKSPACE, and msa_last_error_detail() states the bytes
+ * needed and available.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress, with that device current) and caches
+ * it; make that first call before any stream capture.  Every call uses the
+ * same array and leaves its contents behind (each call clears what must start
+ * at zero), so calls whose kernels may overlap on the GPU -- on different
+ * streams, or from several host threads -- race and must be serialised by the
+ * caller. */
+msa_status_t msa_sparse_attn_decode_static(const msa_problem_t *problem, const void *q,
+                                           const void *k, const void *v, const int32_t *idx,
+                                           void *o, float *lse, msa_stream_t stream);
+
 /* Both branches: msa_index_topk then the matching Main Branch call.  Writes
  * idx (the selection), o and lse. */
 msa_status_t msa_forward(const msa_problem_t *problem, const void *q, const void *k,
@@ -186,7 +213,8 @@ msa_status_t msa_set_stage_events(void *const *events);
 int64_t msa_kernel_launch_count(void);
 
 /* For the calling host thread: a description of the CUDA failure behind the
- * last MSA_ERR_CUDA (stage and CUDA error name), or "" if none. */
+ * last MSA_ERR_CUDA (stage and CUDA error name) -- or of the scratch shortfall
+ * behind an MSA_ERR_WORKSPACE from msa_sparse_attn_decode_static -- or "". */
 const char *msa_last_error_detail(void);
 
 /* Static description of a status code. */
