@@ -44,7 +44,6 @@ struct StageScope {
 
 constexpr size_t kAlign = 256;
 constexpr int kWindow = 4096;       // queries per scheduling window
-constexpr int kTilesPerChunk = 16;  // Main Branch tiles per work item
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -59,7 +58,7 @@ struct Derived {
 
 struct Layout {
   size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, count, bstart, bcursor, nchunk, cstart,
-      entries, chunks, scan_tmp, part_o, part_lse, total;
+      entries, chunks, scan_tmp, v16, part_o, part_lse, part_ow, total;
 };
 
 msa_status_t derive(const msa_problem_t* p, Derived& d) {
@@ -142,10 +141,12 @@ Layout layout(const Derived& d, msa_op_t op) {
     L.entries = take(sizeof(int32_t) * (d.n_inc > 0 ? d.n_inc : 1));
     L.chunks = take(sizeof(int4) * (d.max_chunks > 0 ? d.max_chunks : 1));
     L.scan_tmp = take(sizeof(int32_t) * scan_tmp_ints(static_cast<int>(d.n_buckets)));
+    L.v16 = take(sizeof(__half) * static_cast<size_t>(d.N) * d.hkv * kHeadDim);
   }
   if (op_uses_prefill_attn(op, d) || op_uses_decode_attn(op, d)) {
     L.part_o = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.n_inc) * d.G * kHeadDim);
     L.part_lse = take(sizeof(float) * static_cast<size_t>(d.n_inc) * d.G);
+    L.part_ow = take(sizeof(float) * static_cast<size_t>(d.n_inc) * d.G);
   }
   L.total = off;
   return L;
@@ -201,11 +202,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // bf16 tensor of `rank` dims (innermost first), 128-byte swizzle, zero fill.
 bool make_map(CUtensorMap& m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides_bytes, box,
+  CUresult r = fn(&m, dtype, rank, const_cast<void*>(ptr), dims, strides_bytes, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -223,11 +224,12 @@ bool map_2d(CUtensorMap& m, const void* ptr, long long rows, int cols, int box_r
 }
 
 // [n, heads, 128] row-major, box = 64 dims x box_heads heads x box_rows rows
-bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_heads, int box_rows) {
+bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_heads, int box_rows,
+            CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(n > 0 ? n : 1)};
   cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
-  return make_map(m, ptr, 3, dims, strides, box);
+  return make_map(m, ptr, 3, dims, strides, box, dtype);
 }
 
 // ---------------------------------------------------------------- common prologue
@@ -378,6 +380,7 @@ PartialBuffers partials(Ctx& c) {
   PartialBuffers pb;
   pb.o = at<__nv_bfloat16>(c.ws, c.L.part_o);
   pb.lse = at<float>(c.ws, c.L.part_lse);
+  pb.ow = at<float>(c.ws, c.L.part_ow);
   return pb;
 }
 
@@ -433,9 +436,10 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
   }
   if (st != MSA_OK) return st;
 
+  __half* v16 = at<__half>(c.ws, c.L.v16);
   CUtensorMap tq, tk, tv;
   if (!map_3d(tq, q, c.d.T, c.d.hq, c.d.G, 1) || !map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) ||
-      !map_3d(tv, v, c.d.N, c.d.hkv, 1, 128))
+      !map_3d(tv, v16, c.d.N, c.d.hkv, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return MSA_ERR_CUDA;
   AttnParams ap{};
   ap.seq = c.seq;
@@ -450,7 +454,9 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
   ap.scale_log2 = c.d.scale * 1.4426950408889634f;
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);
-    st = cuda_status(launch_sparse_attn(tq, tk, tv, ap, c.dev.sms, c.stream));
+    st = cuda_status(launch_v_prep(static_cast<const __nv_bfloat16*>(v), v16,
+                                   static_cast<long long>(c.d.N) * c.d.hkv * kHeadDim, c.hdr, c.dev.sms, c.stream));
+    if (st == MSA_OK) st = cuda_status(launch_sparse_attn(tq, tk, tv, ap, c.dev.sms, c.stream));
   }
   if (st != MSA_OK) return st;
   return run_combine(p, c, idx, o, lse);

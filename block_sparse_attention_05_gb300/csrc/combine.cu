@@ -5,6 +5,9 @@
 // output normalised within the block, O_s, and its log-sum-exp L_s.  Exact
 // softmax attention over the union of the blocks is then
 //     L = log sum_s exp(L_s),   O = sum_s exp(L_s - L) O_s .
+// The stored partial is U_s = O_s exp(L_s - W_s) with its own log weight W_s
+// (W_s = L_s when it is stored normalised), so the merge is
+//     O = sum_s exp(W_s - L) U_s .
 // (The atlas record of the report lists a two-phase combine with per-partial
 // LSE buffers and no atomics; this kernel is that second phase.)
 //
@@ -35,18 +38,22 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
   const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
   const int64_t sel_base = (static_cast<int64_t>(i) * p.hkv + g) * p.topk;
 
-  float l_s = -INFINITY;
+  float l_s = -INFINITY, w_s = -INFINITY;
   if (lane < p.topk) {
     const int b = p.idx[sel_base + lane];
-    if (b >= 0 && b <= local) l_s = p.part.lse[(sel_base + lane) * p.group + hh];
+    if (b >= 0 && b <= local) {
+      l_s = p.part.lse[(sel_base + lane) * p.group + hh];
+      w_s = p.part.ow[(sel_base + lane) * p.group + hh];
+    }
   }
   float m = l_s;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  float w = (l_s == -INFINITY) ? 0.f : expf(l_s - m);
-  float sum = w;
+  float sum = (l_s == -INFINITY) ? 0.f : expf(l_s - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  const float L = m + logf(sum);
+  const float w = (l_s == -INFINITY) ? 0.f : expf(w_s - L);
 
   // issue every slot's load before using any (memory-level parallelism)
   const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + lane * 4;
@@ -71,14 +78,13 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
     acc[3] = fmaf(ws, __high2float(b), acc[3]);
   }
   const bool empty = (m == -INFINITY);
-  const float inv = empty ? 0.f : 1.f / sum;
-  __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
-  __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+  __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[0], acc[1]);
+  __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[2], acc[3]);
   uint2 out;
   out.x = *reinterpret_cast<uint32_t*>(&o01);
   out.y = *reinterpret_cast<uint32_t*>(&o23);
   *reinterpret_cast<uint2*>(p.o + row * kHeadDim + lane * 4) = out;
-  if (lane == 0) p.lse[row] = empty ? -INFINITY : m + logf(sum);
+  if (lane == 0) p.lse[row] = empty ? -INFINITY : L;
 }
 
 }  // namespace

@@ -445,7 +445,9 @@ __global__ void __launch_bounds__(kDecThreads)
       const float mw = red[(w * 16 + h) * 2];
       if (mw != -INFINITY) L += red[(w * 16 + h) * 2 + 1] * exp2f(mw - M);
     }
-    p.part.lse[sel * G + h] = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+    const float lse = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+    p.part.lse[sel * G + h] = lse;
+    p.part.ow[sel * G + h] = lse;  // o is stored normalised
   }
 }
 

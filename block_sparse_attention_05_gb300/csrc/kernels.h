@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -83,11 +84,23 @@ size_t decode_scan_smem_bytes();
 cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- main branch
-// Partial results of one (query, group, slot): G rows of 128 bf16 + G lse.
+// Partial results of one (query, group, slot): G rows of 128 bf16 + G lse + G
+// log weights.  The true partial output (normalised within the block) is
+// o * exp(ow - lse): the decode kernel stores it as is (ow = lse), the prefill
+// kernel over V scaled by 2^-e (ow = lse + e ln 2).
 struct PartialBuffers {
   __nv_bfloat16* o;   // [total_q, hkv, topk, G, 128]
   float* lse;         // [total_q, hkv, topk, G]
+  float* ow;          // [total_q, hkv, topk, G]
 };
+
+// fp16 copy of V for the prefill Main Branch: V * 2^-v_scale_shift(max |V|).
+// Two launches: max |V| into hdr->vmax_bits (zeroed by the caller), then the copy.
+cudaError_t launch_v_prep(const __nv_bfloat16* v, __half* v16, long long n_elems, WsHeader* hdr, int sms,
+                          cudaStream_t stream);
+
+// Main Branch work item: at most this many tiles (of qpt <= 16 queries each).
+constexpr int kTilesPerChunk = 16;
 
 struct ScheduleParams {
   int num_seqs, total_q, hkv, topk, window, total_blocks, n_windows, qpc;

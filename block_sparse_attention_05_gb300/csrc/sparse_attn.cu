@@ -14,25 +14,25 @@
 // (128 tokens x 128 dims each) are loaded once by TMA; the queries are taken
 // qpt at a time (qpt x G heads = 128 rows; G = 16 gives 8 queries per tile),
 // their Q rows gathered by TMA.  Per tile:
-//   S = Q K^T                 tcgen05, 128 x 128 x 128, fp32 in TMEM
-//   P = exp2(S*c - max)       softmax warpgroup, one TMEM lane (row) per thread,
+//   S = Q K^T                 tcgen05 (bf16), 128 x 128 x 128, fp32 in TMEM
+//   P = exp2(S*c - m)         softmax warpgroup, one TMEM lane (row) per thread,
 //                             causal limit per row (only the local block is cut);
-//                             P is split into bf16 hi + lo parts written back
-//                             over S in TMEM (each 32-key chunk over its own
-//                             columns: 16 hi, then 16 lo)
-//   O = P_hi V + P_lo V       tcgen05 with A read from TMEM, V MN-major in smem
-//   partial O / l and LSE     written per (query, group, slot, head)
-// The tile covers exactly one key block, so no running rescale is needed.
+//                             one pass over S; P written back over S in TMEM
+//                             as fp16, m a per-row reference (below)
+//   U = P V16                 tcgen05 (fp16) with A read from TMEM, V16 = the
+//                             fp16 copy of V, MN-major in smem
+//   U / l, LSE, log weight    written per (query, group, slot, head); the log
+//                             weight W = LSE + e ln 2 undoes V's 2^-e scale
+// The tile covers exactly one key block, so no running rescale of U is needed.
 //
 // Warp roles (512 threads): warp 0 = TMA producer and chunk claiming, warps 1
 // and 3 = one MMA issuer per softmax warpgroup, warp 2 = TMEM allocator,
-// warps 4..7 and 8..11 = two
-// softmax warpgroups taking alternate tiles (each owns an S/P and an O
-// accumulator in TMEM: 2 x (128 + 128) = 512 columns), warps 12..15 = the
-// epilogue warpgroup (O read-back, normalisation, partial stores) for every
-// tile.  The softmax warpgroups hand each row's max and sum to the epilogue
-// through a 4-slot shared buffer.  Q tiles live in a 2-stage ring, freed as
-// soon as QK^T retires; K/V are double-buffered across chunks.
+// warps 4..7 and 8..11 = two softmax warpgroups taking alternate tiles (each
+// owns an S/P and a U accumulator in TMEM: 2 x (128 + 128) = 512 columns),
+// warps 12..15 = the epilogue warpgroup (U read-back, normalisation, partial
+// stores) for every tile, which gets each row's sum of P through a 4-slot
+// shared buffer.  Q tiles live in a 2-stage ring, freed as soon as
+// QK^T retires; K/V are double-buffered across chunks.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -48,14 +48,31 @@ constexpr int kKVBytes = 2 * kQTileBytes;     // K + V of one block, 64 KB
 constexpr int kAttnThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
+struct ChunkInfo {
+  int g, b, s, begin, count, ntile, krow;
+};
+
+// Per tile and row, softmax -> epilogue: the sum of P and where the row goes
+// (0 for a padding row).
+struct RowStat {
+  float l;
+  int pad;
+  unsigned long long orow;
+};
+
+constexpr int kMaxChunkEntries = 16 * kTilesPerChunk;  // qpt <= 16 queries per tile
+
 struct AttnSmem {
+  uint8_t stage[4][32 * 64];     // epilogue: per warp, 32 rows x 32 bf16 (one quarter of the row)
+  int ent[2][kMaxChunkEntries];  // producer: entries of the current and the next chunk
   uint64_t q_full[kQStages], q_empty[kQStages];
   uint64_t kv_full[2], kv_empty[2];
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2];
   uint64_t stat_full[kStatSlots];
   uint64_t work_full[kWorkSlots], work_empty[kWorkSlots];
   uint64_t mma_done[2];
-  float2 stat[kStatSlots][128];  // per tile slot and row: (max in scaled log2 units, sum of P)
+  RowStat stat[kStatSlots][128];
+  ChunkInfo work_ci[kWorkSlots];  // the published chunks, decoded by the producer
   int work[kWorkSlots];
   uint32_t tmem_base;
   int abort_flag;
@@ -63,9 +80,6 @@ struct AttnSmem {
 
 constexpr size_t kAttnSmemBytes = 1024 + 2 * kKVBytes + kQStages * kQTileBytes + sizeof(AttnSmem);
 
-struct ChunkInfo {
-  int g, b, s, begin, count, ntile, krow;
-};
 
 __device__ __forceinline__ ChunkInfo decode_chunk(const AttnParams& p, int item) {
   const int4 c = p.chunks[item];
@@ -168,58 +182,96 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
+  const float v_shift = static_cast<float>(v_scale_shift(hdr->vmax_bits));  // V copy = V * 2^-v_shift
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      uint32_t q_iter = 0, kv_iter = 0;
-      for (uint32_t w = 0;; ++w) {
-        const int slot = w % kWorkSlots;
-        if (w >= kWorkSlots &&
-            !mbar_wait(&sm.work_empty[slot], ((w / kWorkSlots) - 1) & 1, abort_flag)) {
-          report_timeout(abort_flag, hdr, 201);
-          break;
-        }
-        const int u = static_cast<int>(atomicAdd(&hdr->counter[1], 1u));
-        const int item = (u < n_chunks && !*abort_flag) ? u : -1;
+    // ------------------------------------------------------------ producer warp
+    // Claims chunks one ahead of the one it feeds: while chunk w's K/V and Q
+    // tiles are loaded into shared memory, chunk w+1's entries already sit in
+    // shared memory and its K, V and Q rows are on their way into L2, so the
+    // Q gathers of the next chunk find their rows there.
+    uint32_t q_iter = 0, kv_iter = 0;
+    auto claim = [&]() -> int {
+      int u = -1;
+      if (lane == 0) {
+        u = static_cast<int>(atomicAdd(&hdr->counter[1], 1u));
+        if (u >= n_chunks || *abort_flag) u = -1;
+      }
+      return __shfl_sync(0xFFFFFFFFu, u, 0);
+    };
+    auto stage_chunk = [&](int item, int buf) {
+      if (item < 0) return;
+      const ChunkInfo ci = decode_chunk(p, item);
+      for (int e = lane; e < ci.count; e += 32) {
+        const int ent = p.entries[ci.begin + e];
+        sm.ent[buf][e] = ent;
+        tma_prefetch_3d(&tm_q, 0, ci.g * G, ent >> 5);
+        tma_prefetch_3d(&tm_q, 64, ci.g * G, ent >> 5);
+      }
+      if (lane < 4) tma_prefetch_3d((lane & 2) ? &tm_v : &tm_k, (lane & 1) * 64, ci.g, ci.krow);
+      __syncwarp();
+    };
+    int cur = claim();
+    stage_chunk(cur, 0);
+    for (uint32_t w = 0;; ++w) {
+      const int item = cur;
+      const int buf = w & 1;
+      int nxt = -1;
+      if (item >= 0) {
+        nxt = claim();
+        stage_chunk(nxt, buf ^ 1);  // chunk w-1's loads are all issued: its entries are free
+      }
+      const int slot = w % kWorkSlots;
+      if (w >= kWorkSlots && !mbar_wait_warp(&sm.work_empty[slot], ((w / kWorkSlots) - 1) & 1, abort_flag)) {
+        if (lane == 0) report_timeout(abort_flag, hdr, 201);
+        break;
+      }
+      ChunkInfo ci{};
+      if (item >= 0) ci = decode_chunk(p, item);
+      if (lane == 0) {
         sm.work[slot] = item;
+        sm.work_ci[slot] = ci;
         mbar_arrive(&sm.work_full[slot]);
-        if (item < 0) break;
-        const ChunkInfo ci = decode_chunk(p, item);
-        const int kvb = kv_iter & 1;
-        if (kv_iter >= 2 && !mbar_wait(&sm.kv_empty[kvb], ((kv_iter >> 1) - 1) & 1, abort_flag)) {
-          report_timeout(abort_flag, hdr, 202);
-          break;
-        }
+      }
+      if (item < 0) break;
+      const int kvb = kv_iter & 1;
+      if (kv_iter >= 2 && !mbar_wait_warp(&sm.kv_empty[kvb], ((kv_iter >> 1) - 1) & 1, abort_flag)) {
+        if (lane == 0) report_timeout(abort_flag, hdr, 202);
+        break;
+      }
+      if (lane == 0) {
         uint8_t* kvp = kv_buf + kvb * kKVBytes;
         mbar_arrive_expect_tx(&sm.kv_full[kvb], kKVBytes);
         tma_load_3d(kvp, &tm_k, &sm.kv_full[kvb], 0, ci.g, ci.krow);
         tma_load_3d(kvp + 16384, &tm_k, &sm.kv_full[kvb], 64, ci.g, ci.krow);
         tma_load_3d(kvp + 32768, &tm_v, &sm.kv_full[kvb], 0, ci.g, ci.krow);
         tma_load_3d(kvp + 49152, &tm_v, &sm.kv_full[kvb], 64, ci.g, ci.krow);
-        ++kv_iter;
-        bool ok = true;
-        for (int tt = 0; tt < ci.ntile; ++tt) {
-          const int qs = q_iter % kQStages;
-          if (q_iter >= kQStages &&
-              !mbar_wait(&sm.q_empty[qs], ((q_iter / kQStages) - 1) & 1, abort_flag)) {
-            report_timeout(abort_flag, hdr, 203);
-            ok = false;
-            break;
-          }
-          uint8_t* qp = q_buf + qs * kQTileBytes;
-          mbar_arrive_expect_tx(&sm.q_full[qs], kQTileBytes);
-          for (int ql = 0; ql < p.qpt; ++ql) {
-            int e = ci.begin + tt * p.qpt + ql;
-            if (e >= ci.begin + ci.count) e = ci.begin;  // pad the last tile with a real row
-            const int qi = p.entries[e] >> 5;
-            tma_load_3d(qp + ql * G * 128, &tm_q, &sm.q_full[qs], 0, ci.g * G, qi);
-            tma_load_3d(qp + 16384 + ql * G * 128, &tm_q, &sm.q_full[qs], 64, ci.g * G, qi);
-          }
-          ++q_iter;
-        }
-        if (!ok) break;
       }
+      ++kv_iter;
+      bool ok = true;
+      for (int tt = 0; tt < ci.ntile; ++tt) {
+        const int qs = q_iter % kQStages;
+        if (q_iter >= kQStages && !mbar_wait_warp(&sm.q_empty[qs], ((q_iter / kQStages) - 1) & 1, abort_flag)) {
+          if (lane == 0) report_timeout(abort_flag, hdr, 203);
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qs], kQTileBytes);
+        __syncwarp();
+        if (lane < p.qpt) {  // one lane per query row of the tile
+          int e = tt * p.qpt + lane;
+          if (e >= ci.count) e = 0;  // pad the last tile with a real row
+          const int qi = sm.ent[buf][e] >> 5;
+          uint8_t* qp = q_buf + qs * kQTileBytes + lane * G * 128;
+          tma_load_3d(qp, &tm_q, &sm.q_full[qs], 0, ci.g * G, qi);
+          tma_load_3d(qp + 16384, &tm_q, &sm.q_full[qs], 64, ci.g * G, qi);
+        }
+        ++q_iter;
+      }
+      if (!ok) break;
+      cur = nxt;
+    }
+    if (lane == 0) {
       for (int s = 0; s < kQStages; ++s)
         if (q_iter > static_cast<uint32_t>(s)) {
           const uint32_t last = ((q_iter - 1 - s) / kQStages) * kQStages + s;
@@ -239,7 +291,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (lane == 0) {
       const int wg = (warp == 1) ? 0 : 1;
       const uint32_t idesc_qk = idesc_bf16(128, 128, false);
-      const uint32_t idesc_pv = idesc_bf16(128, 128, true);
+      const uint32_t idesc_pv = idesc_f16(128, 128, true);
       const uint32_t s_col = tmem + wg * 256, o_col = tmem + wg * 256 + 128;
       uint32_t w_iter = 0, kv_iter = 0, t = 0;
       bool ok = true;
@@ -250,10 +302,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         const int item = sm.work[slot];
+        const ChunkInfo ci = sm.work_ci[slot];
         mbar_arrive(&sm.work_empty[slot]);
         ++w_iter;
         if (item < 0) break;
-        const ChunkInfo ci = decode_chunk(p, item);
         const int kvb = kv_iter & 1;
         // every issuer waits for every chunk's K/V, used or not, so that it can
         // never arrive on kv_empty for a later use of this buffer too early
@@ -287,7 +339,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           umma_commit(&sm.s_full[wg]);
           umma_commit(&sm.q_empty[wg]);  // the Q stage is free once QK^T has retired
-          // ---- O = P_hi V + P_lo V
+          // ---- U = P V (fp16)
           if (!mbar_wait(&sm.p_full[wg], n & 1, abort_flag) ||
               (n >= 1 && !mbar_wait(&sm.o_free[wg], (n - 1) & 1, abort_flag))) {
             report_timeout(abort_flag, hdr, 214);
@@ -295,15 +347,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             break;
           }
           tc_fence_after();
-          // P sits in the S columns of TMEM as bf16 pairs, per 32 keys: the high
-          // parts (16 columns), then the low parts (p - bf16(p), 16 columns).
-          // K-step kk covers keys 16kk..16kk+15.
+          // P sits in the S columns of TMEM as fp16 pairs: K-step kk (keys
+          // 16kk..16kk+15) in columns 8kk..8kk+7.
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              umma_bf16_ts(o_col, s_col + (kk >> 1) * 32 + part * 16 + (kk & 1) * 8,
-                           sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, (part | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_bf16_ts(o_col, s_col + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, kk ? 1u : 0u);
           umma_commit(&sm.o_full[wg]);
           umma_commit(&sm.s_free[wg]);  // S/P columns reusable once PV has retired
           if (m == mine - 1) umma_commit(&sm.kv_empty[kvb]);
@@ -330,11 +378,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       const int item = sm.work[slot];
+      const ChunkInfo ci = sm.work_ci[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.work_empty[slot]);
       ++w_iter;
       if (item < 0) break;
-      const ChunkInfo ci = decode_chunk(p, item);
       for (int tt = 0; tt < ci.ntile; ++tt, ++t) {
         if ((t & 1) != static_cast<uint32_t>(wg)) continue;
         const uint32_t n = t >> 1;
@@ -345,62 +393,120 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        // pass 1: row max over the visible keys (raw scores)
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32cols(lane_addr + c * 32, v);
-          tmem_ld_wait();
-          if (ri.lim >= 127) {
+        // One pass over S, 16 keys at a time, each chunk's load issued one chunk
+        // ahead.  The exponent reference m starts at the max of the first
+        // chunk's visible keys; a later chunk whose max exceeds it by more than
+        // 2^15 first rescales the P already stored by an exact power of two and
+        // raises m (rare), so every P lies in [0, 2^15] and fits fp16.  P goes
+        // back over the chunk's own S columns as fp16 pairs: keys 16c..16c+15
+        // -> columns 8c..8c+7.  With l = sum_k P_k the epilogue stores
+        // U / l, U = sum_k P_k v_k over V scaled by 2^-e: the block's normalised
+        // output times 2^-e, so its LSE is (m + log2 l) ln 2 and its log weight
+        // that LSE + e ln 2.
+        const int lim = ri.valid ? ri.lim : kBlock - 1;  // padding rows: computed, never stored
+        const bool warp_full = __all_sync(0xFFFFFFFFu, lim >= kBlock - 1);
+        float l = 0.f, m_ref = 0.f;
+        {
+          uint32_t va[16], vb[16];
+          tmem_ld_16cols(lane_addr, va);
+          tmem_ld_wait_regs16(va);
+          float m0 = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(v[j]));
+          for (int j = 0; j < 16; ++j) m0 = fmaxf(m0, (j <= lim) ? __uint_as_float(va[j]) : -INFINITY);
+          if (m0 != -INFINITY) m_ref = m0 * p.scale_log2;
+          auto process = [&](const uint32_t (&v)[16], int c, bool masked) {
+            float sv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              sv[j] = (!masked || c * 16 + j <= lim) ? __uint_as_float(v[j]) : -INFINITY;
+            float cm = fmax3(sv[0], sv[1], sv[2]);
+#pragma unroll
+            for (int j = 3; j < 15; j += 2) cm = fmax3(cm, sv[j], sv[j + 1]);
+            cm = fmaxf(cm, sv[15]);
+            // The rescale uses warp-collective TMEM loads and stores, so the
+            // whole warp enters it when any of its rows needs it; the other rows
+            // scale by exactly 1.
+            const bool need = cm != -INFINITY && cm * p.scale_log2 - m_ref > 15.f;
+            if (__any_sync(0xFFFFFFFFu, need)) {
+              const float kexp = need ? ceilf(cm * p.scale_log2 - m_ref) : 0.f;
+              const __half2 f2 = __float2half2_rn(exp2f(-kexp));
+              tmem_st_wait();
+              for (int cc = 0; cc < c; ++cc) {
+                uint32_t w8[8];
+                tmem_ld_8cols(lane_addr + cc * 8, w8);
+                tmem_ld_wait_regs8(w8);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w8[j]), f2);
+                  w8[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                tmem_st_8cols(lane_addr + cc * 8, w8);
+              }
+              l *= exp2f(-kexp);
+              m_ref += kexp;
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float x0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_ref));
+              const float x1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_ref));
+              l += x0 + x1;
+              const __half2 h = __floats2half2_rn(x0, x1);
+              pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            tmem_st_8cols(lane_addr + c * 8, pk);
+          };
+          if (warp_full) {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+              tmem_ld_16cols(lane_addr + (2 * i + 1) * 16, vb);
+              process(va, 2 * i, false);
+              tmem_ld_wait_regs16(vb);
+              if (i < 3) tmem_ld_16cols(lane_addr + (2 * i + 2) * 16, va);
+              process(vb, 2 * i + 1, false);
+              if (i < 3) tmem_ld_wait_regs16(va);
+            }
           } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, (c * 32 + j <= ri.lim) ? __uint_as_float(v[j]) : -INFINITY);
-          }
-        }
-        const float ms = (mx == -INFINITY) ? 0.f : mx * p.scale_log2;  // max in scaled log2 units
-        // pass 2: P = 2^(s*c - ms), its sum, and the bf16 hi + lo split written over S
-        float l = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32cols(lane_addr + c * 32, v);
-          tmem_ld_wait();
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int k0 = c * 32 + 2 * j;
-            float a = exp2_approx(fmaf(__uint_as_float(v[2 * j]), p.scale_log2, -ms));
-            float b = exp2_approx(fmaf(__uint_as_float(v[2 * j + 1]), p.scale_log2, -ms));
-            if (k0 > ri.lim) a = 0.f;
-            if (k0 + 1 > ri.lim) b = 0.f;
-            l += a + b;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-            hi[j] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[j] = pack_bf16(a - __low2float(h), b - __high2float(h));
+            for (int i = 0; i < 4; ++i) {
+              tmem_ld_16cols(lane_addr + (2 * i + 1) * 16, vb);
+              process(va, 2 * i, true);
+              tmem_ld_wait_regs16(vb);
+              if (i < 3) tmem_ld_16cols(lane_addr + (2 * i + 2) * 16, va);
+              process(vb, 2 * i + 1, true);
+              if (i < 3) tmem_ld_wait_regs16(va);
+            }
           }
-          // keys 32c..32c+31 of this row: hi pairs to columns 32c..32c+15, lo pairs
-          // to 32c+16..32c+31 -- only columns this pass has already read
-          tmem_st_16cols(lane_addr + c * 32, hi);
-          tmem_st_16cols(lane_addr + c * 32 + 16, lo);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[wg]);
-        sm.stat[t % kStatSlots][r] = make_float2(mx == -INFINITY ? -INFINITY : ms, l);
+        {
+          RowStat rs;
+          rs.l = l;
+          rs.pad = 0;
+          rs.orow = ri.valid ? reinterpret_cast<unsigned long long>(
+                                   p.part.o +
+                                   ((static_cast<int64_t>(ri.qi) * p.hkv + ci.g) * p.topk + ri.slot) * G * kHeadDim +
+                                   static_cast<int64_t>(hh) * kHeadDim)
+                             : 0ull;
+          sm.stat[t % kStatSlots][r] = rs;
+        }
         mbar_arrive(&sm.stat_full[t % kStatSlots]);
-        if (ri.valid)
-          p.part.lse[((static_cast<int64_t>(ri.qi) * p.hkv + ci.g) * p.topk + ri.slot) * G + hh] =
-              (mx == -INFINITY) ? -INFINITY : (ms + log2f(l)) * kLn2;
+        if (ri.valid) {
+          const int64_t at = ((static_cast<int64_t>(ri.qi) * p.hkv + ci.g) * p.topk + ri.slot) * G + hh;
+          const bool empty = lim < 0;
+          const float lse2 = m_ref + log2f(l);
+          p.part.lse[at] = empty ? -INFINITY : lse2 * kLn2;
+          p.part.ow[at] = empty ? -INFINITY : (lse2 + v_shift) * kLn2;
+        }
       }
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------------ epilogue
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    const int q_local = r / G, hh = r % G;
+    uint8_t* stg = sm.stage[warp & 3];
     uint32_t t = 0, w_iter = 0;
     bool ok = true;
     while (ok) {
@@ -410,14 +516,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         break;
       }
       const int item = sm.work[slot];
+      const ChunkInfo ci = sm.work_ci[slot];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.work_empty[slot]);
       ++w_iter;
       if (item < 0) break;
-      const ChunkInfo ci = decode_chunk(p, item);
       for (int tt = 0; tt < ci.ntile; ++tt, ++t) {
         const int w = t & 1;
-        const RowInfo ri = row_info(p, ci, tt, q_local);
         if (!mbar_wait_warp(&sm.o_full[w], (t >> 1) & 1, abort_flag) ||
             !mbar_wait_warp(&sm.stat_full[t % kStatSlots], (t / kStatSlots) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 232);
@@ -425,30 +530,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        const float2 st = sm.stat[t % kStatSlots][r];
-        const float inv_l = (st.y > 0.f) ? 1.f / st.y : 0.f;
-        __nv_bfloat16* orow =
-            p.part.o + ((static_cast<int64_t>(ri.qi) * p.hkv + ci.g) * p.topk + ri.slot) * G * kHeadDim +
-            static_cast<int64_t>(hh) * kHeadDim;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld_32cols(lane_addr + w * 256 + 128 + c * 32, o);
-          tmem_ld_wait();
-          if (ri.valid) {
+        const RowStat rs = sm.stat[t % kStatSlots][r];
+        const float inv_l = (rs.l > 0.f) ? 1.f / rs.l : 0.f;
+        // Each lane owns one row (one TMEM lane); the rows of one query are
+        // contiguous in the partial buffer.  A quarter of the row (32 values)
+        // at a time goes through this warp's staging area (16-byte chunks
+        // XOR-swizzled by row pair, so neither side has bank conflicts) and
+        // leaves as 16-byte stores that fill whole 64-byte runs of 8 rows.
+        const unsigned long long orow = rs.orow;
+        unsigned long long rowp[4];
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[j + 0]) * inv_l, __uint_as_float(o[j + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[j + 2]) * inv_l, __uint_as_float(o[j + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[j + 4]) * inv_l, __uint_as_float(o[j + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[j + 6]) * inv_l, __uint_as_float(o[j + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + c * 32 + j) = v;
-            }
+        for (int k = 0; k < 4; ++k) rowp[k] = __shfl_sync(0xFFFFFFFFu, orow, 8 * k + (lane >> 2));
+        const int ck = lane & 3;  // the 16-byte chunk this lane stores
+        auto emit = [&](const uint32_t (&o)[32], int quarter) {
+          uint4 pk[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            pk[c].x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+            pk[c].y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+            pk[c].z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+            pk[c].w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk[c];
           }
-        }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int R = 8 * k + (lane >> 2);
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + R * 64 + ((ck ^ ((R >> 1) & 3)) << 4));
+            if (rowp[k]) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(rowp[k]) + quarter * 32 + ck * 8) = v;
+          }
+          __syncwarp();
+        };
+        uint32_t va[32], vb[32];
+        const uint32_t o_addr = lane_addr + w * 256 + 128;
+        tmem_ld_32cols(o_addr, va);
+        tmem_ld_wait_regs(va);
+        tmem_ld_32cols(o_addr + 32, vb);
+        emit(va, 0);
+        tmem_ld_wait_regs(vb);
+        tmem_ld_32cols(o_addr + 64, va);
+        emit(vb, 1);
+        tmem_ld_wait_regs(va);
+        tmem_ld_32cols(o_addr + 96, vb);
+        emit(va, 2);
+        tmem_ld_wait_regs(vb);
         tc_fence_before();
-        mbar_arrive(&sm.o_free[w]);
+        mbar_arrive(&sm.o_free[w]);  // every read of this U accumulator is done
+        emit(vb, 3);
       }
     }
   }

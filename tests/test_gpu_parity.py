@@ -135,6 +135,24 @@ def test_sparse_attn_prefill_random_selections(msa):
     assert_attention_close(to_np(o), to_np(lse), {"o": o_ref, "lse": lse_ref}, 16, what="random selections")
 
 
+@pytest.mark.parametrize("shift", [20, 100])
+def test_sparse_attn_prefill_large_values(msa, shift):
+    """V far outside fp16's range: attention is linear in V, so V * 2^shift (exact
+    in bf16) must give exactly 2^shift times the oracle's output for V and the
+    same LSE.  Compared after dividing by 2^shift, at the usual tolerance."""
+    cfg = make_small("varlen_g16", seed=9)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    idx = torch.from_numpy(ref["idx"]).cuda()
+    big = x.v * float(2.0 ** shift)
+    assert torch.isfinite(big.float()).all()
+    o, lse = msa.msa_sparse_attn_prefill(prob, x.q, x.k, big, idx)
+    torch.cuda.synchronize()
+    o_scaled = to_np(o).astype(np.float64) / 2.0 ** shift
+    assert_attention_close(o_scaled, to_np(lse), ref, cfg.hq // cfg.hkv, what=f"V * 2^{shift}")
+
+
 # ------------------------------------------------------------------ end to end (prefill)
 @pytest.mark.parametrize("name", ["varlen_g16", "tiny_shape_short", "k_covers_all"])
 def test_forward_prefill_end_to_end(msa, name):
