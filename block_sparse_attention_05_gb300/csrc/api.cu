@@ -442,6 +442,7 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
       !map_3d(tv, v16, c.d.N, c.d.hkv, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return MSA_ERR_CUDA;
   AttnParams ap{};
+  ap.q = static_cast<const __nv_bfloat16*>(q);
   ap.seq = c.seq;
   ap.chunks = sp.chunks;
   ap.entries = sp.entries;

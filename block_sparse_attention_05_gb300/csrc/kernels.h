@@ -122,6 +122,7 @@ struct ScheduleParams {
 cudaError_t launch_schedule(const ScheduleParams& p, cudaStream_t stream);
 
 struct AttnParams {
+  const __nv_bfloat16* q;  // [total_q, hq, 128] (also behind tm_q; read directly for L2 prefetches)
   const SeqInfo* seq;
   const int4* chunks;
   const int32_t* entries;

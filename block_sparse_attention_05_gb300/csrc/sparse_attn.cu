@@ -43,6 +43,7 @@ namespace {
 constexpr int kQStages = 2;
 constexpr int kWorkSlots = 4;
 constexpr int kStatSlots = 4;
+constexpr int kQPrefetch = 4;  // Q rows are prefetched into L2 this many tiles ahead of their gather
 constexpr int kQTileBytes = 128 * 128 * 2;   // 32 KB
 constexpr int kKVBytes = 2 * kQTileBytes;     // K + V of one block, 64 KB
 constexpr int kAttnThreads = 512;
@@ -188,8 +189,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------ producer warp
     // Claims chunks one ahead of the one it feeds: while chunk w's K/V and Q
     // tiles are loaded into shared memory, chunk w+1's entries already sit in
-    // shared memory and its K, V and Q rows are on their way into L2, so the
-    // Q gathers of the next chunk find their rows there.
+    // shared memory and its K and V are on their way into L2.  Along with the
+    // Q gather of each tile, the Q rows of the tile kQPrefetch places later
+    // (in this chunk or the next) are prefetched into L2, so that the gathers
+    // find their rows there; spread this way, the prefetches never queue up
+    // in front of a gather.
     uint32_t q_iter = 0, kv_iter = 0;
     auto claim = [&]() -> int {
       int u = -1;
@@ -202,24 +206,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto stage_chunk = [&](int item, int buf) {
       if (item < 0) return;
       const ChunkInfo ci = decode_chunk(p, item);
-      for (int e = lane; e < ci.count; e += 32) {
-        const int ent = p.entries[ci.begin + e];
-        sm.ent[buf][e] = ent;
-        tma_prefetch_3d(&tm_q, 0, ci.g * G, ent >> 5);
-        tma_prefetch_3d(&tm_q, 64, ci.g * G, ent >> 5);
-      }
+      for (int e = lane; e < ci.count; e += 32) sm.ent[buf][e] = p.entries[ci.begin + e];
       if (lane < 4) tma_prefetch_3d((lane & 2) ? &tm_v : &tm_k, (lane & 1) * 64, ci.g, ci.krow);
       __syncwarp();
     };
+    // L2 prefetch of the Q rows of tile tt of a staged chunk (one lane per
+    // query): a query's G heads of group g are G * 256 contiguous bytes of Q.
+    auto prefetch_q = [&](const ChunkInfo& c, int buf, int tt) {
+      const int e = tt * p.qpt + lane;
+      if (lane < p.qpt && e < c.count) {
+        const int qi = sm.ent[buf][e] >> 5;
+        bulk_prefetch_l2(p.q + (static_cast<int64_t>(qi) * p.hkv + c.g) * G * kHeadDim, G * kHeadDim * 2);
+      }
+    };
     int cur = claim();
     stage_chunk(cur, 0);
+    if (cur >= 0) {
+      const ChunkInfo c0 = decode_chunk(p, cur);
+      for (int tt = 0; tt < kQPrefetch && tt < c0.ntile; ++tt) prefetch_q(c0, 0, tt);
+    }
     for (uint32_t w = 0;; ++w) {
       const int item = cur;
       const int buf = w & 1;
       int nxt = -1;
+      ChunkInfo nci{};
       if (item >= 0) {
         nxt = claim();
         stage_chunk(nxt, buf ^ 1);  // chunk w-1's loads are all issued: its entries are free
+        if (nxt >= 0) nci = decode_chunk(p, nxt);
       }
       const int slot = w % kWorkSlots;
       if (w >= kWorkSlots && !mbar_wait_warp(&sm.work_empty[slot], ((w / kWorkSlots) - 1) & 1, abort_flag)) {
@@ -257,6 +271,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qs], kQTileBytes);
+        {
+          const int ahead = tt + kQPrefetch;
+          if (ahead < ci.ntile) prefetch_q(ci, buf, ahead);
+          else if (nxt >= 0 && ahead - ci.ntile < nci.ntile) prefetch_q(nci, buf ^ 1, ahead - ci.ntile);
+        }
         __syncwarp();
         if (lane < p.qpt) {  // one lane per query row of the tile
           int e = tt * p.qpt + lane;
