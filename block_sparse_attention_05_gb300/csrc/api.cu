@@ -205,7 +205,7 @@ bool make_map(CUtensorMap& m, const void* ptr, int rank, const cuuint64_t* dims,
               const cuuint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(&m, dtype, rank, const_cast<void*>(ptr), dims, strides_bytes, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -230,6 +230,18 @@ bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_hea
   cuuint64_t strides[2] = {256, static_cast<cuuint64_t>(heads) * 256};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
   return make_map(m, ptr, 3, dims, strides, box, dtype);
+}
+
+// Q [n, hq, 128] seen per (query, group) with the group's G heads split into
+// 8-row groups and each row into its two 64-dim halves: dims {64 dims, 8 heads,
+// 2 halves, G / 8 row groups, n * hkv query-groups}.  One box = one query's
+// group, landing as [row group][half][8 rows][128 B] (128-byte swizzle).
+bool map_q_groups(CUtensorMap& m, const void* ptr, long long n, int hkv, int G) {
+  const long long nqg = n * hkv;
+  cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(G / 8), static_cast<cuuint64_t>(nqg > 0 ? nqg : 1)};
+  cuuint64_t strides[4] = {256, 128, 8 * 256, static_cast<cuuint64_t>(G) * 256};
+  cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(G / 8), 1};
+  return make_map(m, ptr, 5, dims, strides, box);
 }
 
 // ---------------------------------------------------------------- common prologue
@@ -438,7 +450,7 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
 
   __half* v16 = at<__half>(c.ws, c.L.v16);
   CUtensorMap tq, tk, tv;
-  if (!map_3d(tq, q, c.d.T, c.d.hq, c.d.G, 1) || !map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) ||
+  if (!map_q_groups(tq, q, c.d.T, c.d.hkv, c.d.G) || !map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) ||
       !map_3d(tv, v16, c.d.N, c.d.hkv, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return MSA_ERR_CUDA;
   AttnParams ap{};

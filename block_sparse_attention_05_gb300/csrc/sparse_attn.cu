@@ -25,14 +25,17 @@
 //                             weight W = LSE + e ln 2 undoes V's 2^-e scale
 // The tile covers exactly one key block, so no running rescale of U is needed.
 //
-// Warp roles (512 threads): warp 0 = TMA producer and chunk claiming, warps 1
-// and 3 = one MMA issuer per softmax warpgroup, warp 2 = TMEM allocator,
-// warps 4..7 and 8..11 = two softmax warpgroups taking alternate tiles (each
-// owns an S/P and a U accumulator in TMEM: 2 x (128 + 128) = 512 columns),
-// warps 12..15 = the epilogue warpgroup (U read-back, normalisation, partial
-// stores) for every tile, which gets each row's sum of P through a 4-slot
-// shared buffer.  Q tiles live in a 2-stage ring, freed as soon as
-// QK^T retires; K/V are double-buffered across chunks.
+// Warp roles (512 threads): warp 0 = producer (chunk claiming, K and Q
+// gathers, L2 prefetches), warps 1 and 3 = one MMA issuer per softmax
+// warpgroup, warp 2 = TMEM allocator, then V loader, warps 4..7 and 8..11 =
+// two softmax warpgroups taking alternate tiles (each owns an S/P and a U
+// accumulator in TMEM: 2 x (128 + 128) = 512 columns), warps 12..15 = the
+// epilogue warpgroup (U read-back, normalisation, partial stores) for every
+// tile, which gets each row's sum of P through a 4-slot shared buffer.  Q
+// tiles live in a 4-stage ring (two stages per MMA issuer), each freed as soon
+// as its QK^T retires.  K and V have one buffer each with their own barriers:
+// the next chunk's K is loaded once the current chunk's last QK^T retires and
+// its V once the last PV does, which chunks of about 16 tiles hide.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -40,12 +43,12 @@ namespace msa {
 
 namespace {
 
-constexpr int kQStages = 2;
+constexpr int kQStages = 4;     // tile t uses stage t % 4: stages 0, 2 feed issuer 0, stages 1, 3 issuer 1
 constexpr int kWorkSlots = 4;
 constexpr int kStatSlots = 4;
 constexpr int kQPrefetch = 4;  // Q rows are prefetched into L2 this many tiles ahead of their gather
 constexpr int kQTileBytes = 128 * 128 * 2;   // 32 KB
-constexpr int kKVBytes = 2 * kQTileBytes;     // K + V of one block, 64 KB
+constexpr int kKVTileBytes = kQTileBytes;     // K or V of one block, 32 KB
 constexpr int kAttnThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -67,7 +70,7 @@ struct AttnSmem {
   uint8_t stage[4][32 * 64];     // epilogue: per warp, 32 rows x 32 bf16 (one quarter of the row)
   int ent[2][kMaxChunkEntries];  // producer: entries of the current and the next chunk
   uint64_t q_full[kQStages], q_empty[kQStages];
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full, k_empty, v_full, v_empty;
   uint64_t s_full[2], s_free[2], p_full[2], o_full[2], o_free[2];
   uint64_t stat_full[kStatSlots];
   uint64_t work_full[kWorkSlots], work_empty[kWorkSlots];
@@ -79,7 +82,7 @@ struct AttnSmem {
   int abort_flag;
 };
 
-constexpr size_t kAttnSmemBytes = 1024 + 2 * kKVBytes + kQStages * kQTileBytes + sizeof(AttnSmem);
+constexpr size_t kAttnSmemBytes = 1024 + 2 * kKVTileBytes + kQStages * kQTileBytes + sizeof(AttnSmem);
 
 
 __device__ __forceinline__ ChunkInfo decode_chunk(const AttnParams& p, int item) {
@@ -128,6 +131,25 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, const ChunkInfo
   return ri;
 }
 
+// Multiplies this lane's first n8 groups of 8 P columns (fp16 pairs) by f, an
+// exact power of two.  Warp-collective (tcgen05 loads and stores); rare, so
+// kept out of line to leave the softmax loop its registers.
+__device__ __noinline__ void rescale_p(uint32_t lane_addr, int n8, float f) {
+  const __half2 f2 = __float2half2_rn(f);
+  tmem_st_wait();
+  for (int cc = 0; cc < n8; ++cc) {
+    uint32_t w8[8];
+    tmem_ld_8cols(lane_addr + cc * 8, w8);
+    tmem_ld_wait_regs8(w8);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w8[j]), f2);
+      w8[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    tmem_st_8cols(lane_addr + cc * 8, w8);
+  }
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -138,9 +160,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (hdr->status & kFlagBadSeqlens) return;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* kv_buf = base;                       // 2 x (K 32 KB | V 32 KB)
-  uint8_t* q_buf = base + 2 * kKVBytes;         // kQStages x 32 KB
-  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(base + 2 * kKVBytes + kQStages * kQTileBytes);
+  uint8_t* k_buf = base;                        // K of the current chunk, 32 KB
+  uint8_t* v_buf = base + kKVTileBytes;         // V (fp16 copy) of the current chunk, 32 KB
+  uint8_t* q_buf = base + 2 * kKVTileBytes;     // kQStages x 32 KB
+  AttnSmem& sm = *reinterpret_cast<AttnSmem*>(base + 2 * kKVTileBytes + kQStages * kQTileBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,9 +175,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&sm.q_full[i], 1);
       mbar_init(&sm.q_empty[i], 1);
     }
+    mbar_init(&sm.k_full, 1);
+    mbar_init(&sm.k_empty, 2);  // one arrival per MMA issuer
+    mbar_init(&sm.v_full, 1);
+    mbar_init(&sm.v_empty, 2);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.kv_full[i], 1);
-      mbar_init(&sm.kv_empty[i], 2);  // one arrival per MMA issuer
       mbar_init(&sm.s_full[i], 1);
       mbar_init(&sm.s_free[i], 1);
       mbar_init(&sm.p_full[i], 128);
@@ -164,7 +189,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     for (int i = 0; i < kStatSlots; ++i) mbar_init(&sm.stat_full[i], 128);
     for (int i = 0; i < kWorkSlots; ++i) {
       mbar_init(&sm.work_full[i], 1);
-      mbar_init(&sm.work_empty[i], 14);  // 2 MMA threads + 8 softmax warps + 4 epilogue warps
+      mbar_init(&sm.work_empty[i], 15);  // 2 MMA threads + V loader + 8 softmax + 4 epilogue warps
     }
     mbar_init(&sm.mma_done[0], 1);
     mbar_init(&sm.mma_done[1], 1);
@@ -248,18 +273,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&sm.work_full[slot]);
       }
       if (item < 0) break;
-      const int kvb = kv_iter & 1;
-      if (kv_iter >= 2 && !mbar_wait_warp(&sm.kv_empty[kvb], ((kv_iter >> 1) - 1) & 1, abort_flag)) {
+      // K of this chunk, once every QK^T of the previous chunk has retired
+      // (V is loaded by warp 2 once every PV of the previous chunk has).
+      if (kv_iter >= 1 && !mbar_wait_warp(&sm.k_empty, (kv_iter - 1) & 1, abort_flag)) {
         if (lane == 0) report_timeout(abort_flag, hdr, 202);
         break;
       }
       if (lane == 0) {
-        uint8_t* kvp = kv_buf + kvb * kKVBytes;
-        mbar_arrive_expect_tx(&sm.kv_full[kvb], kKVBytes);
-        tma_load_3d(kvp, &tm_k, &sm.kv_full[kvb], 0, ci.g, ci.krow);
-        tma_load_3d(kvp + 16384, &tm_k, &sm.kv_full[kvb], 64, ci.g, ci.krow);
-        tma_load_3d(kvp + 32768, &tm_v, &sm.kv_full[kvb], 0, ci.g, ci.krow);
-        tma_load_3d(kvp + 49152, &tm_v, &sm.kv_full[kvb], 64, ci.g, ci.krow);
+        mbar_arrive_expect_tx(&sm.k_full, kKVTileBytes);
+        tma_load_3d(k_buf, &tm_k, &sm.k_full, 0, ci.g, ci.krow);
+        tma_load_3d(k_buf + 16384, &tm_k, &sm.k_full, 64, ci.g, ci.krow);
       }
       ++kv_iter;
       bool ok = true;
@@ -270,20 +293,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qs], kQTileBytes);
         {
           const int ahead = tt + kQPrefetch;
           if (ahead < ci.ntile) prefetch_q(ci, buf, ahead);
           else if (nxt >= 0 && ahead - ci.ntile < nci.ntile) prefetch_q(nci, buf ^ 1, ahead - ci.ntile);
         }
+        // The gather: one TMA box per query brings its G heads of group g
+        // (G * 256 contiguous bytes of Q) in the layout the MMA reads: 8-row
+        // groups 2 KB apart, each holding the rows' first 64 dims (1 KB,
+        // 128-byte swizzle) and then their last 64.
+        if (lane == 0) mbar_arrive_expect_tx(&sm.q_full[qs], kQTileBytes);
         __syncwarp();
-        if (lane < p.qpt) {  // one lane per query row of the tile
+        if (lane < p.qpt) {  // one lane per query of the tile
           int e = tt * p.qpt + lane;
           if (e >= ci.count) e = 0;  // pad the last tile with a real row
-          const int qi = sm.ent[buf][e] >> 5;
-          uint8_t* qp = q_buf + qs * kQTileBytes + lane * G * 128;
-          tma_load_3d(qp, &tm_q, &sm.q_full[qs], 0, ci.g * G, qi);
-          tma_load_3d(qp + 16384, &tm_q, &sm.q_full[qs], 64, ci.g * G, qi);
+          const int qg = (sm.ent[buf][e] >> 5) * p.hkv + ci.g;
+          tma_load_5d(q_buf + qs * kQTileBytes + lane * G * 256, &tm_q, &sm.q_full[qs], qg);
         }
         ++q_iter;
       }
@@ -296,17 +321,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t last = ((q_iter - 1 - s) / kQStages) * kQStages + s;
           mbar_wait(&sm.q_full[s], (last / kQStages) & 1, nullptr);
         }
-      for (int s = 0; s < 2; ++s)
-        if (kv_iter > static_cast<uint32_t>(s)) {
-          const uint32_t last = ((kv_iter - 1 - s) / 2) * 2 + s;
-          mbar_wait(&sm.kv_full[s], (last >> 1) & 1, nullptr);
-        }
+      if (kv_iter > 0) mbar_wait(&sm.k_full, (kv_iter - 1) & 1, nullptr);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ V loader
+    // (after allocating TMEM) loads each chunk's V once every PV of the
+    // previous chunk has retired, so that a chunk change stalls neither the
+    // Q gathers nor the first QK^T of the next chunk.
+    uint32_t w_iter = 0, v_iter = 0;
+    for (;;) {
+      const int slot = w_iter % kWorkSlots;
+      if (!mbar_wait_warp(&sm.work_full[slot], (w_iter / kWorkSlots) & 1, abort_flag)) {
+        if (lane == 0) report_timeout(abort_flag, hdr, 241);
+        break;
+      }
+      const int item = sm.work[slot];
+      const ChunkInfo ci = sm.work_ci[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.work_empty[slot]);
+      ++w_iter;
+      if (item < 0) break;
+      if (v_iter >= 1 && !mbar_wait_warp(&sm.v_empty, (v_iter - 1) & 1, abort_flag)) {
+        if (lane == 0) report_timeout(abort_flag, hdr, 242);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sm.v_full, kKVTileBytes);
+        tma_load_3d(v_buf, &tm_v, &sm.v_full, 0, ci.g, ci.krow);
+        tma_load_3d(v_buf + 16384, &tm_v, &sm.v_full, 64, ci.g, ci.krow);
+      }
+      ++v_iter;
+    }
+    if (lane == 0 && v_iter > 0) mbar_wait(&sm.v_full, (v_iter - 1) & 1, nullptr);
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers
     // One issuing thread per softmax warpgroup: warp 1 drives the even tiles,
     // warp 3 the odd ones, so a wait for one warpgroup never stalls the other.
-    // Tile t uses Q stage t % 2 == its warpgroup, so each stage has one consumer.
+    // Tile t uses Q stage t % 4, so stages 0 and 2 belong to warp 1 and
+    // stages 1 and 3 to warp 3: each stage has one consumer.
     if (lane == 0) {
       const int wg = (warp == 1) ? 0 : 1;
       const uint32_t idesc_qk = idesc_bf16(128, 128, false);
@@ -325,10 +377,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&sm.work_empty[slot]);
         ++w_iter;
         if (item < 0) break;
-        const int kvb = kv_iter & 1;
-        // every issuer waits for every chunk's K/V, used or not, so that it can
-        // never arrive on kv_empty for a later use of this buffer too early
-        if (!mbar_wait(&sm.kv_full[kvb], (kv_iter >> 1) & 1, abort_flag)) {
+        // every issuer waits for every chunk's K and V, used or not, so that it
+        // never arrives on k_empty / v_empty for a later fill too early
+        const uint32_t kv_par = kv_iter & 1;
+        if (!mbar_wait(&sm.k_full, kv_par, abort_flag)) {
           report_timeout(abort_flag, hdr, 212);
           break;
         }
@@ -336,28 +388,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // this issuer's tiles of the chunk: t0 + tt with (t0 + tt) & 1 == wg
         const int first = ((t & 1) == static_cast<uint32_t>(wg)) ? 0 : 1;
         const int mine = (ci.ntile > first) ? (ci.ntile - first + 1) / 2 : 0;
-        const uint32_t ka = smem_u32(kv_buf + kvb * kKVBytes);
-        const uint32_t va = ka + 32768;
+        const uint32_t ka = smem_u32(k_buf);
+        const uint32_t va = smem_u32(v_buf);
         for (int m = 0; m < mine; ++m) {
           const uint32_t tm = t + first + 2 * m;
           const uint32_t n = tm >> 1;
           // ---- S = Q K^T
-          if (!mbar_wait(&sm.q_full[wg], n & 1, abort_flag) ||
+          const int qs = tm & (kQStages - 1);
+          if (!mbar_wait(&sm.q_full[qs], (tm / kQStages) & 1, abort_flag) ||
               (n >= 1 && !mbar_wait(&sm.s_free[wg], (n - 1) & 1, abort_flag))) {
             report_timeout(abort_flag, hdr, 213);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t qa = smem_u32(q_buf + wg * kQTileBytes);
+          const uint32_t qa = smem_u32(q_buf + qs * kQTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_bf16(s_col, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_qk,
+            const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;  // K: 64-dim halves 16 KB apart
+            const uint32_t qoff = (kk >> 2) * 1024 + (kk & 3) * 32;   // Q: halves interleaved per row group
+            umma_bf16(s_col, sdesc_sw128(qa + qoff, 16, 2048), sdesc_sw128(ka + koff, 16, 1024), idesc_qk,
                       kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.s_full[wg]);
-          umma_commit(&sm.q_empty[wg]);  // the Q stage is free once QK^T has retired
+          umma_commit(&sm.q_empty[qs]);  // the Q stage is free once QK^T has retired
+          if (m == mine - 1) umma_commit(&sm.k_empty);
+          if (m == 0 && !mbar_wait(&sm.v_full, kv_par, abort_flag)) {
+            report_timeout(abort_flag, hdr, 215);
+            ok = false;
+            break;
+          }
           // ---- U = P V (fp16)
           if (!mbar_wait(&sm.p_full[wg], n & 1, abort_flag) ||
               (n >= 1 && !mbar_wait(&sm.o_free[wg], (n - 1) & 1, abort_flag))) {
@@ -373,10 +433,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             umma_bf16_ts(o_col, s_col + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, kk ? 1u : 0u);
           umma_commit(&sm.o_full[wg]);
           umma_commit(&sm.s_free[wg]);  // S/P columns reusable once PV has retired
-          if (m == mine - 1) umma_commit(&sm.kv_empty[kvb]);
+          if (m == mine - 1) umma_commit(&sm.v_empty);
         }
         if (!ok) break;
-        if (mine == 0) mbar_arrive(&sm.kv_empty[kvb]);
+        if (mine == 0) {
+          mbar_arrive(&sm.k_empty);
+          if (!mbar_wait(&sm.v_full, kv_par, abort_flag)) {
+            report_timeout(abort_flag, hdr, 216);
+            break;
+          }
+          mbar_arrive(&sm.v_empty);
+        }
         t += ci.ntile;
       }
       umma_commit(&sm.mma_done[wg]);
@@ -412,91 +479,92 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           break;
         }
         tc_fence_after();
-        // One pass over S, 16 keys at a time, each chunk's load issued one chunk
+        // One pass over S, 32 keys at a time, each step's load issued one step
         // ahead.  The exponent reference m starts at the max of the first
-        // chunk's visible keys; a later chunk whose max exceeds it by more than
+        // step's visible keys; a later step whose max exceeds it by more than
         // 2^15 first rescales the P already stored by an exact power of two and
         // raises m (rare), so every P lies in [0, 2^15] and fits fp16.  P goes
-        // back over the chunk's own S columns as fp16 pairs: keys 16c..16c+15
-        // -> columns 8c..8c+7.  With l = sum_k P_k the epilogue stores
-        // U / l, U = sum_k P_k v_k over V scaled by 2^-e: the block's normalised
-        // output times 2^-e, so its LSE is (m + log2 l) ln 2 and its log weight
-        // that LSE + e ln 2.
+        // back over the step's own S columns as fp16 pairs: keys 32c..32c+31
+        // -> columns 16c..16c+15 (keys 16k..16k+15 in columns 8k..8k+7, one
+        // PV K-step each).  With l = sum_k P_k the epilogue stores U / l,
+        // U = sum_k P_k v_k over V scaled by 2^-e: the block's normalised output
+        // times 2^-e, so its LSE is (m + log2 l) ln 2 and its log weight that
+        // LSE + e ln 2.
         const int lim = ri.valid ? ri.lim : kBlock - 1;  // padding rows: computed, never stored
         const bool warp_full = __all_sync(0xFFFFFFFFu, lim >= kBlock - 1);
-        float l = 0.f, m_ref = 0.f;
+        float2 l2 = make_float2(0.f, 0.f);
+        float m_ref = 0.f;
         {
-          uint32_t va[16], vb[16];
-          tmem_ld_16cols(lane_addr, va);
-          tmem_ld_wait_regs16(va);
-          float m0 = -INFINITY;
+          uint32_t va[32], vb[32];
+          // score j of step c, -inf past the row's causal limit on the masked path
+          auto sval = [&](const uint32_t (&v)[32], int c, bool masked, int j) {
+            return (!masked || c * 32 + j <= lim) ? __uint_as_float(v[j]) : -INFINITY;
+          };
+          auto process = [&](const uint32_t (&v)[32], int c, bool masked) {
+            float t8[11];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) m0 = fmaxf(m0, (j <= lim) ? __uint_as_float(va[j]) : -INFINITY);
-          if (m0 != -INFINITY) m_ref = m0 * p.scale_log2;
-          auto process = [&](const uint32_t (&v)[16], int c, bool masked) {
-            float sv[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              sv[j] = (!masked || c * 16 + j <= lim) ? __uint_as_float(v[j]) : -INFINITY;
-            float cm = fmax3(sv[0], sv[1], sv[2]);
-#pragma unroll
-            for (int j = 3; j < 15; j += 2) cm = fmax3(cm, sv[j], sv[j + 1]);
-            cm = fmaxf(cm, sv[15]);
+            for (int j = 0; j < 10; ++j)
+              t8[j] = fmax3(sval(v, c, masked, 3 * j), sval(v, c, masked, 3 * j + 1), sval(v, c, masked, 3 * j + 2));
+            t8[10] = fmaxf(sval(v, c, masked, 30), sval(v, c, masked, 31));
+            const float cm = fmaxf(fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
+                                         fmax3(t8[6], t8[7], t8[8])),
+                                   fmaxf(t8[9], t8[10]));
+            if (c == 0) m_ref = (cm == -INFINITY) ? 0.f : cm * p.scale_log2;
             // The rescale uses warp-collective TMEM loads and stores, so the
             // whole warp enters it when any of its rows needs it; the other rows
             // scale by exactly 1.
             const bool need = cm != -INFINITY && cm * p.scale_log2 - m_ref > 15.f;
             if (__any_sync(0xFFFFFFFFu, need)) {
               const float kexp = need ? ceilf(cm * p.scale_log2 - m_ref) : 0.f;
-              const __half2 f2 = __float2half2_rn(exp2f(-kexp));
-              tmem_st_wait();
-              for (int cc = 0; cc < c; ++cc) {
-                uint32_t w8[8];
-                tmem_ld_8cols(lane_addr + cc * 8, w8);
-                tmem_ld_wait_regs8(w8);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&w8[j]), f2);
-                  w8[j] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-                tmem_st_8cols(lane_addr + cc * 8, w8);
-              }
-              l *= exp2f(-kexp);
+              const float f = exp2f(-kexp);
+              rescale_p(lane_addr, 2 * c, f);
+              l2.x *= f;
+              l2.y *= f;
               m_ref += kexp;
             }
-            uint32_t pk[8];
+            const float2 sc = make_float2(p.scale_log2, p.scale_log2), nm = make_float2(-m_ref, -m_ref);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float x0 = exp2_approx(fmaf(sv[2 * j], p.scale_log2, -m_ref));
-              const float x1 = exp2_approx(fmaf(sv[2 * j + 1], p.scale_log2, -m_ref));
-              l += x0 + x1;
-              const __half2 h = __floats2half2_rn(x0, x1);
-              pk[j] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int k = 16 * h + 2 * j;
+                const float2 z = ffma2(make_float2(sval(v, c, masked, k), sval(v, c, masked, k + 1)), sc, nm);
+                const float2 x = make_float2(exp2_approx(z.x), exp2_approx(z.y));
+                l2 = fadd2(l2, x);
+                const __half2 hx = __floats2half2_rn(x.x, x.y);
+                pk[j] = *reinterpret_cast<const uint32_t*>(&hx);
+              }
+              tmem_st_8cols(lane_addr + c * 16 + h * 8, pk);
             }
-            tmem_st_8cols(lane_addr + c * 8, pk);
           };
+          tmem_ld_32cols(lane_addr, va);
+          tmem_ld_wait_regs(va);
           if (warp_full) {
-#pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-              tmem_ld_16cols(lane_addr + (2 * i + 1) * 16, vb);
-              process(va, 2 * i, false);
-              tmem_ld_wait_regs16(vb);
-              if (i < 3) tmem_ld_16cols(lane_addr + (2 * i + 2) * 16, va);
-              process(vb, 2 * i + 1, false);
-              if (i < 3) tmem_ld_wait_regs16(va);
-            }
+            tmem_ld_32cols(lane_addr + 32, vb);
+            process(va, 0, false);
+            tmem_ld_wait_regs(vb);
+            tmem_ld_32cols(lane_addr + 64, va);
+            process(vb, 1, false);
+            tmem_ld_wait_regs(va);
+            tmem_ld_32cols(lane_addr + 96, vb);
+            process(va, 2, false);
+            tmem_ld_wait_regs(vb);
+            process(vb, 3, false);
           } else {
-#pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
-              tmem_ld_16cols(lane_addr + (2 * i + 1) * 16, vb);
-              process(va, 2 * i, true);
-              tmem_ld_wait_regs16(vb);
-              if (i < 3) tmem_ld_16cols(lane_addr + (2 * i + 2) * 16, va);
-              process(vb, 2 * i + 1, true);
-              if (i < 3) tmem_ld_wait_regs16(va);
-            }
+            tmem_ld_32cols(lane_addr + 32, vb);
+            process(va, 0, true);
+            tmem_ld_wait_regs(vb);
+            tmem_ld_32cols(lane_addr + 64, va);
+            process(vb, 1, true);
+            tmem_ld_wait_regs(va);
+            tmem_ld_32cols(lane_addr + 96, vb);
+            process(va, 2, true);
+            tmem_ld_wait_regs(vb);
+            process(vb, 3, true);
           }
         }
+        const float l = l2.x + l2.y;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[wg]);
@@ -565,10 +633,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           uint4 pk[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            pk[c].x = pack_bf16(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
-            pk[c].y = pack_bf16(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
-            pk[c].z = pack_bf16(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
-            pk[c].w = pack_bf16(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+            const float2 il = make_float2(inv_l, inv_l);
+            float2 z;
+            z = fmul2(make_float2(__uint_as_float(o[8 * c + 0]), __uint_as_float(o[8 * c + 1])), il);
+            pk[c].x = pack_bf16(z.x, z.y);
+            z = fmul2(make_float2(__uint_as_float(o[8 * c + 2]), __uint_as_float(o[8 * c + 3])), il);
+            pk[c].y = pack_bf16(z.x, z.y);
+            z = fmul2(make_float2(__uint_as_float(o[8 * c + 4]), __uint_as_float(o[8 * c + 5])), il);
+            pk[c].z = pack_bf16(z.x, z.y);
+            z = fmul2(make_float2(__uint_as_float(o[8 * c + 6]), __uint_as_float(o[8 * c + 7])), il);
+            pk[c].w = pack_bf16(z.x, z.y);
             *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk[c];
           }
           __syncwarp();
