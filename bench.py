@@ -89,8 +89,8 @@ def algorithmic_work(x, idx: torch.Tensor):
     # K/V bytes the Main Branch must read at least once: each selected block's K and V rows
     kv_bytes_selected = float(2 * 2 * cfg.head_dim * ntok.double().sum().item())  # per (query,group) reads
     k_idx_bytes = float(2 * cfg.d_idx * (pos + 1).double().sum().item()) if cfg.is_decode else None
-    # combine: read every valid partial (G x 128 bf16 + G fp32), write O and LSE
-    combine_bytes = float(n_slots * G * (cfg.head_dim * 2 + 4) + x.total_q * cfg.hq * (cfg.head_dim * 2 + 4) +
+    # combine: read every valid partial (G x 128 bf16 + G fp32 LSE + G fp32 log weight), write O and LSE
+    combine_bytes = float(n_slots * G * (cfg.head_dim * 2 + 8) + x.total_q * cfg.hq * (cfg.head_dim * 2 + 4) +
                           x.total_q * cfg.hkv * cfg.topk * 4)
     return {"index_flops": index_flops, "attn_flops": attn_flops, "n_slots": n_slots,
             "kv_bytes_selected": kv_bytes_selected, "k_idx_bytes": k_idx_bytes,
@@ -162,20 +162,21 @@ def kernel_source_hash(name: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str, kernel_file: str, units_now: float):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu record, scaled to this launch
-    by the units processed; None when absent or taken on a different version of the kernel."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+def ncu_traffic(workload: str, kernel_file: str, x):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu record (profiles/traffic.txt, JSON),
+    scaled from the captured case to this one by the record's unit (queries for prefill, cached keys for
+    decode); None when absent or taken on a different version of the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     try:
         rec = json.load(open(p)).get(workload)
     except (ValueError, OSError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash(kernel_file):
+    if not rec or rec.get("source") != kernel_file or rec.get("source_hash") != kernel_source_hash(kernel_file):
         return None
-    per_unit = rec["dram_bytes"] / rec["units"]
-    return per_unit * units_now
+    units_now = {"total_q": x.total_q, "total_k": x.total_k}[rec["units_kind"]]
+    return rec["dram_bytes"] / rec["units"] * units_now
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -340,7 +341,7 @@ def main():
         bound, unit_r, amount = "hbm", "GB/s", work["kv_bytes_selected"]
         achieved = amount / (stage_mean[dominant] * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
-    traffic = ncu_traffic(cfg.name, kernel_file[dominant], units_per_gpu)
+    traffic = ncu_traffic(cfg.name, kernel_file[dominant], x)
     roofline = {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak, "unit": unit_r,
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peaks['source']} ({'bf16 burst' if bound == 'tensor' else 'HBM copy'})"}

@@ -57,6 +57,9 @@ CONFIGS = {
     "prefill_16k": Workload(
         "prefill_16k", ((16384, 16384),), seed=1016,
         description="T=N=16384 causal, Hq 64 / Hkv 4, d_idx 128, k 16, 64 topics (profiling size)"),
+    "decode_64k": Workload(
+        "decode_64k", None, seed=1017, decode_batch=16, decode_ctx=65536,
+        description="16 sequences x 1 query, KV cache 65536-128+U{1..128}, k 16, 64 topics (profiling size)"),
     "prefill_128k": Workload(
         "prefill_128k", ((131072, 131072),), seed=1010,
         description="T=N=131072 causal, Hq 64 / Hkv 4, d_idx 128, k 16, 64 topics"),
