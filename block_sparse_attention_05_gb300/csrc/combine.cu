@@ -11,10 +11,15 @@
 // (The atlas record of the report lists a two-phase combine with per-partial
 // LSE buffers and no atomics; this kernel is that second phase.)
 //
-// One warp per (query, head): lanes own 4 of the 128 output columns and loop
-// over the slots; the slot weights come from a warp reduction over the LSEs.
-// Slots whose block index is -1 or past the query's causal end hold no partial
-// and are skipped, matching the scheduler.
+// One warp per two heads of a query (same group, G >= 8): each half-warp
+// owns a head, its lanes 8 of the 128 output columns and, for the slot
+// loads, one slot each.  Every load -- the slots' block indices, LSEs, log
+// weights and all k partial rows -- is issued before any is used, so a row
+// costs one memory round trip; the sequence lookup that decides which slots
+// are valid runs alongside.  Slots whose block index is -1 or past the
+// query's causal end hold no partial (their memory is never written, so its
+// contents are only ever selected away, never multiplied) and are skipped,
+// matching the scheduler.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,71 +33,76 @@ constexpr int kMaxTopk = 16;
 __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombineParams p) {
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kCombineWarps + warp;  // (query, head)
-  if (row >= static_cast<int64_t>(p.total_q) * p.hq) return;
-  const int i = static_cast<int>(row / p.hq);
-  const int h = static_cast<int>(row % p.hq);
+  const int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombineWarps + warp;  // (query, head pair)
+  if (pair >= static_cast<int64_t>(p.total_q) * (p.hq >> 1)) return;
+  const int half = lane >> 4, hl = lane & 15;
+  const int i = static_cast<int>(pair / (p.hq >> 1));
+  const int h = static_cast<int>(pair % (p.hq >> 1)) * 2 + half;
   const int g = h / p.group, hh = h % p.group;
+  const int64_t sel_base = (static_cast<int64_t>(i) * p.hkv + g) * p.topk;
+
+  int b = -1;
+  float l_s = -INFINITY, w_s = -INFINITY;
+  if (hl < p.topk) {
+    b = p.idx[sel_base + hl];
+    l_s = p.part.lse[(sel_base + hl) * p.group + hh];
+    w_s = p.part.ow[(sel_base + hl) * p.group + hh];
+  }
+  const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
+  const int64_t slot_stride = static_cast<int64_t>(p.group) * kHeadDim;
+  uint4 raw[kMaxTopk];
+#pragma unroll
+  for (int sl = 0; sl < kMaxTopk; ++sl)
+    raw[sl] = (sl < p.topk) ? __ldcs(reinterpret_cast<const uint4*>(base + sl * slot_stride)) : make_uint4(0, 0, 0, 0);
+
   const int s = find_seq(p.cu_q, p.num_seqs, i);
   const SeqInfo si = p.seq[s];
   const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
-  const int64_t sel_base = (static_cast<int64_t>(i) * p.hkv + g) * p.topk;
+  const bool valid = hl < p.topk && b >= 0 && b <= local;
+  if (!valid) l_s = -INFINITY;
 
-  float l_s = -INFINITY, w_s = -INFINITY;
-  if (lane < p.topk) {
-    const int b = p.idx[sel_base + lane];
-    if (b >= 0 && b <= local) {
-      l_s = p.part.lse[(sel_base + lane) * p.group + hh];
-      w_s = p.part.ow[(sel_base + lane) * p.group + hh];
-    }
-  }
   float m = l_s;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  float sum = (l_s == -INFINITY) ? 0.f : expf(l_s - m);
+  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  float sum = valid ? expf(l_s - m) : 0.f;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
   const float L = m + logf(sum);
-  const float w = (l_s == -INFINITY) ? 0.f : expf(w_s - L);
+  const float w = valid ? expf(w_s - L) : 0.f;
 
-  // issue every slot's load before using any (memory-level parallelism)
-  const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + lane * 4;
-  const int64_t slot_stride = static_cast<int64_t>(p.group) * kHeadDim;
-  uint2 raw[kMaxTopk];
-  float wsl[kMaxTopk];
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int sl = 0; sl < kMaxTopk; ++sl) {
-    wsl[sl] = __shfl_sync(0xFFFFFFFFu, w, sl);
-    raw[sl] = make_uint2(0u, 0u);
-    if (sl < p.topk && wsl[sl] != 0.f) raw[sl] = __ldcs(reinterpret_cast<const uint2*>(base + sl * slot_stride));
-  }
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float ws = __shfl_sync(0xFFFFFFFFu, w, (lane & 16) | sl);
+    if (sl < p.topk && ws != 0.f) {
+      const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
 #pragma unroll
-  for (int sl = 0; sl < kMaxTopk; ++sl) {
-    const float ws = wsl[sl];
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw[sl].x);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw[sl].y);
-    acc[0] = fmaf(ws, __low2float(a), acc[0]);
-    acc[1] = fmaf(ws, __high2float(a), acc[1]);
-    acc[2] = fmaf(ws, __low2float(b), acc[2]);
-    acc[3] = fmaf(ws, __high2float(b), acc[3]);
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+        acc[2 * j] = fmaf(ws, __low2float(t), acc[2 * j]);
+        acc[2 * j + 1] = fmaf(ws, __high2float(t), acc[2 * j + 1]);
+      }
+    }
   }
   const bool empty = (m == -INFINITY);
-  __nv_bfloat162 o01 = __floats2bfloat162_rn(acc[0], acc[1]);
-  __nv_bfloat162 o23 = __floats2bfloat162_rn(acc[2], acc[3]);
-  uint2 out;
-  out.x = *reinterpret_cast<uint32_t*>(&o01);
-  out.y = *reinterpret_cast<uint32_t*>(&o23);
-  *reinterpret_cast<uint2*>(p.o + row * kHeadDim + lane * 4) = out;
-  if (lane == 0) p.lse[row] = empty ? -INFINITY : L;
+  uint4 out;
+  uint32_t* ow = &out.x;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+    ow[j] = *reinterpret_cast<const uint32_t*>(&t);
+  }
+  const int64_t row = static_cast<int64_t>(i) * p.hq + h;
+  *reinterpret_cast<uint4*>(p.o + row * kHeadDim + hl * 8) = out;
+  if (hl == 0) p.lse[row] = empty ? -INFINITY : L;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(p.total_q) * p.hq;
-  if (rows == 0) return cudaSuccess;
-  const int64_t grid = (rows + kCombineWarps - 1) / kCombineWarps;
+  const int64_t pairs = static_cast<int64_t>(p.total_q) * (p.hq >> 1);  // hq is a multiple of 8
+  if (pairs == 0) return cudaSuccess;
+  const int64_t grid = (pairs + kCombineWarps - 1) / kCombineWarps;
   combine_kernel<<<static_cast<unsigned>(grid), 32 * kCombineWarps, 0, stream>>>(p);
   note_launches(1);
   return cudaGetLastError();
