@@ -87,7 +87,7 @@ msa_status_t derive(const msa_problem_t* p, Derived& d) {
   d.max_k = p->max_seqlen_k;
   d.max_nb = (p->max_seqlen_k + 127) / 128;
   if (d.max_nb < 1) d.max_nb = 1;
-  d.qt = 128 / d.hkv;
+  d.qt = 256 / d.hkv;  // index work item: 256 rows of Q_idx (two 128-row sub-tiles)
   d.qpt = 128 / G;
   d.qpc = d.qpt * kTilesPerChunk;
   d.total_blocks = (p->total_k + 127) / 128 + d.S;
