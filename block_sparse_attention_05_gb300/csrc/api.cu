@@ -87,7 +87,7 @@ msa_status_t derive(const msa_problem_t* p, Derived& d) {
   d.max_k = p->max_seqlen_k;
   d.max_nb = (p->max_seqlen_k + 127) / 128;
   if (d.max_nb < 1) d.max_nb = 1;
-  d.qt = 256 / d.hkv;  // index work item: 256 rows of Q_idx (two 128-row sub-tiles)
+  d.qt = 128 / d.hkv;  // index work item: 128 rows of Q_idx
   d.qpt = 128 / G;
   d.qpc = d.qpt * kTilesPerChunk;
   d.total_blocks = (p->total_k + 127) / 128 + d.S;
@@ -314,7 +314,7 @@ msa_status_t run_index_prefill(const msa_problem_t* p, Ctx& c, const void* q_idx
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tq, tk;
   if (!map_2d(tq, q_idx, static_cast<long long>(c.d.T) * c.d.hkv, c.d.d_idx, 128) ||
-      !map_2d(tk, k_idx, c.d.N, c.d.d_idx, 128))
+      !map_2d(tk, k_idx, c.d.N, c.d.d_idx, 256))  // index scoring loads two key blocks per box
     return MSA_ERR_CUDA;
   IndexParams ip{};
   ip.seq = c.seq;

@@ -5,23 +5,23 @@
 // Q_idx . K_idx^T, max-pooled over 128-token key blocks, then top-k blocks
 // with the query's own (local) block always kept.
 //
-// Work item: a tile of 256 rows of Q_idx viewed as [T * Hkv, d_idx] (two
-// 128-row sub-tiles); with Hkv = 4 that is 64 consecutive queries x 4 groups,
-// so one K_idx tile (the shared index-key head) serves every group at once.
-// The CTA walks the key blocks 0..L_max of the tile in order; each block's
-// K_idx tile is loaded once and feeds two 128 x 128 x d_idx tcgen05 MMAs, one
-// per sub-tile (bf16 in, fp32 accumulate in TMEM; two accumulator pairs), so
-// every byte brought from L2 serves 256 rows.  The epilogue warps reduce each
-// accumulator row (one TMEM lane per thread) to the block's pooled score with
-// the causal limit of that row.  In the fused mode the epilogue keeps a
-// running top-(k-1) of the non-local blocks per row in registers and writes
-// the final selection; otherwise it writes pooled scores.
+// Work item: a tile of 128 rows of Q_idx viewed as [T * Hkv, d_idx]; with
+// Hkv = 4 that is 32 consecutive queries x 4 groups, so one K_idx tile (the
+// shared index-key head) serves every group at once.  The CTA walks the key
+// blocks 0..L_max of the tile in pairs; each pair is one 128 x 256 x d_idx
+// tcgen05 MMA (bf16 in, fp32 accumulate in TMEM, two 256-column
+// accumulators): N = 256 halves the shared-memory operand traffic per FLOP
+// of a 128-key MMA, which is what limits a 128 x 128 MMA from shared memory.
+// The epilogue warps reduce each accumulator row (one TMEM lane per thread) to
+// the two blocks' pooled scores with the causal limit of that row.  In the
+// fused mode the epilogue keeps a running top-(k-1) of the non-local blocks
+// per row in registers and writes the final selection; otherwise it writes
+// pooled scores.
 //
-// Warp roles (384 threads): warp 0 = TMA producer and work claiming, warp 1 =
-// MMA issuer, warp 2 = TMEM allocator, warp 3 idle, warps 4..7 and 8..11 =
-// epilogue of sub-tile 0 and 1.  Work items are claimed dynamically (atomic
-// counter) from a list sorted by descending cost, so the persistent grid
-// balances itself.
+// Warp roles (256 threads): warp 0 = TMA producer and work claiming, warp 1 =
+// MMA issuer, warp 2 = TMEM allocator, warp 3 idle, warps 4..7 = epilogue.
+// Work items are claimed dynamically (atomic counter) from a list sorted by
+// descending cost, so the persistent grid balances itself.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,13 +29,13 @@ namespace msa {
 
 namespace {
 
-constexpr int kIdxStagesK = 3;            // K_idx ring depth
-constexpr int kTileBytes = 128 * 128 * 2; // one 128-row tile of 128 bf16 columns
-constexpr int kSub = 2;                   // 128-row sub-tiles per work item
-constexpr int kIdxThreads = 384;
+constexpr int kIdxStagesK = 3;             // K_idx ring depth (block pairs)
+constexpr int kQTile = 128 * 128 * 2;      // 128 rows x 128 bf16 columns
+constexpr int kKPair = 2 * kQTile;         // 256 keys x 128 bf16 columns
+constexpr int kIdxThreads = 256;
 
 struct IdxSmem {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full, q_empty;
   uint64_t k_full[kIdxStagesK], k_empty[kIdxStagesK];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t work_full[2], work_empty[2];
@@ -45,10 +45,8 @@ struct IdxSmem {
   int abort_flag;
 };
 
-constexpr size_t kIdxSmemBytes =
-    1024 /*align slack*/ + (2 * kSub + kIdxStagesK) * kTileBytes + sizeof(IdxSmem);
+constexpr size_t kIdxSmemBytes = 1024 /*align slack*/ + kQTile + kIdxStagesK * kKPair + sizeof(IdxSmem);
 
-// Queries of the work item (nq) and the last key block any of them sees.
 __device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt, int& nq, int& lmax) {
   nq = min(qt, si.q_len - t0);
   const int last_pos = si.kv_len - si.q_len + t0 + nq - 1;
@@ -66,26 +64,25 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   if (hdr->status & kFlagBadSeqlens) return;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_buf = base;                                // 2 stages x kSub tiles
-  uint8_t* k_buf = base + 2 * kSub * kTileBytes;        // kIdxStagesK tiles
-  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(base + (2 * kSub + kIdxStagesK) * kTileBytes);
+  uint8_t* q_buf = base;                      // one 128-row tile
+  uint8_t* k_buf = base + kQTile;             // kIdxStagesK pairs of key blocks
+  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(base + kQTile + kIdxStagesK * kKPair);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = static_cast<int>(hdr->n_qtiles);
   const int kchunks = p.d_idx >> 6;                // 64-column chunks per row
   const int ksteps = p.d_idx >> 4;                 // UMMA K = 16 steps
-  const uint32_t sub_tx = 128u * p.d_idx * 2u;     // bytes of one 128-row sub-tile
-  const int sub_q = 128 / p.hkv;                   // queries per sub-tile
+  const uint32_t row_tx = p.d_idx * 2u;            // bytes of one row
 
   if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.q_full[i], 1);
-      mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.acc_full[i], 1);
-      mbar_init(&sm.acc_empty[i], 256);  // both epilogue warpgroups
+      mbar_init(&sm.acc_empty[i], 128);
       mbar_init(&sm.work_full[i], 1);
-      mbar_init(&sm.work_empty[i], 9);   // MMA thread + 8 epilogue warps
+      mbar_init(&sm.work_empty[i], 5);
     }
     for (int i = 0; i < kIdxStagesK; ++i) {
       mbar_init(&sm.k_full[i], 1);
@@ -126,21 +123,16 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const SeqInfo si = p.seq[tile.x];
         int nq, lmax;
         tile_geometry(si, tile.y, p.qt, nq, lmax);
-        const int nsub = (nq + sub_q - 1) / sub_q;
         const int row0 = (si.q_start + tile.y) * p.hkv;
-        const int qb = q_iter & 1;
-        if (q_iter >= 2 && !mbar_wait(&sm.q_empty[qb], ((q_iter >> 1) - 1) & 1, abort_flag)) {
+        if (q_iter >= 1 && !mbar_wait(&sm.q_empty, (q_iter - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 102);
           break;
         }
-        mbar_arrive_expect_tx(&sm.q_full[qb], nsub * sub_tx);
-        for (int us = 0; us < nsub; ++us)
-          for (int c = 0; c < kchunks; ++c)
-            tma_load_2d(q_buf + (qb * kSub + us) * kTileBytes + c * 16384, &tm_q, &sm.q_full[qb], c * 64,
-                        row0 + us * 128);
+        mbar_arrive_expect_tx(&sm.q_full, 128u * row_tx);
+        for (int c = 0; c < kchunks; ++c) tma_load_2d(q_buf + c * 16384, &tm_q, &sm.q_full, c * 64, row0);
         ++q_iter;
         bool ok = true;
-        for (int b = 0; b <= lmax; ++b) {
+        for (int bp = 0; 2 * bp <= lmax; ++bp) {
           const int ks = k_iter % kIdxStagesK;
           if (k_iter >= kIdxStagesK &&
               !mbar_wait(&sm.k_empty[ks], ((k_iter / kIdxStagesK) - 1) & 1, abort_flag)) {
@@ -148,21 +140,18 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.k_full[ks], sub_tx);
+          // keys 256 bp .. 256 bp + 255 of the sequence (past its end: zero fill
+          // or the next sequence's keys, both masked by the causal limit)
+          mbar_arrive_expect_tx(&sm.k_full[ks], 256u * row_tx);
           for (int c = 0; c < kchunks; ++c)
-            tma_load_2d(k_buf + ks * kTileBytes + c * 16384, &tm_k, &sm.k_full[ks], c * 64,
-                        si.k_start + b * kBlock);
+            tma_load_2d(k_buf + ks * kKPair + c * 32768, &tm_k, &sm.k_full[ks], c * 64, si.k_start + bp * 256);
           ++k_iter;
         }
         if (!ok) break;
       }
       // Let every issued copy land before the CTA can exit (matters only
       // after an abort; in a normal run the MMA warp consumed them all).
-      for (int s = 0; s < 2; ++s)
-        if (q_iter > static_cast<uint32_t>(s)) {
-          const uint32_t last = ((q_iter - 1 - s) / 2) * 2 + s;
-          mbar_wait(&sm.q_full[s], (last >> 1) & 1, nullptr);
-        }
+      if (q_iter > 0) mbar_wait(&sm.q_full, (q_iter - 1) & 1, nullptr);
       for (int s = 0; s < kIdxStagesK; ++s)
         if (k_iter > static_cast<uint32_t>(s)) {
           const uint32_t last = ((k_iter - 1 - s) / kIdxStagesK) * kIdxStagesK + s;
@@ -172,7 +161,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, 128, false);
+      const uint32_t idesc = idesc_bf16(128, 256, false);
       uint32_t q_iter = 0, k_iter = 0, a_iter = 0;
       for (uint32_t w = 0;; ++w) {
         const int slot = w & 1;
@@ -187,16 +176,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         const SeqInfo si = p.seq[tile.x];
         int nq, lmax;
         tile_geometry(si, tile.y, p.qt, nq, lmax);
-        const int nsub = (nq + sub_q - 1) / sub_q;
-        // last key block seen by each sub-tile: sub-tile 0 stops earlier
-        const int lmax0 = (si.kv_len - si.q_len + tile.y + min(nq, sub_q) - 1) >> 7;
-        const int qb = q_iter & 1;
-        if (!mbar_wait(&sm.q_full[qb], (q_iter >> 1) & 1, abort_flag)) {
+        if (!mbar_wait(&sm.q_full, q_iter & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 112);
           break;
         }
+        const uint32_t qa = smem_u32(q_buf);
         bool ok = true;
-        for (int b = 0; b <= lmax; ++b) {
+        for (int bp = 0; 2 * bp <= lmax; ++bp) {
           const int ks = k_iter % kIdxStagesK;
           const int ab = a_iter & 1;
           if (!mbar_wait(&sm.k_full[ks], (k_iter / kIdxStagesK) & 1, abort_flag) ||
@@ -206,15 +192,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t ka = smem_u32(k_buf + ks * kTileBytes);
-          for (int us = 0; us < nsub; ++us) {
-            if (us == 0 && b > lmax0) continue;  // no row of sub-tile 0 sees this block
-            const uint32_t qa = smem_u32(q_buf + (qb * kSub + us) * kTileBytes);
-            for (int kk = 0; kk < ksteps; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              umma_bf16(tmem + ab * 256 + us * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                        idesc, kk > 0 ? 1u : 0u);
-            }
+          const uint32_t ka = smem_u32(k_buf + ks * kKPair);
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * 32768 + (kk & 3) * 32;
+            umma_bf16(tmem + ab * 256, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), idesc,
+                      kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.k_empty[ks]);
           umma_commit(&sm.acc_full[ab]);
@@ -222,7 +205,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           ++a_iter;
         }
         if (!ok) break;
-        umma_commit(&sm.q_empty[qb]);
+        umma_commit(&sm.q_empty);
         ++q_iter;
       }
       // all MMAs retired before TMEM can be released
@@ -231,9 +214,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int us = (warp - 4) >> 2;            // sub-tile of this warpgroup
-    const int row = us * 128 + (warp & 3) * 32 + lane;  // row of the work item; TMEM lane (warp & 3) * 32 + lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + us * 128;
+    const int row = (warp - 4) * 32 + lane;  // TMEM lane == tile row
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     uint32_t a_iter = 0;
     for (uint32_t w = 0;; ++w) {
       const int slot = w & 1;
@@ -249,7 +231,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const SeqInfo si = p.seq[tile.x];
       int nq, lmax;
       tile_geometry(si, tile.y, p.qt, nq, lmax);
-      const int tq = row / p.hkv;               // query offset inside the work item
+      const int tq = row / p.hkv;               // query offset inside the tile
       const bool valid = tq < nq;
       const int t = tile.y + tq;
       const int pos = si.kv_len - si.q_len + t;
@@ -258,7 +240,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       TopkList<CAP> list;
       list.clear();
       bool ok = true;
-      for (int b = 0; b <= lmax; ++b) {
+      for (int bp = 0; 2 * bp <= lmax; ++bp) {
         const int ab = a_iter & 1;
         if (!mbar_wait_warp(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 122);
@@ -266,47 +248,46 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           break;
         }
         tc_fence_after();
-        // two halves of 64 columns: half the registers of one 128-column read
-        float m = -INFINITY;
-        const bool use = valid && b <= local;
-        const int lim = (b == local) ? (pos & 127) : 127;
 #pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          uint32_t r[2][32];
-          tmem_ld_32cols(lane_addr + ab * 256 + hv * 64, r[0]);
-          tmem_ld_32cols(lane_addr + ab * 256 + hv * 64 + 32, r[1]);
-          tmem_ld_wait_regs(r[0]);
-          regs_after_wait(r[1]);
-          if (hv == 1) {
+        for (int h = 0; h < 2; ++h) {  // block 2 bp + h: accumulator columns 128 h .. 128 h + 127
+          const int b = 2 * bp + h;
+          uint32_t r[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c]);
+          tmem_ld_wait();
+          if (h == 1) {
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[ab]);
           }
-          if (use) {
-            float m0 = -INFINITY, m1 = -INFINITY;
+          if (valid && b <= local) {
+            const int lim = (b == local) ? (pos & 127) : 127;
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
             if (lim == 127) {
 #pragma unroll
               for (int c = 0; c < 32; c += 2) {
                 m0 = fmax3(m0, __uint_as_float(r[0][c]), __uint_as_float(r[0][c + 1]));
                 m1 = fmax3(m1, __uint_as_float(r[1][c]), __uint_as_float(r[1][c + 1]));
+                m2 = fmax3(m2, __uint_as_float(r[2][c]), __uint_as_float(r[2][c + 1]));
+                m3 = fmax3(m3, __uint_as_float(r[3][c]), __uint_as_float(r[3][c + 1]));
               }
             } else {
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                m0 = fmaxf(m0, hv * 64 + c <= lim ? __uint_as_float(r[0][c]) : -INFINITY);
-                m1 = fmaxf(m1, hv * 64 + 32 + c <= lim ? __uint_as_float(r[1][c]) : -INFINITY);
+                m0 = fmaxf(m0, c <= lim ? __uint_as_float(r[0][c]) : -INFINITY);
+                m1 = fmaxf(m1, c + 32 <= lim ? __uint_as_float(r[1][c]) : -INFINITY);
+                m2 = fmaxf(m2, c + 64 <= lim ? __uint_as_float(r[2][c]) : -INFINITY);
+                m3 = fmaxf(m3, c + 96 <= lim ? __uint_as_float(r[3][c]) : -INFINITY);
               }
             }
-            m = fmax3(m, m0, m1);
+            const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            if constexpr (FUSED) {
+              if (b < local) list.insert(topk_key(m, b));
+            } else {
+              p.pooled[grow * p.pooled_stride + b] = m;
+            }
           }
         }
         ++a_iter;
-        if (use) {
-          if constexpr (FUSED) {
-            if (b < local) list.insert(topk_key(m, b));
-          } else {
-            p.pooled[grow * p.pooled_stride + b] = m;
-          }
-        }
       }
       if (!ok) break;
       if constexpr (FUSED) {
