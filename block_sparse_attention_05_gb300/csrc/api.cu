@@ -491,6 +491,7 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
   dp.part = partials(c);
   dp.scale_log2 = c.d.scale * 1.4426950408889634f;
   dp.hdr = c.hdr;
+  dp.sms = c.dev.sms;
   msa_status_t st;
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);

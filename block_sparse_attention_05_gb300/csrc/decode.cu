@@ -236,8 +236,11 @@ cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p,
 // ----------------------------------------------------------------------------
 namespace {
 
-constexpr int kDecThreads = 128;
-constexpr size_t kDecSmemBytes = 1024 + 2 * 32768 + 4 * 16 * 2 * sizeof(float) + 64;
+constexpr int kDecThreads = 128;  // compute warps; one more warp streams K and V
+constexpr int kDecStages = 1;  // one block per CTA; two CTAs per SM overlap load and compute
+constexpr size_t kDecSmemBytes =
+    1024 + kDecStages * 65536 + 4 * 16 * 128 * sizeof(float) + 4 * 16 * 2 * sizeof(float) + (2 * kDecStages + 3) * 8 +
+    16;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -254,200 +257,287 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 
 }  // namespace
 
-__global__ void __launch_bounds__(kDecThreads)
+// Persistent: two CTAs per SM, each walking the items (sequence, group, slot)
+// it owns (item = blockIdx.x + j * gridDim.x).  Warp 4 streams each valid
+// item's K and V block (64 KB) into the CTA's ring while warps 0..3 compute,
+// and the two CTAs of an SM overlap one's loads with the other's compute.
+// Both sides skip empty slots by the same test, so they agree on the ring
+// order.
+// Per item: 16 heads x 128 keys; each compute warp takes 32 keys (S = Q K^T
+// and O_w = P V with mma.sync m16n8k16, P split into bf16 hi + lo), then the
+// four warps merge through shared memory (each writes its scaled partial to
+// its own slice, then every element is summed over the four slices: no
+// shared-memory atomics).
+__global__ void __launch_bounds__(kDecThreads + 32)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        DecodeAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   if (hdr->status & kFlagBadSeqlens) return;
-  const int bid = blockIdx.x;
-  const int slot = bid % p.topk;
-  const int g = (bid / p.topk) % p.hkv;
-  const int s = bid / (p.topk * p.hkv);
-  const int64_t sel = (static_cast<int64_t>(s) * p.hkv + g) * p.topk + slot;
-  const int b = p.idx[sel];
-  const SeqInfo si = p.seq[s];
-  const int pos = si.kv_len - 1;
-  if (b < 0 || b > (pos >> 7)) return;  // empty slot: no partial, the combine skips it
-
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ks = base;            // K tile, 2 x 16 KB halves
-  uint8_t* vs = base + 32768;    // V tile
-  float* red = reinterpret_cast<float*>(base + 65536);          // [4 warps][16 heads][m, l]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 4 * 16 * 2);
-  int* abort_flag = reinterpret_cast<int*>(bar + 1);
+  uint8_t* ring = base;                                                    // kDecStages x (K 32 KB | V 32 KB)
+  float* osum = reinterpret_cast<float*>(base + kDecStages * 65536);       // [4 warps][16 heads][128] fp32
+  float* red = osum + 4 * 16 * 128;                                        // [4 warps][16 heads][m, l]
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + 4 * 16 * 2);
+  uint64_t* empty = full + kDecStages;
+  uint64_t* mrg = empty + kDecStages;  // per item: red written, partial sums added, merged output read
+  int* abort_flag = reinterpret_cast<int*>(mrg + 3);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int krow = si.k_start + b * kBlock;
+  const int G = p.group;  // 16
+  const long long n_items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
   if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+    for (int i = 0; i < kDecStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 4);  // one arrival per compute warp
+    }
+    for (int i = 0; i < 3; ++i) mbar_init(&mrg[i], 4);
     *abort_flag = 0;
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, 65536);
-    tma_load_3d(ks, &tm_k, bar, 0, g, krow);
-    tma_load_3d(ks + 16384, &tm_k, bar, 64, g, krow);
-    tma_load_3d(vs, &tm_v, bar, 0, g, krow);
-    tma_load_3d(vs + 16384, &tm_v, bar, 64, g, krow);
   }
-  // Q fragments (16 heads x 128 dims) straight from global memory
-  const int G = p.group;  // 16
-  const __nv_bfloat16* qg = p.q + (static_cast<int64_t>(s) * p.hkv * G + g * G) * kHeadDim;
-  uint32_t qa[8][4];
-  {
-    const int h0 = lane >> 2, d0 = (lane & 3) * 2;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      qa[k][0] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0);
-      qa[k][1] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0);
-      qa[k][2] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0 + 8);
-      qa[k][3] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0 + 8);
+  __syncthreads();
+
+  // the block of an item, or -1 for an empty slot (no partial; the combine skips it)
+  auto item_block = [&](long long it, int& s, int& g, int& b) {
+    const int slot = static_cast<int>(it % p.topk);
+    g = static_cast<int>((it / p.topk) % p.hkv);
+    s = static_cast<int>(it / (static_cast<long long>(p.topk) * p.hkv));
+    b = p.idx[it];  // it == (s * hkv + g) * topk + slot
+    const SeqInfo si = p.seq[s];
+    if (b < 0 || b > ((si.kv_len - 1) >> 7)) b = -1;
+    (void)slot;
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t n = 0;
+      for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+        int s, g, b;
+        item_block(it, s, g, b);
+        if (b < 0) continue;
+        const int st = n % kDecStages;
+        if (n >= kDecStages && !mbar_wait(&empty[st], ((n / kDecStages) - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 322);
+          break;
+        }
+        const int krow = p.seq[s].k_start + b * kBlock;
+        uint8_t* kv = ring + st * 65536;
+        mbar_arrive_expect_tx(&full[st], 65536);
+        tma_load_3d(kv, &tm_k, &full[st], 0, g, krow);
+        tma_load_3d(kv + 16384, &tm_k, &full[st], 64, g, krow);
+        tma_load_3d(kv + 32768, &tm_v, &full[st], 0, g, krow);
+        tma_load_3d(kv + 49152, &tm_v, &full[st], 64, g, krow);
+        ++n;
+      }
+      // let every issued copy land before the CTA exits
+      for (int st = 0; st < kDecStages; ++st)
+        if (n > static_cast<uint32_t>(st)) {
+          const uint32_t last = ((n - 1 - st) / kDecStages) * kDecStages + st;
+          mbar_wait(&full[st], (last / kDecStages) & 1, nullptr);
+        }
     }
-  }
-  __syncthreads();
-  if (!mbar_wait(bar, 0, abort_flag)) {
-    report_timeout(abort_flag, hdr, 321);
-  }
-  __syncthreads();
-  if (*reinterpret_cast<volatile int*>(abort_flag)) {
-    // the copies may still be in flight: wait once more (bounded) before leaving
-    mbar_wait(bar, 0, nullptr);
     return;
   }
-  const uint32_t kt = smem_u32(ks), vt = smem_u32(vs);
-  const int mtx = lane >> 3, mr = lane & 7;
 
-  // S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
-  float sacc[4][4];
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.f;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-#pragma unroll
-    for (int ntp = 0; ntp < 2; ++ntp) {
-      // matrices: (keys nt, d lo), (keys nt, d hi), (keys nt+1, d lo), (keys nt+1, d hi)
-      const int key = warp * 32 + (ntp * 2 + (mtx >> 1)) * 8 + mr;
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4(kt + sw128_off(key, k * 2 + (mtx & 1)), b0, b1, b2, b3);
-      mma_16816(sacc[ntp * 2], qa[k], b0, b1);
-      mma_16816(sacc[ntp * 2 + 1], qa[k], b2, b3);
+  // ------------------------------------------------------------ compute warps
+  // The four warps merge each item through shared memory; they meet at three
+  // mbarriers per item (bounded waits, so a timeout in one warp ends the others).
+  auto meet = [&](int k, uint32_t item_no) -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&mrg[k]);
+    if (!mbar_wait_warp(&mrg[k], item_no & 1, abort_flag)) {
+      if (lane == 0) report_timeout(abort_flag, hdr, 330 + k);
+      return false;
     }
-  }
-  // masked, scaled logits; per-head max and sum over this warp's keys
-  const int lim = pos - b * kBlock;
-  float m0 = -INFINITY, m1 = -INFINITY;
+    return true;
+  };
+  uint32_t n = 0;
+  for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+    int s, g, b;
+    item_block(it, s, g, b);
+    if (b < 0) continue;
+    const SeqInfo si = p.seq[s];
+    const int pos = si.kv_len - 1;
+    const long long sel = it;
+    const int st = n % kDecStages;
+    // Q fragments (16 heads x 128 dims) straight from global memory
+    const __nv_bfloat16* qg = p.q + (static_cast<int64_t>(s) * p.hkv * G + g * G) * kHeadDim;
+    uint32_t qa[8][4];
+    {
+      const int h0 = lane >> 2, d0 = (lane & 3) * 2;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int c0 = warp * 32 + nt * 8 + (lane & 3) * 2;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = c0 + (j & 1);
-      const float x = (c <= lim) ? sacc[nt][j] * p.scale_log2 : -INFINITY;
-      sacc[nt][j] = x;
+      for (int k = 0; k < 8; ++k) {
+        qa[k][0] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0);
+        qa[k][1] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0);
+        qa[k][2] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0 + 8);
+        qa[k][3] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0 + 8);
+      }
     }
-    m0 = fmaxf(m0, fmaxf(sacc[nt][0], sacc[nt][1]));
-    m1 = fmaxf(m1, fmaxf(sacc[nt][2], sacc[nt][3]));
-  }
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, o));
-  }
-  const float r0 = (m0 == -INFINITY) ? 0.f : m0, r1 = (m1 == -INFINITY) ? 0.f : m1;
-  float l0 = 0.f, l1 = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    sacc[nt][0] = exp2f(sacc[nt][0] - r0);
-    sacc[nt][1] = exp2f(sacc[nt][1] - r0);
-    sacc[nt][2] = exp2f(sacc[nt][2] - r1);
-    sacc[nt][3] = exp2f(sacc[nt][3] - r1);
-    l0 += sacc[nt][0] + sacc[nt][1];
-    l1 += sacc[nt][2] + sacc[nt][3];
-  }
-#pragma unroll
-  for (int o = 1; o < 4; o <<= 1) {
-    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
-    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
-  }
-  // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
-  float oacc[16][4];
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) oacc[nt][j] = 0.f;
-#pragma unroll
-  for (int kj = 0; kj < 2; ++kj) {
-    // P = hi + lo (both bf16): ~16 significant bits for the PV product
-    uint32_t pa[4], pl[4];
-    split_bf16x2(sacc[2 * kj][0], sacc[2 * kj][1], pa[0], pl[0]);
-    split_bf16x2(sacc[2 * kj][2], sacc[2 * kj][3], pa[1], pl[1]);
-    split_bf16x2(sacc[2 * kj + 1][0], sacc[2 * kj + 1][1], pa[2], pl[2]);
-    split_bf16x2(sacc[2 * kj + 1][2], sacc[2 * kj + 1][3], pa[3], pl[3]);
-#pragma unroll
-    for (int dp = 0; dp < 8; ++dp) {
-      // matrices: (keys lo, d 16dp..+7), (keys hi, same d), (keys lo, d +8..15), (keys hi, d +8..15)
-      const int key = warp * 32 + kj * 16 + (mtx & 1) * 8 + mr;
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(vt + sw128_off(key, dp * 2 + (mtx >> 1)), b0, b1, b2, b3);
-      mma_16816(oacc[2 * dp], pa, b0, b1);
-      mma_16816(oacc[2 * dp + 1], pa, b2, b3);
-      mma_16816(oacc[2 * dp], pl, b0, b1);
-      mma_16816(oacc[2 * dp + 1], pl, b2, b3);
+    if (!mbar_wait_warp(&full[st], (n / kDecStages) & 1, abort_flag)) {
+      if (lane == 0) report_timeout(abort_flag, hdr, 321);
+      break;
     }
-  }
-  // merge the four warps: rescale to the common max, sum, normalise
-  const int h0 = lane >> 2;
-  if ((lane & 3) == 0) {
-    red[(warp * 16 + h0) * 2 + 0] = m0;
-    red[(warp * 16 + h0) * 2 + 1] = l0;
-    red[(warp * 16 + h0 + 8) * 2 + 0] = m1;
-    red[(warp * 16 + h0 + 8) * 2 + 1] = l1;
-  }
-  __syncthreads();  // all warps are done with K and V from here on
-  float M0 = -INFINITY, M1 = -INFINITY;
+    const uint32_t kt = smem_u32(ring + st * 65536), vt = kt + 32768;
+    const int mtx = lane >> 3, mr = lane & 7;
+
+    // S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
+    float sacc[4][4];
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    M0 = fmaxf(M0, red[(w * 16 + h0) * 2]);
-    M1 = fmaxf(M1, red[(w * 16 + h0 + 8) * 2]);
-  }
-  const float R0 = (M0 == -INFINITY) ? 0.f : M0, R1 = (M1 == -INFINITY) ? 0.f : M1;
-  float L0 = 0.f, L1 = 0.f;
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float mw0 = red[(w * 16 + h0) * 2], mw1 = red[(w * 16 + h0 + 8) * 2];
-    L0 += (mw0 == -INFINITY) ? 0.f : red[(w * 16 + h0) * 2 + 1] * exp2f(mw0 - R0);
-    L1 += (mw1 == -INFINITY) ? 0.f : red[(w * 16 + h0 + 8) * 2 + 1] * exp2f(mw1 - R1);
-  }
-  const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0;
-  const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1;
-  // sum of the four warps' scaled partial outputs, through shared memory (reuses the K tile)
-  float* osum = reinterpret_cast<float*>(base);  // [16 heads][128] fp32 = 8 KB
-  for (int i = threadIdx.x; i < 16 * 128; i += kDecThreads) osum[i] = 0.f;
-  __syncthreads();
+      for (int j = 0; j < 4; ++j) sacc[nt][j] = 0.f;
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int d = nt * 8 + (lane & 3) * 2;
-    atomicAdd(&osum[h0 * 128 + d], oacc[nt][0] * f0);
-    atomicAdd(&osum[h0 * 128 + d + 1], oacc[nt][1] * f0);
-    atomicAdd(&osum[(h0 + 8) * 128 + d], oacc[nt][2] * f1);
-    atomicAdd(&osum[(h0 + 8) * 128 + d + 1], oacc[nt][3] * f1);
-  }
-  __syncthreads();
-  __nv_bfloat16* out = p.part.o + sel * G * kHeadDim;
-  for (int i = threadIdx.x * 2; i < 16 * 128; i += kDecThreads * 2)
-    *reinterpret_cast<uint32_t*>(out + i) = pack_bf16x2(osum[i], osum[i + 1]);
-  if (threadIdx.x < 16) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * 2]);
-    float L = 0.f;
+    for (int k = 0; k < 8; ++k) {
+#pragma unroll
+      for (int ntp = 0; ntp < 2; ++ntp) {
+        // matrices: (keys nt, d lo), (keys nt, d hi), (keys nt+1, d lo), (keys nt+1, d hi)
+        const int key = warp * 32 + (ntp * 2 + (mtx >> 1)) * 8 + mr;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(kt + sw128_off(key, k * 2 + (mtx & 1)), b0, b1, b2, b3);
+        mma_16816(sacc[ntp * 2], qa[k], b0, b1);
+        mma_16816(sacc[ntp * 2 + 1], qa[k], b2, b3);
+      }
+    }
+    // masked, scaled logits; per-head max and sum over this warp's keys
+    const int lim = pos - b * kBlock;
+    float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int c0 = warp * 32 + nt * 8 + (lane & 3) * 2;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + (j & 1);
+        const float x = (c <= lim) ? sacc[nt][j] * p.scale_log2 : -INFINITY;
+        sacc[nt][j] = x;
+      }
+      m0 = fmaxf(m0, fmaxf(sacc[nt][0], sacc[nt][1]));
+      m1 = fmaxf(m1, fmaxf(sacc[nt][2], sacc[nt][3]));
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, o));
+    }
+    const float r0 = (m0 == -INFINITY) ? 0.f : m0, r1 = (m1 == -INFINITY) ? 0.f : m1;
+    float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sacc[nt][0] = exp2f(sacc[nt][0] - r0);
+      sacc[nt][1] = exp2f(sacc[nt][1] - r0);
+      sacc[nt][2] = exp2f(sacc[nt][2] - r1);
+      sacc[nt][3] = exp2f(sacc[nt][3] - r1);
+      l0 += sacc[nt][0] + sacc[nt][1];
+      l1 += sacc[nt][2] + sacc[nt][3];
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
+      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
+    }
+    // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
+    float oacc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) oacc[nt][j] = 0.f;
+#pragma unroll
+    for (int kj = 0; kj < 2; ++kj) {
+      // P = hi + lo (both bf16): ~16 significant bits for the PV product
+      uint32_t pa[4], pl[4];
+      split_bf16x2(sacc[2 * kj][0], sacc[2 * kj][1], pa[0], pl[0]);
+      split_bf16x2(sacc[2 * kj][2], sacc[2 * kj][3], pa[1], pl[1]);
+      split_bf16x2(sacc[2 * kj + 1][0], sacc[2 * kj + 1][1], pa[2], pl[2]);
+      split_bf16x2(sacc[2 * kj + 1][2], sacc[2 * kj + 1][3], pa[3], pl[3]);
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        // matrices: (keys lo, d 16dp..+7), (keys hi, same d), (keys lo, d +8..15), (keys hi, d +8..15)
+        const int key = warp * 32 + kj * 16 + (mtx & 1) * 8 + mr;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(vt + sw128_off(key, dp * 2 + (mtx >> 1)), b0, b1, b2, b3);
+        mma_16816(oacc[2 * dp], pa, b0, b1);
+        mma_16816(oacc[2 * dp + 1], pa, b2, b3);
+        mma_16816(oacc[2 * dp], pl, b0, b1);
+        mma_16816(oacc[2 * dp + 1], pl, b2, b3);
+      }
+    }
+    // this warp is done with the stage's K and V
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    ++n;
+    // merge the four warps: rescale to the common max, sum, normalise
+    const int h0 = lane >> 2;
+    if ((lane & 3) == 0) {
+      red[(warp * 16 + h0) * 2 + 0] = m0;
+      red[(warp * 16 + h0) * 2 + 1] = l0;
+      red[(warp * 16 + h0 + 8) * 2 + 0] = m1;
+      red[(warp * 16 + h0 + 8) * 2 + 1] = l1;
+    }
+    if (!meet(0, n - 1)) break;
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
     for (int w = 0; w < 4; ++w) {
-      const float mw = red[(w * 16 + h) * 2];
-      if (mw != -INFINITY) L += red[(w * 16 + h) * 2 + 1] * exp2f(mw - M);
+      M0 = fmaxf(M0, red[(w * 16 + h0) * 2]);
+      M1 = fmaxf(M1, red[(w * 16 + h0 + 8) * 2]);
     }
-    const float lse = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
-    p.part.lse[sel * G + h] = lse;
-    p.part.ow[sel * G + h] = lse;  // o is stored normalised
+    const float R0 = (M0 == -INFINITY) ? 0.f : M0, R1 = (M1 == -INFINITY) ? 0.f : M1;
+    float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw0 = red[(w * 16 + h0) * 2], mw1 = red[(w * 16 + h0 + 8) * 2];
+      L0 += (mw0 == -INFINITY) ? 0.f : red[(w * 16 + h0) * 2 + 1] * exp2f(mw0 - R0);
+      L1 += (mw1 == -INFINITY) ? 0.f : red[(w * 16 + h0 + 8) * 2 + 1] * exp2f(mw1 - R1);
+    }
+    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0;
+    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1;
+    // each warp's scaled partial into its own slice, then a 4-way sum per element
+    float* mine = osum + warp * 16 * 128;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int d = nt * 8 + (lane & 3) * 2;
+      *reinterpret_cast<float2*>(&mine[h0 * 128 + d]) = make_float2(oacc[nt][0] * f0, oacc[nt][1] * f0);
+      *reinterpret_cast<float2*>(&mine[(h0 + 8) * 128 + d]) = make_float2(oacc[nt][2] * f1, oacc[nt][3] * f1);
+    }
+    if (!meet(1, n - 1)) break;
+    __nv_bfloat16* out = p.part.o + sel * G * kHeadDim;
+    for (int i = threadIdx.x * 8; i < 16 * 128; i += kDecThreads * 8) {
+      float acc[8];
+#pragma unroll
+      for (int j = 0; j < 8; j += 4) {
+        float4 a = *reinterpret_cast<const float4*>(&osum[i + j]);
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+          const float4 b4 = *reinterpret_cast<const float4*>(&osum[w * 16 * 128 + i + j]);
+          a.x += b4.x;
+          a.y += b4.y;
+          a.z += b4.z;
+          a.w += b4.w;
+        }
+        acc[j] = a.x;
+        acc[j + 1] = a.y;
+        acc[j + 2] = a.z;
+        acc[j + 3] = a.w;
+      }
+      uint4 v;
+      v.x = pack_bf16x2(acc[0], acc[1]);
+      v.y = pack_bf16x2(acc[2], acc[3]);
+      v.z = pack_bf16x2(acc[4], acc[5]);
+      v.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + i) = v;
+    }
+    if (threadIdx.x < 16) {
+      const int h = threadIdx.x;
+      float M = -INFINITY;
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * 2]);
+      float L = 0.f;
+      for (int w = 0; w < 4; ++w) {
+        const float mw = red[(w * 16 + h) * 2];
+        if (mw != -INFINITY) L += red[(w * 16 + h) * 2 + 1] * exp2f(mw - M);
+      }
+      const float lse = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
+      p.part.lse[sel * G + h] = lse;
+      p.part.ow[sel * G + h] = lse;  // o is stored normalised
+    }
+    if (!meet(2, n - 1)) break;  // red and osum are reused by the next item
   }
 }
 
@@ -455,12 +545,13 @@ size_t decode_attn_smem_bytes() { return kDecSmemBytes; }
 
 cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeAttnParams& p,
                                cudaStream_t stream) {
-  const long long grid = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
-  if (grid == 0) return cudaSuccess;
+  const long long items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
+  if (items == 0) return cudaSuccess;
+  const long long grid = items < 2LL * p.sms ? items : 2LL * p.sms;  // persistent: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDecSmemBytes));
   if (e != cudaSuccess) return e;
-  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads, kDecSmemBytes, stream>>>(tk, tv, p);
+  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads + 32, kDecSmemBytes, stream>>>(tk, tv, p);
   note_launches(1);
   return cudaGetLastError();
 }

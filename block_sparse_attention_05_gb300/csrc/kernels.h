@@ -137,6 +137,7 @@ cudaError_t launch_sparse_attn(const CUtensorMap& tq, const CUtensorMap& tk, con
 
 struct DecodeAttnParams {
   int num_seqs, hkv, group, topk;
+  int sms;                 // persistent grid size
   const SeqInfo* seq;
   const __nv_bfloat16* q;  // [num_seqs, hq, 128]
   const int32_t* idx;      // [num_seqs, hkv, topk]
