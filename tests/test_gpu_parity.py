@@ -38,6 +38,10 @@ SMALL_CASES = {
     "k_covers_all": dict(seqs=((200, 200), (64, 1000)), hq=64, hkv=4, d_idx=128, topk=16, n_topics=4),
     "k_small": dict(seqs=((1100, 1100),), hq=32, hkv=4, d_idx=128, topk=2, n_topics=8),
     "k_one": dict(seqs=((520, 520),), hq=64, hkv=4, d_idx=64, topk=1, n_topics=8),
+    # larger groups: 4, 2 and 1 queries per Main Branch tile; one index head (Hkv = 1: 128 queries per tile)
+    "g32": dict(seqs=((600, 600), (333, 1400)), hq=64, hkv=2, d_idx=128, topk=8, n_topics=8),
+    "g64": dict(seqs=((500, 900),), hq=64, hkv=1, d_idx=64, topk=6, n_topics=8),
+    "g128": dict(seqs=((400, 400), (130, 700)), hq=128, hkv=1, d_idx=128, topk=4, n_topics=4),
 }
 
 
