@@ -365,41 +365,85 @@ def main():
         stages[k] = e
 
     # ---------------- end to end through the C ABI with host buffers
+    # Every step copies its inputs in from pinned host memory and its outputs back, inside the timed
+    # region.  Two buffer sets: step n+1's inputs go in (one copy stream) and step n-1's outputs come back
+    # (another) while step n computes on the library's stream.
+    # Decode keeps the KV cache (k, v, k_idx) resident on the device as state: a step brings in the new
+    # token's q and q_idx and its own k, v and k_idx rows, which are appended into the cache on the device.
     e2e = None
     if not args.no_e2e:
-        host_in = {n: getattr(x, n).cpu().pin_memory() for n in ("q", "k", "v", "q_idx", "k_idx", "cu_q", "cu_k")}
-        dev_in = {n: torch.empty_like(getattr(x, n)) for n in host_in}
-        host_out = {"idx": torch.empty(idx.shape, dtype=idx.dtype).pin_memory(),
-                    "o": torch.empty(o.shape, dtype=o.dtype).pin_memory(),
-                    "lse": torch.empty(lse.shape, dtype=lse.dtype).pin_memory()}
-        prob_e = msa.Problem(dev_in["cu_q"], dev_in["cu_k"], x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq,
-                             cfg.hkv, cfg.d_idx, cfg.topk)
+        nbuf = 2
+        if cfg.is_decode:
+            rows = (x.cu_k[1:].long() - 1)                       # cache row of each sequence's new token
+            names = ("q", "q_idx", "k_new", "v_new", "k_idx_new")
+            src = {"q": x.q, "q_idx": x.q_idx, "k_new": x.k[rows], "v_new": x.v[rows], "k_idx_new": x.k_idx[rows]}
+        else:
+            names = ("q", "k", "v", "q_idx", "k_idx", "cu_q", "cu_k")
+            src = {n: getattr(x, n) for n in names}
+        host_in = {n: src[n].cpu().pin_memory() for n in names}
+        dev_in = [{n: torch.empty_like(src[n]) for n in names} for _ in range(nbuf)]
+        if cfg.is_decode:
+            for d in dev_in:  # the resident cache and sequence layout are shared by both buffer sets
+                d.update(k=x.k, v=x.v, k_idx=x.k_idx, cu_q=x.cu_q, cu_k=x.cu_k)
+        dev_out = [dict(idx=torch.empty_like(idx), o=torch.empty_like(o), lse=torch.empty_like(lse))
+                   for _ in range(nbuf)]
+        host_out = [{n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in d.items()} for d in dev_out]
+        probs = [msa.Problem(dev_in[i]["cu_q"], dev_in[i]["cu_k"], x.total_q, x.total_k, x.max_q, x.max_k,
+                             cfg.hq, cfg.hkv, cfg.d_idx, cfg.topk) for i in range(nbuf)]
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
+        s_comp = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_done = [torch.cuda.Event() for _ in range(nbuf)]
+        ev_out = [torch.cuda.Event() for _ in range(nbuf)]
 
-        def e2e_step():
-            for n, t in host_in.items():
-                dev_in[n].copy_(t, non_blocking=True)
-            msa.msa_forward(prob_e, dev_in["q"], dev_in["k"], dev_in["v"], dev_in["q_idx"], dev_in["k_idx"],
-                            idx=idx, o=o, lse=lse, ws=ws)
-            host_out["idx"].copy_(idx, non_blocking=True)
-            host_out["o"].copy_(o, non_blocking=True)
-            host_out["lse"].copy_(lse, non_blocking=True)
+        def e2e_step(n):
+            bi = n % nbuf
+            with torch.cuda.stream(s_in):
+                if n >= nbuf:
+                    s_in.wait_event(ev_done[bi])  # step n-2 has finished reading these inputs
+                for name in names:
+                    dev_in[bi][name].copy_(host_in[name], non_blocking=True)
+                ev_in[bi].record(s_in)
+            s_comp.wait_event(ev_in[bi])
+            if n >= nbuf:
+                s_comp.wait_event(ev_out[bi])  # step n-2's outputs have been copied out
+            if cfg.is_decode:  # append the new token's rows to the resident cache
+                x.k.index_copy_(0, rows, dev_in[bi]["k_new"])
+                x.v.index_copy_(0, rows, dev_in[bi]["v_new"])
+                x.k_idx.index_copy_(0, rows, dev_in[bi]["k_idx_new"])
+            d = dev_out[bi]
+            msa.msa_forward(probs[bi], dev_in[bi]["q"], dev_in[bi]["k"], dev_in[bi]["v"], dev_in[bi]["q_idx"],
+                            dev_in[bi]["k_idx"], idx=d["idx"], o=d["o"], lse=d["lse"], ws=ws)
+            ev_done[bi].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[bi])
+                for name in ("idx", "o", "lse"):
+                    host_out[bi][name].copy_(d[name], non_blocking=True)
+                ev_out[bi].record(s_out)
 
-        for _ in range(2):
-            e2e_step()
+        for n in range(2 * nbuf):
+            e2e_step(n)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for _ in range(args.steps):
-            e2e_step()
-        t1.record()
+        t0.record(s_comp)
+        s_in.wait_event(t0)
+        s_out.wait_event(t0)
+        for n in range(args.steps):
+            e2e_step(n + 2 * nbuf)
+        for ev in ev_out:
+            s_comp.wait_event(ev)  # every step's outputs are back in host memory
+        t1.record(s_comp)
         t1.synchronize()
         e2e_ms = t0.elapsed_time(t1) / args.steps
         e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "overlap": "two buffer sets: step n+1's inputs in and step n-1's outputs out during step n"}
+        if cfg.is_decode:
+            e2e["inputs"] = "q, q_idx and the new token's k, v, k_idx rows (appended on the device); KV cache resident"
 
     # ---------------- CPU oracle baseline (rank 0, N = 1 only)
     cpu = None
