@@ -42,8 +42,22 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   const int lo = warp * per, hi = min(local, lo + per);
   TopkList<CAP> lst;
   lst.clear();
-  for (int b = lo + lane; b < hi; b += 32)
-    if (index_ok(p.hdr, b, p.max_nb, 501)) lst.insert(topk_key(pr[b], b));
+  // eight loads in flight per lane before any insertion (one memory round
+  // trip per eight values instead of one per value)
+  for (int b0 = lo + lane; b0 < hi; b0 += 8 * 32) {
+    float v[8];
+    unsigned ok = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int b = b0 + 32 * j;
+      const bool use = b < hi && index_ok(p.hdr, b, p.max_nb, 501);
+      v[j] = use ? pr[b] : 0.f;
+      ok |= use ? (1u << j) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ok & (1u << j)) lst.insert(topk_key(v[j], b0 + 32 * j));
+  }
 #pragma unroll
   for (int r = 0; r < CAP; ++r) {
     if (r < want) {
