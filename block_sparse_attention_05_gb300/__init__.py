@@ -95,6 +95,9 @@ _lib.msa_sparse_attn_decode_static.restype = ctypes.c_int
 _lib.msa_sparse_attn_decode_static.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.msa_forward.restype = ctypes.c_int
 _lib.msa_forward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.msa_forward_decode_paged.restype = ctypes.c_int
+_lib.msa_forward_decode_paged.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp,
+                                          _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
 _lib.msa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.msa_set_stage_events.restype = ctypes.c_int
@@ -284,6 +287,30 @@ def msa_forward(problem: Problem, q, k, v, q_idx, k_idx, idx=None, o=None, lse=N
     ws, nws = _ws(problem, Op.FORWARD, ws)
     _check(_lib.msa_forward(ctypes.byref(problem.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx),
                             _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()), "msa_forward")
+    return idx, o, lse
+
+
+def msa_forward_decode_paged(problem: Problem, q, k_cache, v_cache, q_idx, k_idx_cache, block_table, idx=None,
+                             o=None, lse=None, ws=None):
+    """Decode from paged caches ([num_pages * 128, ...] rows, block_table int32 [num_seqs, max_blocks]).
+    Returns (idx, o, lse) as msa_forward."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache"), (q_idx, "q_idx"), (k_idx_cache, "k_idx_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or k_cache.shape[0] % 128:
+        raise ValueError("block_table must be [num_seqs, max_blocks] and the caches whole pages of 128 rows")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.FORWARD, ws)
+    _check(_lib.msa_forward_decode_paged(ctypes.byref(problem.c()), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(q_idx), _ptr(k_idx_cache), _ptr(block_table), block_table.shape[1],
+                                         k_cache.shape[0] // 128, _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws,
+                                         _stream()), "msa_forward_decode_paged")
     return idx, o, lse
 
 

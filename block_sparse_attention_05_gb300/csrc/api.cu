@@ -253,6 +253,11 @@ struct Ctx {
   SeqInfo* seq;
   cudaStream_t stream;
   void* ws;
+  // decode from a paged cache (msa_forward_decode_paged): null block_table = packed rows
+  const int32_t* block_table = nullptr;
+  int bt_stride = 0;
+  long long n_pages = 0;
+  long long cache_rows() const { return block_table ? n_pages * 128 : d.N; }
 };
 
 msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_bytes, msa_stream_t stream,
@@ -355,7 +360,7 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
 msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx, const void* k_idx, int32_t* idx) {
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tk;
-  if (!map_2d(tk, k_idx, c.d.N, c.d.d_idx, 128)) return MSA_ERR_CUDA;
+  if (!map_2d(tk, k_idx, c.cache_rows(), c.d.d_idx, 128)) return MSA_ERR_CUDA;
   float* pooled = at<float>(c.ws, c.L.pooled);
   DecodeScanParams sp{};
   sp.num_seqs = c.d.S;
@@ -374,8 +379,11 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   ups = (c.d.max_nb + bpu - 1) / bpu;
   sp.units_per_seq = ups;
   sp.blocks_per_unit = bpu;
-  sp.total_k = c.d.N;
+  sp.total_k = c.cache_rows();
   sp.hdr = c.hdr;
+  sp.block_table = c.block_table;
+  sp.bt_stride = c.bt_stride;
+  sp.n_pages = c.n_pages;
   long long units = static_cast<long long>(c.d.S) * ups;
   int grid = static_cast<int>(units < c.dev.sms ? units : c.dev.sms);
   if (grid < 1) grid = 1;
@@ -479,7 +487,8 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
                              const int32_t* idx, void* o, float* lse) {
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tk, tv;
-  if (!map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) || !map_3d(tv, v, c.d.N, c.d.hkv, 1, 128)) return MSA_ERR_CUDA;
+  if (!map_3d(tk, k, c.cache_rows(), c.d.hkv, 1, 128) || !map_3d(tv, v, c.cache_rows(), c.d.hkv, 1, 128))
+    return MSA_ERR_CUDA;
   DecodeAttnParams dp{};
   dp.num_seqs = c.d.S;
   dp.hkv = c.d.hkv;
@@ -492,6 +501,9 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
   dp.scale_log2 = c.d.scale * 1.4426950408889634f;
   dp.hdr = c.hdr;
   dp.sms = c.dev.sms;
+  dp.block_table = c.block_table;
+  dp.bt_stride = c.bt_stride;
+  dp.n_pages = c.n_pages;
   msa_status_t st;
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);
@@ -713,6 +725,31 @@ msa_status_t msa_forward(const msa_problem_t* problem, const void* q, const void
   if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
   if ((st = run_index_prefill(problem, c, q_idx, k_idx, true, nullptr, 0, idx)) != MSA_OK) return st;
   return run_attn_prefill(problem, c, q, k, v, idx, o, lse);
+}
+
+msa_status_t msa_forward_decode_paged(const msa_problem_t* problem, const void* q, const void* k_cache,
+                                      const void* v_cache, const void* q_idx, const void* k_idx_cache,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq, int64_t num_pages,
+                                      int32_t* idx, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                      msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!d.decode) return MSA_ERR_INVALID_ARG;  // one query per sequence
+  if ((st = check_attn_args(q, k_cache, v_cache, idx, o, lse)) != MSA_OK) return st;
+  if (!q_idx || !k_idx_cache || !block_table) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx_cache) || (reinterpret_cast<uintptr_t>(block_table) & 3u))
+    return MSA_ERR_ALIGNMENT;
+  if (num_pages < 1 || num_pages * 128 >= (1LL << 31)) return MSA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < d.max_nb) return MSA_ERR_INVALID_ARG;  // a row must hold every block of the longest sequence
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_FORWARD, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  c.block_table = block_table;
+  c.bt_stride = max_blocks_per_seq;
+  c.n_pages = num_pages;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  if ((st = run_index_decode(problem, c, q_idx, k_idx_cache, idx)) != MSA_OK) return st;
+  return run_attn_decode(problem, c, q, k_cache, v_cache, idx, o, lse);
 }
 
 msa_status_t msa_read_device_status(const void* workspace, uint32_t* flags, msa_stream_t stream) {

@@ -131,6 +131,25 @@ __device__ __forceinline__ void report_timeout(volatile int* abort_flag, WsHeade
   atomicExch(&hdr->timeout_site, site);
 }
 
+// First row of key block b of sequence s: packed (k_start + 128 b) or, with a
+// block table, its page times 128.  A page outside the cache is recorded in
+// the status (always, not only in checked builds) and mapped to a row past
+// the end of the cache, which a TMA load reads as zeros instead of faulting.
+__device__ __forceinline__ int key_block_row(const int32_t* block_table, int bt_stride, long long n_pages,
+                                             int k_start, int s, int b, WsHeader* hdr) {
+  if (!block_table) return k_start + b * 128;
+  const int page = block_table[static_cast<long long>(s) * bt_stride + b];
+  if (page < 0 || page >= n_pages) {
+    if (atomicCAS(&hdr->bad_site, 0u, 601u) == 0u) {
+      hdr->bad_index = page;
+      hdr->bad_bound = n_pages;
+    }
+    atomicOr(&hdr->status, 4u);  // MSA_DEVICE_BAD_INDEX
+    return static_cast<int>(n_pages) * 128;
+  }
+  return page * 128;
+}
+
 // True when 0 <= i < n; otherwise (in checked builds) records the failure.
 __device__ __forceinline__ bool index_ok(WsHeader* hdr, long long i, long long n, uint32_t site) {
 #if MSA_CHECKED

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
           report_timeout(abort_flag, hdr, 301);
           break;
         }
-        const int row = p.seq[c.s].k_start + c.b * kBlock;
+        const int row = key_block_row(p.block_table, p.bt_stride, p.n_pages, p.seq[c.s].k_start, c.s, c.b, hdr);
         index_ok(hdr, c.s, p.num_seqs, 401);
         index_ok(hdr, row, p.total_k, 402);
         mbar_arrive_expect_tx(&sm.full[st], tile_tx);
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
           report_timeout(abort_flag, hdr, 322);
           break;
         }
-        const int krow = p.seq[s].k_start + b * kBlock;
+        const int krow = key_block_row(p.block_table, p.bt_stride, p.n_pages, p.seq[s].k_start, s, b, hdr);
         uint8_t* kv = ring + st * 65536;
         mbar_arrive_expect_tx(&full[st], 65536);
         tma_load_3d(kv, &tm_k, &full[st], 0, g, krow);

@@ -79,6 +79,11 @@ struct DecodeScanParams {
   int blocks_per_unit;
   long long total_k;            // rows of K_idx (for checked builds)
   WsHeader* hdr;
+  // Paged cache (optional): key block b of sequence s is page block_table[s * bt_stride + b] of 128 rows;
+  // null: packed rows starting at the sequence's k_start.
+  const int32_t* block_table;
+  int bt_stride;
+  long long n_pages;
 };
 size_t decode_scan_smem_bytes();
 cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream);
@@ -144,6 +149,9 @@ struct DecodeAttnParams {
   PartialBuffers part;
   float scale_log2;
   WsHeader* hdr;
+  const int32_t* block_table;  // as in DecodeScanParams
+  int bt_stride;
+  long long n_pages;
 };
 size_t decode_attn_smem_bytes();
 cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeAttnParams& p,

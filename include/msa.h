@@ -81,7 +81,8 @@ typedef enum msa_status {
 /* Device-side error flags (msa_read_device_status). */
 #define MSA_DEVICE_TIMEOUT 1u        /* a kernel wait exceeded its time limit */
 #define MSA_DEVICE_BAD_SEQLENS 2u    /* cu_seqlens disagree with the host sizes */
-#define MSA_DEVICE_BAD_INDEX 4u      /* a computed index failed its check (checked builds only) */
+#define MSA_DEVICE_BAD_INDEX 4u      /* a computed index failed its check (checked builds), or a block-table
+                                        entry of msa_forward_decode_paged named a page outside the cache */
 
 typedef struct msa_problem {
   int32_t num_seqs;              /* >= 1 */
@@ -187,6 +188,38 @@ msa_status_t msa_forward(const msa_problem_t *problem, const void *q, const void
                          const void *v, const void *q_idx, const void *k_idx, int32_t *idx,
                          void *o, float *lse, void *workspace, size_t workspace_bytes,
                          msa_stream_t stream);
+
+/* msa_forward for a decode batch whose cache is paged: the same operation
+ * ("MiniMax Sparse Attention: let each query pick its own blocks", section
+ * "The mechanism, precisely": index scores over the cached keys, block
+ * max-pool, top-k with the local block forced, exact attention over the
+ * selected blocks), with K, V and K_idx read from pages of 128 tokens -- one
+ * key block each -- instead of packed rows.  The pages describe no paged
+ * layout; this is the decode call in the form a serving cache keeps it.
+ *   problem     as for msa_forward, every sequence with q_len = 1;
+ *               cu_seqlens_k gives the cached lengths (its offsets are not
+ *               used as row positions here).
+ *   k_cache, v_cache  [num_pages * 128, Hkv, 128] bf16; k_idx_cache
+ *               [num_pages * 128, d_idx] bf16.  Row 128 * p + t of a cache is
+ *               token t of page p.
+ *   block_table int32 [num_seqs, max_blocks_per_seq], device: key block b of
+ *               sequence s (tokens 128 b .. 128 b + 127) is page
+ *               block_table[s * max_blocks_per_seq + b]; entries past a
+ *               sequence's last block are not read.  4-byte aligned.
+ *   max_blocks_per_seq  row stride of block_table; at least
+ *               ceil(max_seqlen_k / 128).
+ *   num_pages   pages in each cache; num_pages * 128 < 2^31.
+ *   idx, o, lse, workspace, stream  as for msa_forward (workspace size: op
+ *               MSA_OP_FORWARD of the same problem).
+ * A block-table entry outside [0, num_pages) is not dereferenced: its block
+ * reads as zeros and the workspace status gets MSA_DEVICE_BAD_INDEX (read it
+ * with msa_read_device_status).  Host-side argument errors return before any
+ * launch, as for msa_forward. */
+msa_status_t msa_forward_decode_paged(const msa_problem_t *problem, const void *q, const void *k_cache,
+                                      const void *v_cache, const void *q_idx, const void *k_idx_cache,
+                                      const int32_t *block_table, int32_t max_blocks_per_seq,
+                                      int64_t num_pages, int32_t *idx, void *o, float *lse,
+                                      void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Waits for `stream`, then returns in *flags the MSA_DEVICE_* bits that the
  * last call on this workspace raised (0 = none).  The only synchronising call. */

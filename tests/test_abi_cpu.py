@@ -103,6 +103,21 @@ def test_calls_reject_bad_arguments_before_touching_the_device(msa):
                            None) == -2
 
 
+def test_paged_decode_rejects_bad_arguments_on_the_host(msa):
+    lib = msa._lib
+    dec = base_problem(msa, num_seqs=4, total_q=4, max_seqlen_q=1)
+    p = ctypes.byref(dec)
+    args = lambda bt=FAKE, mb=16, npg=100: (p, FAKE, FAKE, FAKE, FAKE, FAKE, bt, mb, npg, FAKE, FAKE, FAKE, FAKE,
+                                             1 << 40, None)
+    assert lib.msa_forward_decode_paged(*args(bt=None)) == -1        # no block table
+    assert lib.msa_forward_decode_paged(*args(bt=FAKE + 2)) == -3    # misaligned block table
+    assert lib.msa_forward_decode_paged(*args(npg=0)) == -1          # no pages
+    assert lib.msa_forward_decode_paged(*args(npg=1 << 24)) == -1    # rows past int32 coordinates
+    assert lib.msa_forward_decode_paged(*args(mb=7)) == -1           # a row cannot hold the longest sequence
+    pre = base_problem(msa)                                          # a prefill batch
+    assert lib.msa_forward_decode_paged(ctypes.byref(pre), *args()[1:]) == -1
+
+
 def test_status_strings(msa):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert msa._lib.msa_status_string(code)

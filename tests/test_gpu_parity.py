@@ -216,6 +216,72 @@ def test_forward_decode_end_to_end(msa, n, ctx, topk, d_idx):
     assert_attention_close(to_np(o2), to_np(lse2), ref, 16, what="decode, oracle indices")
 
 
+# ------------------------------------------------------------------ decode from a paged cache
+def _paged(x, cfg, seed, spare=5, stride_extra=2):
+    """Scatters the packed caches into pages of 128 rows in a random order (plus unused pages); returns the
+    paged k, v, k_idx caches and the block table [num_seqs, max_blocks + stride_extra] (junk past each row)."""
+    cu_k = x.cu_k.cpu().numpy()
+    n = len(cu_k) - 1
+    nbs = [int(cu_k[s + 1] - cu_k[s] + 127) // 128 for s in range(n)]
+    n_pages = sum(nbs) + spare
+    perm = np.random.default_rng(seed).permutation(n_pages)
+    bt = np.full((n, max(nbs) + stride_extra), -7, np.int32)
+    k_c = torch.zeros((n_pages * 128,) + tuple(x.k.shape[1:]), dtype=x.k.dtype, device="cuda")
+    v_c = torch.zeros_like(k_c)
+    ki_c = torch.zeros((n_pages * 128,) + tuple(x.k_idx.shape[1:]), dtype=x.k_idx.dtype, device="cuda")
+    at = 0
+    for s in range(n):
+        for b in range(nbs[s]):
+            pg = int(perm[at])
+            at += 1
+            bt[s, b] = pg
+            lo, hi = int(cu_k[s]) + 128 * b, min(int(cu_k[s]) + 128 * (b + 1), int(cu_k[s + 1]))
+            k_c[pg * 128: pg * 128 + hi - lo] = x.k[lo:hi]
+            v_c[pg * 128: pg * 128 + hi - lo] = x.v[lo:hi]
+            ki_c[pg * 128: pg * 128 + hi - lo] = x.k_idx[lo:hi]
+    return k_c, v_c, ki_c, torch.from_numpy(bt).cuda()
+
+
+@pytest.mark.parametrize("n,ctx,seed", [(12, 9000, 31), (3, 40000, 32), (2, 200, 33)])
+def test_forward_decode_paged(msa, n, ctx, seed):
+    """The paged cache gives the packed path's results bit for bit, and the oracle's within tolerance."""
+    cfg = decode_case(n, ctx, seed=seed)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    k_c, v_c, ki_c, bt = _paged(x, cfg, seed)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward_decode_paged(prob, x.q, k_c, v_c, x.q_idx, ki_c, bt, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
+    idx_p, o_p, lse_p = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_p) and torch.equal(o, o_p) and torch.equal(lse, lse_p)
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(to_np(idx), ref)
+    assert mism == 0
+    assert_attention_close(to_np(o), to_np(lse), ref, 16, exempt=tie, what="paged decode")
+
+
+def test_forward_decode_paged_bad_page_sets_a_flag(msa):
+    """A block-table entry outside the cache is not dereferenced: the call completes and the workspace
+    status carries MSA_DEVICE_BAD_INDEX."""
+    cfg = decode_case(4, 3000, seed=34)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    k_c, v_c, ki_c, bt = _paged(x, cfg, 34)
+    bt[1, 3] = k_c.shape[0] // 128 + 1000   # past the last page
+    bt[2, 0] = -5
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward_decode_paged(prob, x.q, k_c, v_c, x.q_idx, ki_c, bt, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) & 4  # MSA_DEVICE_BAD_INDEX
+    # the other sequences are unaffected
+    idx_p, o_p, _ = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    for s in (0, 3):
+        assert torch.equal(idx[s], idx_p[s]) and torch.equal(o[s], o_p[s])
+
+
 # ------------------------------------------------------------------ device-side validation
 def test_inconsistent_seqlens_raise_a_device_flag(msa):
     cfg = make_small("varlen_g16")
