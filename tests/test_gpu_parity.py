@@ -139,6 +139,31 @@ def test_sparse_attn_prefill_random_selections(msa):
     assert_attention_close(to_np(o), to_np(lse), {"o": o_ref, "lse": lse_ref}, 16, what="random selections")
 
 
+@pytest.mark.parametrize("spikes", [(100,), (40, 100), (33, 64, 127)])
+def test_sparse_attn_prefill_exponent_rescale(msa, spikes):
+    """Logits far above the first keys of a block: the softmax's exponent reference starts at the max of a
+    block's first 32 keys and is raised (with an exact power-of-two rescale of the P already stored) when a
+    later key exceeds it by more than 2^15 in P.  Spike keys at the given offsets of every block make their
+    logits exceed the first keys' by ~22 in log2 units."""
+    cfg = make_small("varlen_g16", seed=13)
+    x = workloads.generate(cfg, device="cuda")
+    q, k = x.q.clone(), x.k.clone()
+    q[:, :, 0] = 10.0
+    cu_k = x.cu_k.cpu().numpy()
+    for s_ in range(len(cu_k) - 1):
+        for b0 in range(int(cu_k[s_]), int(cu_k[s_ + 1]), 128):
+            for off in spikes:
+                if b0 + off < int(cu_k[s_ + 1]):
+                    k[b0 + off, :, :] = 0.0
+                    k[b0 + off, :, 0] = 20.0
+    prob = problem_for(msa, x)
+    ref = oracle.forward(x.cu_q, x.cu_k, q, k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    idx = torch.from_numpy(ref["idx"]).cuda()
+    o, lse = msa.msa_sparse_attn_prefill(prob, q, k, x.v, idx)
+    torch.cuda.synchronize()
+    assert_attention_close(to_np(o), to_np(lse), ref, cfg.hq // cfg.hkv, what=f"spikes at {spikes}")
+
+
 @pytest.mark.parametrize("shift", [20, 100])
 def test_sparse_attn_prefill_large_values(msa, shift):
     """V far outside fp16's range: attention is linear in V, so V * 2^shift (exact
