@@ -142,7 +142,7 @@ __device__ __forceinline__ int key_block_row(const int32_t* block_table, int bt_
       hdr->bad_index = page;
       hdr->bad_bound = n_pages;
     }
-    atomicOr(&hdr->status, 4u);  // MSA_DEVICE_BAD_INDEX
+    atomicOr(&hdr->status, kFlagBadIndex);
     return static_cast<int>(n_pages) * 128;
   }
   return page * 128;

@@ -139,6 +139,27 @@ def test_sparse_attn_prefill_random_selections(msa):
     assert_attention_close(to_np(o), to_np(lse), {"o": o_ref, "lse": lse_ref}, 16, what="random selections")
 
 
+def test_sparse_attn_prefill_scattered_selections(msa):
+    """Selections spread over more (group, key block) pairs than the schedule's per-CTA bucket table holds:
+    128 queries x 8 groups x 16 random blocks out of about 600 reach some 4600 of the 4800 buckets, more than the
+    table's 4096 slots, so part of the incidences take the global-counter path and the rest the table."""
+    cfg = small("scattered", ((256, 76800),), hq=64, hkv=8, d_idx=64, topk=16, n_topics=4, seed=12)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    rng = np.random.default_rng(6)
+    pos = oracle.query_positions(x.cu_q, x.cu_k)
+    local = (pos // 128).astype(np.int64)
+    assert local.min() == 598 and local.max() == 599
+    keys = rng.random((x.total_q, cfg.hkv, 600))
+    keys = np.where((np.arange(600)[None, :] > local[:, None])[:, None, :], np.inf, keys)  # causal blocks only
+    keys[np.arange(x.total_q), :, local] = -1.0  # the local block is always among the picks
+    idx = np.sort(np.argsort(keys, axis=2)[:, :, :cfg.topk], axis=2).astype(np.int32)
+    o, lse = msa.msa_sparse_attn_prefill(prob, x.q, x.k, x.v, torch.from_numpy(idx).cuda())
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention(x.cu_q, x.cu_k, x.q, x.k, x.v, idx, block=128)
+    assert_attention_close(to_np(o), to_np(lse), {"o": o_ref, "lse": lse_ref}, 8, what="scattered selections")
+
+
 @pytest.mark.parametrize("spikes", [(100,), (40, 100), (33, 64, 127)])
 def test_sparse_attn_prefill_exponent_rescale(msa, spikes):
     """Logits far above the first keys of a block: the softmax's exponent reference starts at the max of a
