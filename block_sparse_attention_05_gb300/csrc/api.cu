@@ -412,6 +412,7 @@ msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, voi
   cp.group = c.d.G;
   cp.topk = c.d.topk;
   cp.num_seqs = c.d.S;
+  cp.sms = c.dev.sms;
   cp.cu_q = p->cu_seqlens_q;
   cp.seq = c.seq;
   cp.idx = idx;

@@ -20,6 +20,12 @@
 // query's causal end hold no partial (their memory is never written, so its
 // contents are only ever selected away, never multiplied) and are skipped,
 // matching the scheduler.
+//
+// The kernel is a grid-stride loop (two CTAs per SM), and each warp first
+// prefetches into L2 the partial rows of the item it takes next.  A warp's
+// loads are bounded by its registers (16 slots x 16 bytes per lane); the
+// prefetches hold none, so the HBM stream keeps running while the warps
+// combine rows that are already in L2.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,71 +36,99 @@ namespace {
 constexpr int kCombineWarps = 8;
 constexpr int kMaxTopk = 16;
 
-__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombineParams p) {
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+struct PairRef {
+  int i, h, g, hh;
+  int64_t sel_base;
+};
+
+__device__ __forceinline__ PairRef pair_ref(const CombineParams& p, int64_t pair, int half) {
+  PairRef r;
+  r.i = static_cast<int>(pair / (p.hq >> 1));
+  r.h = static_cast<int>(pair % (p.hq >> 1)) * 2 + half;
+  r.g = r.h / p.group;
+  r.hh = r.h % p.group;
+  r.sel_base = (static_cast<int64_t>(r.i) * p.hkv + r.g) * p.topk;
+  return r;
+}
+
+__global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineParams p) {
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombineWarps + warp;  // (query, head pair)
-  if (pair >= static_cast<int64_t>(p.total_q) * (p.hq >> 1)) return;
   const int half = lane >> 4, hl = lane & 15;
-  const int i = static_cast<int>(pair / (p.hq >> 1));
-  const int h = static_cast<int>(pair % (p.hq >> 1)) * 2 + half;
-  const int g = h / p.group, hh = h % p.group;
-  const int64_t sel_base = (static_cast<int64_t>(i) * p.hkv + g) * p.topk;
-
-  int b = -1;
-  float l_s = -INFINITY, w_s = -INFINITY;
-  if (hl < p.topk) {
-    b = p.idx[sel_base + hl];
-    l_s = p.part.lse[(sel_base + hl) * p.group + hh];
-    w_s = p.part.ow[(sel_base + hl) * p.group + hh];
-  }
-  const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
+  const int64_t n_pairs = static_cast<int64_t>(p.total_q) * (p.hq >> 1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kCombineWarps;
   const int64_t slot_stride = static_cast<int64_t>(p.group) * kHeadDim;
-  uint4 raw[kMaxTopk];
-#pragma unroll
-  for (int sl = 0; sl < kMaxTopk; ++sl)
-    raw[sl] = (sl < p.topk) ? __ldcs(reinterpret_cast<const uint4*>(base + sl * slot_stride)) : make_uint4(0, 0, 0, 0);
+  for (int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombineWarps + warp; pair < n_pairs; pair += stride) {
+    // the next item's rows: lane (half, hl) covers slot hl of head 2 * pair + half, 256 bytes = 2 lines
+    if (pair + stride < n_pairs && hl < p.topk) {
+      const PairRef nx = pair_ref(p, pair + stride, half);
+      const __nv_bfloat16* row = p.part.o + ((nx.sel_base + hl) * p.group + nx.hh) * kHeadDim;
+      prefetch_l2(row);
+      prefetch_l2(row + 64);
+    }
+    const PairRef r = pair_ref(p, pair, half);
+    const int i = r.i, h = r.h, hh = r.hh;
+    const int64_t sel_base = r.sel_base;
 
-  const int s = find_seq(p.cu_q, p.num_seqs, i);
-  const SeqInfo si = p.seq[s];
-  const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
-  const bool valid = hl < p.topk && b >= 0 && b <= local;
-  if (!valid) l_s = -INFINITY;
+    int b = -1;
+    float l_s = -INFINITY, w_s = -INFINITY;
+    if (hl < p.topk) {
+      b = p.idx[sel_base + hl];
+      l_s = p.part.lse[(sel_base + hl) * p.group + hh];
+      w_s = p.part.ow[(sel_base + hl) * p.group + hh];
+    }
+    const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
+    uint4 raw[kMaxTopk];
+#pragma unroll
+    for (int sl = 0; sl < kMaxTopk; ++sl)
+      raw[sl] = (sl < p.topk) ? __ldcs(reinterpret_cast<const uint4*>(base + sl * slot_stride))
+                              : make_uint4(0, 0, 0, 0);
 
-  float m = l_s;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  float sum = valid ? expf(l_s - m) : 0.f;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-  const float L = m + logf(sum);
-  const float w = valid ? expf(w_s - L) : 0.f;
+    const int s = find_seq(p.cu_q, p.num_seqs, i);
+    const SeqInfo si = p.seq[s];
+    const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
+    const bool valid = hl < p.topk && b >= 0 && b <= local;
+    if (!valid) l_s = -INFINITY;
 
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float m = l_s;
 #pragma unroll
-  for (int sl = 0; sl < kMaxTopk; ++sl) {
-    const float ws = __shfl_sync(0xFFFFFFFFu, w, (lane & 16) | sl);
-    if (sl < p.topk && ws != 0.f) {
-      const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float sum = valid ? expf(l_s - m) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&v[j]);
-        acc[2 * j] = fmaf(ws, __low2float(t), acc[2 * j]);
-        acc[2 * j + 1] = fmaf(ws, __high2float(t), acc[2 * j + 1]);
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+    const float L = m + logf(sum);
+    const float w = valid ? expf(w_s - L) : 0.f;
+
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int sl = 0; sl < kMaxTopk; ++sl) {
+      const float ws = __shfl_sync(0xFFFFFFFFu, w, (lane & 16) | sl);
+      if (sl < p.topk && ws != 0.f) {
+        const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+          acc[2 * j] = fmaf(ws, __low2float(t), acc[2 * j]);
+          acc[2 * j + 1] = fmaf(ws, __high2float(t), acc[2 * j + 1]);
+        }
       }
     }
-  }
-  const bool empty = (m == -INFINITY);
-  uint4 out;
-  uint32_t* ow = &out.x;
+    const bool empty = (m == -INFINITY);
+    uint4 out;
+    uint32_t* ow = &out.x;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-    ow[j] = *reinterpret_cast<const uint32_t*>(&t);
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      ow[j] = *reinterpret_cast<const uint32_t*>(&t);
+    }
+    const int64_t orow = static_cast<int64_t>(i) * p.hq + h;
+    *reinterpret_cast<uint4*>(p.o + orow * kHeadDim + hl * 8) = out;
+    if (hl == 0) p.lse[orow] = empty ? -INFINITY : L;
   }
-  const int64_t row = static_cast<int64_t>(i) * p.hq + h;
-  *reinterpret_cast<uint4*>(p.o + row * kHeadDim + hl * 8) = out;
-  if (hl == 0) p.lse[row] = empty ? -INFINITY : L;
 }
 
 }  // namespace
@@ -102,7 +136,8 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(CombinePara
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   const int64_t pairs = static_cast<int64_t>(p.total_q) * (p.hq >> 1);  // hq is a multiple of 8
   if (pairs == 0) return cudaSuccess;
-  const int64_t grid = (pairs + kCombineWarps - 1) / kCombineWarps;
+  int64_t grid = (pairs + kCombineWarps - 1) / kCombineWarps;
+  if (grid > 2LL * p.sms) grid = 2LL * p.sms;
   combine_kernel<<<static_cast<unsigned>(grid), 32 * kCombineWarps, 0, stream>>>(p);
   note_launches(1);
   return cudaGetLastError();

@@ -159,6 +159,7 @@ cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, con
 
 struct CombineParams {
   int total_q, hq, hkv, group, topk, num_seqs;
+  int sms;  // grid: two CTAs per SM, grid-stride over the (query, head pair) items
   const int32_t* cu_q;
   const SeqInfo* seq;
   const int32_t* idx;
