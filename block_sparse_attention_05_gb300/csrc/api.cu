@@ -487,8 +487,9 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
 msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, const void* k, const void* v,
                              const int32_t* idx, void* o, float* lse) {
   if (c.d.T == 0) return MSA_OK;
-  CUtensorMap tk, tv;
-  if (!map_3d(tk, k, c.cache_rows(), c.d.hkv, 1, 128) || !map_3d(tv, v, c.cache_rows(), c.d.hkv, 1, 128))
+  CUtensorMap tq, tk, tv;
+  if (!map_3d(tq, q, c.d.T, c.d.hq, 16, 1) || !map_3d(tk, k, c.cache_rows(), c.d.hkv, 1, 128) ||
+      !map_3d(tv, v, c.cache_rows(), c.d.hkv, 1, 128))
     return MSA_ERR_CUDA;
   DecodeAttnParams dp{};
   dp.num_seqs = c.d.S;
@@ -496,7 +497,6 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
   dp.group = c.d.G;
   dp.topk = c.d.topk;
   dp.seq = c.seq;
-  dp.q = static_cast<const __nv_bfloat16*>(q);
   dp.idx = idx;
   dp.part = partials(c);
   dp.scale_log2 = c.d.scale * 1.4426950408889634f;
@@ -508,7 +508,7 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
   msa_status_t st;
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);
-    st = cuda_status(launch_decode_attn(tk, tv, dp, c.stream));
+    st = cuda_status(launch_decode_attn(tq, tk, tv, dp, c.stream));
   }
   if (st != MSA_OK) return st;
   return run_combine(p, c, idx, o, lse);

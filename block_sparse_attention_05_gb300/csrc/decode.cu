@@ -236,11 +236,14 @@ cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p,
 // ----------------------------------------------------------------------------
 namespace {
 
-constexpr int kDecThreads = 128;  // compute warps; one more warp streams K and V
-constexpr int kDecStages = 1;  // one block per CTA; two CTAs per SM overlap load and compute
-constexpr size_t kDecSmemBytes =
-    1024 + kDecStages * 65536 + 4 * 16 * 128 * sizeof(float) + 4 * 16 * 2 * sizeof(float) + (2 * kDecStages + 3) * 8 +
-    16;
+constexpr int kDecThreads = 128;  // compute warps; one more warp streams Q, K and V
+// Row stride (floats) of the merge slices: 8 floats of padding put the 8 rows a
+// warp's float2 stores touch at once on distinct banks.
+constexpr int kOsumStride = 128 + 8;
+// Per CTA (two per SM): K and V buffers (32 KB each), the item's Q (4 KB),
+// the merge slices and per-warp (max, sum), the item hand-over, barriers.
+constexpr size_t kDecSmemBytes = 1024 + 65536 + 4096 + 4 * 16 * kOsumStride * sizeof(float) +
+                                 4 * 16 * 2 * sizeof(float) + 16 + (4 + 3) * 8 + 16;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -257,36 +260,54 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 
 }  // namespace
 
-// Persistent: two CTAs per SM, each walking the items (sequence, group, slot)
-// it owns (item = blockIdx.x + j * gridDim.x).  Warp 4 streams each valid
-// item's K and V block (64 KB) into the CTA's ring while warps 0..3 compute,
-// and the two CTAs of an SM overlap one's loads with the other's compute.
-// Both sides skip empty slots by the same test, so they agree on the ring
-// order.
+// Persistent: two CTAs per SM, each owning the items (sequence, group, slot)
+// item = blockIdx.x + j * gridDim.x.  Warp 4 (one thread) walks them, skips
+// empty slots, and for each valid item hands the compute warps its output
+// slot and causal limit through shared memory and loads its Q rows (16 heads,
+// 4 KB) with its K block (32 KB) on one barrier and its V block (32 KB) on
+// another.  K and V have a buffer and a pair of barriers each, so the next
+// item's Q and K are loaded as soon as this item's S = Q K^T is done (under
+// the softmax, P V and the merge) and its V as soon as P V is done; the
+// compute warps issue no global loads.  After the last item an arrival
+// without bytes on the K barrier, with slot -1, ends the compute warps.
 // Per item: 16 heads x 128 keys; each compute warp takes 32 keys (S = Q K^T
 // and O_w = P V with mma.sync m16n8k16, P split into bf16 hi + lo), then the
 // four warps merge through shared memory (each writes its scaled partial to
 // its own slice, then every element is summed over the four slices: no
 // shared-memory atomics).
+struct DecodeItem {
+  long long sel;  // (sequence * hkv + group) * topk + slot, or -1 after the last item
+  int lim;        // last visible key of the block (kv_len - 1 - block * 128)
+  int pad;
+};
+
+// Byte offset of (row, 8-element chunk) in the 16-row Q tile: 128-byte
+// swizzle, 64-column halves 2 KB apart.
+__device__ __forceinline__ uint32_t q_off(int row, int chunk) {
+  return (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
 __global__ void __launch_bounds__(kDecThreads + 32)
-    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                       DecodeAttnParams p) {
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, DecodeAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = base;                                                    // kDecStages x (K 32 KB | V 32 KB)
-  float* osum = reinterpret_cast<float*>(base + kDecStages * 65536);       // [4 warps][16 heads][128] fp32
-  float* red = osum + 4 * 16 * 128;                                        // [4 warps][16 heads][m, l]
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + 4 * 16 * 2);
-  uint64_t* empty = full + kDecStages;
-  uint64_t* mrg = empty + kDecStages;  // per item: red written, partial sums added, merged output read
+  uint8_t* ring = base;                                                    // K 32 KB | V 32 KB
+  uint8_t* qbuf = base + 65536;                                            // Q 16 heads x 128 (4 KB)
+  float* osum = reinterpret_cast<float*>(base + 65536 + 4096);             // [4 warps][16 heads][kOsumStride]
+  float* red = osum + 4 * 16 * kOsumStride;                                // [4 warps][16 heads][m, l]
+  DecodeItem* info = reinterpret_cast<DecodeItem*>(red + 4 * 16 * 2);
+  uint64_t* full = reinterpret_cast<uint64_t*>(info + 1);                  // [0] Q + K landed, [1] V landed
+  uint64_t* empty = full + 2;                                              // [0] K read, [1] V read
+  uint64_t* mrg = empty + 2;  // per item: red written, partial sums added, merged output read
   int* abort_flag = reinterpret_cast<int*>(mrg + 3);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;  // 16
   const long long n_items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kDecStages; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4);  // one arrival per compute warp
     }
@@ -310,31 +331,50 @@ __global__ void __launch_bounds__(kDecThreads + 32)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t n = 0;
+      uint32_t nk = 0, nv = 0;  // Q + K and V fills issued
+      bool stopped = false, ended = false;
       for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
         int s, g, b;
         item_block(it, s, g, b);
         if (b < 0) continue;
-        const int st = n % kDecStages;
-        if (n >= kDecStages && !mbar_wait(&empty[st], ((n / kDecStages) - 1) & 1, abort_flag)) {
+        const int krow = key_block_row(p.block_table, p.bt_stride, p.n_pages, p.seq[s].k_start, s, b, hdr);
+        // Q and K of this item once the compute warps have read the previous item's, then V likewise
+        if (nk >= 1 && !mbar_wait(&empty[0], (nk - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 322);
+          stopped = true;
           break;
         }
-        const int krow = key_block_row(p.block_table, p.bt_stride, p.n_pages, p.seq[s].k_start, s, b, hdr);
-        uint8_t* kv = ring + st * 65536;
-        mbar_arrive_expect_tx(&full[st], 65536);
-        tma_load_3d(kv, &tm_k, &full[st], 0, g, krow);
-        tma_load_3d(kv + 16384, &tm_k, &full[st], 64, g, krow);
-        tma_load_3d(kv + 32768, &tm_v, &full[st], 0, g, krow);
-        tma_load_3d(kv + 49152, &tm_v, &full[st], 64, g, krow);
-        ++n;
+        info->sel = it;
+        info->lim = p.seq[s].kv_len - 1 - b * kBlock;
+        mbar_arrive_expect_tx(&full[0], 32768 + 4096);
+        tma_load_3d(qbuf, &tm_q, &full[0], 0, g * 16, s);
+        tma_load_3d(qbuf + 2048, &tm_q, &full[0], 64, g * 16, s);
+        tma_load_3d(ring, &tm_k, &full[0], 0, g, krow);
+        tma_load_3d(ring + 16384, &tm_k, &full[0], 64, g, krow);
+        ++nk;
+        if (nv >= 1 && !mbar_wait(&empty[1], (nv - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 323);
+          stopped = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[1], 32768);
+        tma_load_3d(ring + 32768, &tm_v, &full[1], 0, g, krow);
+        tma_load_3d(ring + 49152, &tm_v, &full[1], 64, g, krow);
+        ++nv;
+      }
+      if (!stopped) {
+        // no more items: one more phase of the K barrier, without bytes, carries slot -1
+        if (nk >= 1 && !mbar_wait(&empty[0], (nk - 1) & 1, abort_flag)) {
+          report_timeout(abort_flag, hdr, 325);
+        } else {
+          info->sel = -1;
+          mbar_arrive(&full[0]);
+          ended = true;  // every Q + K fill has been read, so it has landed
+        }
       }
       // let every issued copy land before the CTA exits
-      for (int st = 0; st < kDecStages; ++st)
-        if (n > static_cast<uint32_t>(st)) {
-          const uint32_t last = ((n - 1 - st) / kDecStages) * kDecStages + st;
-          mbar_wait(&full[st], (last / kDecStages) & 1, nullptr);
-        }
+      if (!ended && nk >= 1) mbar_wait(&full[0], (nk - 1) & 1, nullptr);
+      if (nv >= 1) mbar_wait(&full[1], (nv - 1) & 1, nullptr);
     }
     return;
   }
@@ -351,34 +391,23 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     }
     return true;
   };
+  const volatile DecodeItem* vinfo = info;
   uint32_t n = 0;
-  for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
-    int s, g, b;
-    item_block(it, s, g, b);
-    if (b < 0) continue;
-    const SeqInfo si = p.seq[s];
-    const int pos = si.kv_len - 1;
-    const long long sel = it;
-    const int st = n % kDecStages;
-    // Q fragments (16 heads x 128 dims) straight from global memory
-    const __nv_bfloat16* qg = p.q + (static_cast<int64_t>(s) * p.hkv * G + g * G) * kHeadDim;
-    uint32_t qa[8][4];
-    {
-      const int h0 = lane >> 2, d0 = (lane & 3) * 2;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        qa[k][0] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0);
-        qa[k][1] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0);
-        qa[k][2] = *reinterpret_cast<const uint32_t*>(qg + h0 * kHeadDim + k * 16 + d0 + 8);
-        qa[k][3] = *reinterpret_cast<const uint32_t*>(qg + (h0 + 8) * kHeadDim + k * 16 + d0 + 8);
-      }
-    }
-    if (!mbar_wait_warp(&full[st], (n / kDecStages) & 1, abort_flag)) {
+  while (true) {
+    if (!mbar_wait_warp(&full[0], n & 1, abort_flag)) {
       if (lane == 0) report_timeout(abort_flag, hdr, 321);
       break;
     }
-    const uint32_t kt = smem_u32(ring + st * 65536), vt = kt + 32768;
+    const long long sel = vinfo->sel;
+    const int lim = vinfo->lim;
+    if (sel < 0) break;
+    const uint32_t kt = smem_u32(ring), vt = kt + 32768, qt = smem_u32(qbuf);
     const int mtx = lane >> 3, mr = lane & 7;
+    // Q fragments (16 heads x 128 dims) for the m16n8k16 A operand
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ldmatrix_x4(qt + q_off((mtx & 1) * 8 + mr, k * 2 + (mtx >> 1)), qa[k][0], qa[k][1], qa[k][2], qa[k][3]);
 
     // S = Q K^T for this warp's 32 keys: 4 n-tiles of 8 keys
     float sacc[4][4];
@@ -398,8 +427,10 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         mma_16816(sacc[ntp * 2 + 1], qa[k], b2, b3);
       }
     }
+    // this warp is done with Q, K and the item hand-over: the producer may load the next item's
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[0]);
     // masked, scaled logits; per-head max and sum over this warp's keys
-    const int lim = pos - b * kBlock;
     float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -434,6 +465,10 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
       l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
     }
+    if (!mbar_wait_warp(&full[1], n & 1, abort_flag)) {
+      if (lane == 0) report_timeout(abort_flag, hdr, 324);
+      break;
+    }
     // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
     float oacc[16][4];
 #pragma unroll
@@ -460,9 +495,9 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         mma_16816(oacc[2 * dp + 1], pl, b2, b3);
       }
     }
-    // this warp is done with the stage's K and V
+    // this warp is done with V
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (lane == 0) mbar_arrive(&empty[1]);
     ++n;
     // merge the four warps: rescale to the common max, sum, normalise
     const int h0 = lane >> 2;
@@ -490,23 +525,25 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0;
     const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1;
     // each warp's scaled partial into its own slice, then a 4-way sum per element
-    float* mine = osum + warp * 16 * 128;
+    float* mine = osum + warp * 16 * kOsumStride;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       const int d = nt * 8 + (lane & 3) * 2;
-      *reinterpret_cast<float2*>(&mine[h0 * 128 + d]) = make_float2(oacc[nt][0] * f0, oacc[nt][1] * f0);
-      *reinterpret_cast<float2*>(&mine[(h0 + 8) * 128 + d]) = make_float2(oacc[nt][2] * f1, oacc[nt][3] * f1);
+      *reinterpret_cast<float2*>(&mine[h0 * kOsumStride + d]) = make_float2(oacc[nt][0] * f0, oacc[nt][1] * f0);
+      *reinterpret_cast<float2*>(&mine[(h0 + 8) * kOsumStride + d]) =
+          make_float2(oacc[nt][2] * f1, oacc[nt][3] * f1);
     }
     if (!meet(1, n - 1)) break;
     __nv_bfloat16* out = p.part.o + sel * G * kHeadDim;
     for (int i = threadIdx.x * 8; i < 16 * 128; i += kDecThreads * 8) {
+      const int at = (i >> 7) * kOsumStride + (i & 127);  // head i / 128, column i % 128
       float acc[8];
 #pragma unroll
       for (int j = 0; j < 8; j += 4) {
-        float4 a = *reinterpret_cast<const float4*>(&osum[i + j]);
+        float4 a = *reinterpret_cast<const float4*>(&osum[at + j]);
 #pragma unroll
         for (int w = 1; w < 4; ++w) {
-          const float4 b4 = *reinterpret_cast<const float4*>(&osum[w * 16 * 128 + i + j]);
+          const float4 b4 = *reinterpret_cast<const float4*>(&osum[w * 16 * kOsumStride + at + j]);
           a.x += b4.x;
           a.y += b4.y;
           a.z += b4.z;
@@ -543,15 +580,15 @@ __global__ void __launch_bounds__(kDecThreads + 32)
 
 size_t decode_attn_smem_bytes() { return kDecSmemBytes; }
 
-cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeAttnParams& p,
-                               cudaStream_t stream) {
+cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeAttnParams& p, cudaStream_t stream) {
   const long long items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
   if (items == 0) return cudaSuccess;
   const long long grid = items < 2LL * p.sms ? items : 2LL * p.sms;  // persistent: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kDecSmemBytes));
   if (e != cudaSuccess) return e;
-  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads + 32, kDecSmemBytes, stream>>>(tk, tv, p);
+  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads + 32, kDecSmemBytes, stream>>>(tq, tk, tv, p);
   note_launches(1);
   return cudaGetLastError();
 }

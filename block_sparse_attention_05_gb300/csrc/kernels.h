@@ -144,9 +144,8 @@ struct DecodeAttnParams {
   int num_seqs, hkv, group, topk;
   int sms;                 // persistent grid size
   const SeqInfo* seq;
-  const __nv_bfloat16* q;  // [num_seqs, hq, 128]
   const int32_t* idx;      // [num_seqs, hkv, topk]
-  PartialBuffers part;
+  PartialBuffers part;     // Q [num_seqs, hq, 128] comes through a tensor map (16 heads x 64 dims boxes)
   float scale_log2;
   WsHeader* hdr;
   const int32_t* block_table;  // as in DecodeScanParams
@@ -154,8 +153,8 @@ struct DecodeAttnParams {
   long long n_pages;
 };
 size_t decode_attn_smem_bytes();
-cudaError_t launch_decode_attn(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeAttnParams& p,
-                               cudaStream_t stream);
+cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeAttnParams& p, cudaStream_t stream);
 
 struct CombineParams {
   int total_q, hq, hkv, group, topk, num_seqs;
