@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -154,11 +155,20 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic record from ncu
-def kernel_source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "block_sparse_attention_05_gb300", "csrc", name)
+def code_only(text: str) -> str:
+    """C/CUDA source without comments, blank lines and indentation: what the compiler sees, so that a
+    comment edit keeps a traffic record that a code change invalidates."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+
+
+def kernel_source_hash(name: str, read=None) -> str:
+    """Hash of a kernel file's code and of common.cuh's (comments and layout ignored)."""
+    read = read or (lambda rel: open(os.path.join(ROOT, rel), encoding="utf-8").read())
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "block_sparse_attention_05_gb300", "csrc", "common.cuh")):
-        h.update(open(p, "rb").read())
+    for rel in (f"block_sparse_attention_05_gb300/csrc/{name}", "block_sparse_attention_05_gb300/csrc/common.cuh"):
+        h.update(code_only(read(rel)).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,11 +12,12 @@
 // mma.sync (m16n8k16: keys x d_idx times d_idx x groups) -- it keeps the
 // instruction count per byte low so the issue slots never limit the stream.
 //
-// Attention: one CTA per (sequence, group, selected block): the block's K and
-// V by TMA, the group's 16 heads as the M = 16 rows of mma.sync tiles, four
-// warps over 32 keys each merged in shared memory, then a normalised partial
-// output and its LSE per slot.  combine.cu merges the slots (split-KV with a
-// log-sum-exp combine).
+// Attention: persistent CTAs (two per SM) over the (sequence, group, selected
+// block) items: a producer thread streams each item's Q rows, K block and V
+// block by TMA, four warps compute it (the group's 16 heads as the M = 16 rows
+// of mma.sync tiles, 32 keys per warp) and merge in shared memory, then write
+// a normalised partial output and its LSE per slot.  combine.cu merges the
+// slots (split-KV with a log-sum-exp combine).
 #include "common.cuh"
 #include "kernels.h"
 
