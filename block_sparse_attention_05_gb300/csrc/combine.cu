@@ -103,18 +103,18 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
     const float L = m + logf(sum);
     const float w = valid ? expf(w_s - L) : 0.f;
 
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // acc[j] holds columns 2j, 2j + 1: one packed fma per bf16 pair (the same single rounding per
+    // element as two scalar fmas); a bf16 widens to fp32 by moving its bits to the high half
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int sl = 0; sl < kMaxTopk; ++sl) {
       const float ws = __shfl_sync(0xFFFFFFFFu, w, (lane & 16) | sl);
       if (sl < p.topk && ws != 0.f) {
         const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+        const float2 w2 = make_float2(ws, ws);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __nv_bfloat162 t = *reinterpret_cast<const __nv_bfloat162*>(&v[j]);
-          acc[2 * j] = fmaf(ws, __low2float(t), acc[2 * j]);
-          acc[2 * j + 1] = fmaf(ws, __high2float(t), acc[2 * j + 1]);
-        }
+        for (int j = 0; j < 4; ++j)
+          acc[j] = ffma2(w2, make_float2(__uint_as_float(v[j] << 16), __uint_as_float(v[j] & 0xFFFF0000u)), acc[j]);
       }
     }
     const bool empty = (m == -INFINITY);
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
     uint32_t* ow = &out.x;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 t = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      const __nv_bfloat162 t = __floats2bfloat162_rn(acc[j].x, acc[j].y);
       ow[j] = *reinterpret_cast<const uint32_t*>(&t);
     }
     const int64_t orow = static_cast<int64_t>(i) * p.hq + h;
