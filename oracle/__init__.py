@@ -11,6 +11,7 @@ blocks", section "The mechanism, precisely", and its Figure 1):
   * ``pooled``    -- index scores Q_idx . K_idx^T, max-pooled per block, causal;
   * ``select``    -- top-k blocks by (score desc, index asc), local block forced;
   * ``attention`` -- exact softmax attention over the selected blocks' tokens;
+  * ``index``     -- ``pooled`` then ``select`` (the Index Branch alone);
   * ``forward``   -- the three chained.
 """
 from __future__ import annotations
@@ -61,8 +62,11 @@ def _load(path: str | None = None):
                 ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_double, _u16p, _u16p, _u16p, _u16p, _u16p,
                 ctypes.c_int, _i32p, _i32p, _f64p, _f64p, _f64p]
+            lib.msa_oracle_index.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u16p, _u16p, ctypes.c_int, _i32p, _i32p, _f64p]
             for fn in (lib.msa_oracle_pooled, lib.msa_oracle_select, lib.msa_oracle_attention,
-                       lib.msa_oracle_forward):
+                       lib.msa_oracle_forward, lib.msa_oracle_index):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -158,6 +162,22 @@ def attention(cu_q, cu_k, q, k, v, idx, block: int, scale: float | None = None, 
                                       _ptr(rows_a, _i32p), _ptr(o, _f64p), _ptr(lse, _f64p))
     _check(rc, "attention")
     return o, lse
+
+
+def index(cu_q, cu_k, q_idx, k_idx, block: int, topk: int, rows=None):
+    """Index Branch only (pooled scores, then selection).  Returns dict(idx [n,Hkv,k] i32, gap [n,Hkv] f64)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    qib, kib = _bits(q_idx), _bits(k_idx)
+    total_q, hkv, d_idx = qib.shape
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    idx = np.empty((n_rows, hkv, topk), np.int32)
+    gap = np.empty((n_rows, hkv), np.float64)
+    rc = _load().msa_oracle_index(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hkv, d_idx, block, topk,
+                                  _ptr(qib, _u16p), _ptr(kib, _u16p), n_rows, _ptr(rows_a, _i32p),
+                                  _ptr(idx, _i32p), _ptr(gap, _f64p))
+    _check(rc, "index")
+    return {"idx": idx, "gap": gap}
 
 
 def forward(cu_q, cu_k, q, k, v, q_idx, k_idx, block: int, topk: int, scale: float | None = None,

@@ -22,6 +22,8 @@
  *     local block is forced in and that selection is per query and per group.
  *     Ranking: pooled score descending, ties to the lower block index.
  *
+ *     msa_oracle_index chains steps 1 and 2 (the Index Branch alone).
+ *
  *  3. msa_oracle_attention -- Main Branch: exact softmax attention of every
  *     query head over only the tokens of its group's selected blocks.  Same
  *     section, second bullet ("exact attention over only those blocks",
@@ -59,6 +61,30 @@ static double bf16_bits_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* sum_d q[d] * k[d], accumulated in double in order d = 0 .. n-1, for bf16
+ * vectors already widened to double (exactly; so are their products). */
+static double dot_wide(const double *q, const double *k, int n) {
+  double acc = 0.0;
+  for (int d = 0; d < n; ++d) acc += q[d] * k[d];
+  return acc;
+}
+
+/* dot_wide(q, k + u * n, n) for the four consecutive rows u = 0..3 of k,
+ * computed side by side (four independent sums, each in the same order). */
+static void dot4_wide(const double *q, const double *k, int n, double out[4]) {
+  double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+  for (int d = 0; d < n; ++d) {
+    a0 += q[d] * k[d];
+    a1 += q[d] * k[n + d];
+    a2 += q[d] * k[2 * n + d];
+    a3 += q[d] * k[3 * n + d];
+  }
+  out[0] = a0;
+  out[1] = a1;
+  out[2] = a2;
+  out[3] = a3;
 }
 
 /* Checks the two prefix-sum arrays: nondecreasing, start at 0, and every
@@ -99,35 +125,61 @@ int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   if (hkv <= 0 || d_idx <= 0 || block <= 0 || n_rows < 0 || !pooled) return ORACLE_EINVAL;
   const int total_q = cu_q[num_seqs];
   if (!rows && n_rows != total_q) return ORACLE_EINVAL;
+  /* The rows are processed one sequence at a time, with that sequence's index
+   * keys widened once to double (exact) while its rows are scored. */
   int bad = 0;
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  int *row_seq = (int *)malloc(sizeof(int) * (size_t)(n_rows > 0 ? n_rows : 1));
+  if (!row_seq) return ORACLE_ENOMEM;
   for (int r = 0; r < n_rows; ++r) {
     const int i = rows ? rows[r] : r;
-    const int s = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
-    if (s < 0) { bad = 1; continue; }
+    row_seq[r] = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
+    if (row_seq[r] < 0) bad = 1;
+  }
+  for (int s = 0; s < num_seqs && !bad; ++s) {
+    int used = 0;
+    for (int r = 0; r < n_rows && !used; ++r) used = (row_seq[r] == s);
+    if (!used) continue;
     const int q_len = cu_q[s + 1] - cu_q[s];
     const int kv_len = cu_k[s + 1] - cu_k[s];
-    const int pos = kv_len - q_len + (i - cu_q[s]);
-    const int nb = msa_oracle_num_blocks(pos, block);
-    if (nb > nb_stride) { bad = 1; continue; }
-    for (int g = 0; g < hkv; ++g) {
-      float *out = pooled + ((size_t)r * hkv + g) * nb_stride;
-      for (int b = 0; b < nb_stride; ++b) out[b] = -INFINITY;
-      const uint16_t *qv = q_idx + ((size_t)i * hkv + g) * d_idx;
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1) * d_idx);
+    if (!kd) { bad = 1; break; }
+    for (size_t e = 0; e < (size_t)kv_len * d_idx; ++e)
+      kd[e] = bf16_bits_to_double(k_idx[(size_t)cu_k[s] * d_idx + e]);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int r = 0; r < n_rows; ++r) {
+      if (row_seq[r] != s) continue;
+      const int i = rows ? rows[r] : r;
+      const int pos = kv_len - q_len + (i - cu_q[s]);
+      const int nb = msa_oracle_num_blocks(pos, block);
+      if (nb > nb_stride) { bad = 1; continue; }
+      double *qd = (double *)malloc(sizeof(double) * (size_t)hkv * d_idx);  /* qd[g * d_idx + d] */
+      if (!qd) { bad = 1; continue; }
+      for (int e = 0; e < hkv * d_idx; ++e) qd[e] = bf16_bits_to_double(q_idx[(size_t)i * hkv * d_idx + e]);
+      float *out = pooled + (size_t)r * hkv * nb_stride;  /* out[g * nb_stride + b] */
+      for (int e = 0; e < hkv * nb_stride; ++e) out[e] = -INFINITY;
       for (int b = 0; b < nb; ++b) {
-        float best = -INFINITY;
-        for (int j = b * block; j < (b + 1) * block && j <= pos; ++j) {
-          const uint16_t *kv = k_idx + (size_t)(cu_k[s] + j) * d_idx;
-          double acc = 0.0;
-          for (int d = 0; d < d_idx; ++d)
-            acc += bf16_bits_to_double(qv[d]) * bf16_bits_to_double(kv[d]);
-          float sj = (float)acc;
-          if (sj > best) best = sj;
-        }
-        out[b] = best;
+        const int j_end = ((b + 1) * block < pos + 1) ? (b + 1) * block : pos + 1;
+        int j = b * block;
+        /* four keys at a time (every group's query against the same four key
+         * rows): independent sums, each over d in order */
+        for (; j + 4 <= j_end; j += 4)
+          for (int g = 0; g < hkv; ++g) {
+            double sc[4];
+            dot4_wide(qd + (size_t)g * d_idx, kd + (size_t)j * d_idx, d_idx, sc);
+            for (int u = 0; u < 4; ++u)
+              if ((float)sc[u] > out[g * nb_stride + b]) out[g * nb_stride + b] = (float)sc[u];
+          }
+        for (; j < j_end; ++j)
+          for (int g = 0; g < hkv; ++g) {
+            const float sj = (float)dot_wide(qd + (size_t)g * d_idx, kd + (size_t)j * d_idx, d_idx);
+            if (sj > out[g * nb_stride + b]) out[g * nb_stride + b] = sj;
+          }
       }
+      free(qd);
     }
+    free(kd);
   }
+  free(row_seq);
   return bad ? ORACLE_EINVAL : ORACLE_OK;
 }
 
@@ -264,19 +316,17 @@ int msa_oracle_attention(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
 }
 
 /*
- * Steps 1-3 chained for the query rows listed in rows (all when NULL).
- * Outputs: idx [n_rows][hkv][topk] (ascending, -1 padded), gap
- * [n_rows][hkv] (see msa_oracle_select), o [n_rows][hq][head_dim] and
- * lse [n_rows][hq] in double.
+ * Steps 1-2 chained (the Index Branch alone) for the query rows listed in rows
+ * (all when NULL): idx [n_rows][hkv][topk] (ascending, -1 padded) and gap
+ * [n_rows][hkv] (see msa_oracle_select).
  */
-int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
-                       int hq, int hkv, int head_dim, int d_idx, int block, int topk, double scale,
-                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                       const uint16_t *q_idx, const uint16_t *k_idx,
-                       int n_rows, const int32_t *rows,
-                       int32_t *idx, double *gap, double *o, double *lse) {
+int msa_oracle_index(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                     int hkv, int d_idx, int block, int topk,
+                     const uint16_t *q_idx, const uint16_t *k_idx,
+                     int n_rows, const int32_t *rows,
+                     int32_t *idx, double *gap) {
   if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
-  if (hkv <= 0 || block <= 0 || topk <= 0 || !idx) return ORACLE_EINVAL;
+  if (hkv <= 0 || block <= 0 || topk <= 0 || !idx || n_rows < 0) return ORACLE_EINVAL;
   int max_nb = 1;
   for (int s = 0; s < num_seqs; ++s) {
     int kv_len = cu_k[s + 1] - cu_k[s];
@@ -290,19 +340,36 @@ int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   int rc = msa_oracle_pooled(num_seqs, cu_q, cu_k, hkv, d_idx, block, q_idx, k_idx,
                              n_rows, rows, max_nb, pooled);
   if (rc) { free(pooled); return rc; }
-  const int total_q = cu_q[num_seqs];
-  for (int r = 0; r < n_rows && !rc; ++r) {
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(| : bad)
+  for (int r = 0; r < n_rows; ++r) {
     const int i = rows ? rows[r] : r;
     const int s = seq_of_query(num_seqs, cu_q, i);
     const int pos = (cu_k[s + 1] - cu_k[s]) - (cu_q[s + 1] - cu_q[s]) + (i - cu_q[s]);
     const int nb = msa_oracle_num_blocks(pos, block);
-    (void)total_q;
-    for (int g = 0; g < hkv && !rc; ++g)
-      rc = msa_oracle_select(nb, pooled + ((size_t)r * hkv + g) * max_nb, topk,
-                             idx + ((size_t)r * hkv + g) * topk,
-                             gap ? gap + (size_t)r * hkv + g : NULL);
+    for (int g = 0; g < hkv; ++g)
+      bad |= msa_oracle_select(nb, pooled + ((size_t)r * hkv + g) * max_nb, topk,
+                               idx + ((size_t)r * hkv + g) * topk,
+                               gap ? gap + (size_t)r * hkv + g : NULL) != 0;
   }
   free(pooled);
+  return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/*
+ * Steps 1-3 chained for the query rows listed in rows (all when NULL).
+ * Outputs: idx [n_rows][hkv][topk] (ascending, -1 padded), gap
+ * [n_rows][hkv] (see msa_oracle_select), o [n_rows][hq][head_dim] and
+ * lse [n_rows][hq] in double.
+ */
+int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                       int hq, int hkv, int head_dim, int d_idx, int block, int topk, double scale,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const uint16_t *q_idx, const uint16_t *k_idx,
+                       int n_rows, const int32_t *rows,
+                       int32_t *idx, double *gap, double *o, double *lse) {
+  int rc = msa_oracle_index(num_seqs, cu_q, cu_k, hkv, d_idx, block, topk, q_idx, k_idx,
+                            n_rows, rows, idx, gap);
   if (rc) return rc;
   return msa_oracle_attention(num_seqs, cu_q, cu_k, hq, hkv, head_dim, block, topk, scale,
                               q, k, v, idx, n_rows, rows, o, lse);

@@ -18,7 +18,8 @@ SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), 
                    "msa_oracle.c")
 
 MUTANTS = {
-    "pool_ignores_causality": ("j < (b + 1) * block && j <= pos; ++j) {", "j < (b + 1) * block; ++j) {"),
+    "pool_ignores_causality": ("const int j_end = ((b + 1) * block < pos + 1) ? (b + 1) * block : pos + 1;",
+                               "const int j_end = ((b + 1) * block < kv_len) ? (b + 1) * block : kv_len;"),
     "ties_go_to_higher_index": ("pooled_row[b] > pooled_row[best]) best = b;",
                                 "pooled_row[b] >= pooled_row[best]) best = b;"),
     "local_block_not_forced": ("if (k > 0) taken[local] = 1;", ""),
@@ -28,7 +29,7 @@ MUTANTS = {
     "top_left_alignment": ("const int pos = kv_len - q_len + (i - cu_q[s]);",
                            "const int pos = (i - cu_q[s]);"),
     "lse_without_max": ("lse[(size_t)r * hq + h] = m + log(l);", "lse[(size_t)r * hq + h] = log(l);"),
-    "index_dot_skips_last_dim": ("for (int d = 0; d < d_idx; ++d)", "for (int d = 0; d + 1 < d_idx; ++d)"),
+    "index_dot_skips_last_dim": ("for (int d = 0; d < n; ++d)", "for (int d = 0; d + 1 < n; ++d)"),
     "value_from_wrong_row": ("const uint16_t *vj = v + ((size_t)(cu_k[s] + key[t]) * hkv + g)",
                              "const uint16_t *vj = v + ((size_t)(key[t]) * hkv + g)"),
 }
