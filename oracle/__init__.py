@@ -12,7 +12,11 @@ blocks", section "The mechanism, precisely", and its Figure 1):
   * ``select``    -- top-k blocks by (score desc, index asc), local block forced;
   * ``attention`` -- exact softmax attention over the selected blocks' tokens;
   * ``index``     -- ``pooled`` then ``select`` (the Index Branch alone);
-  * ``forward``   -- the three chained.
+  * ``forward``   -- the three chained;
+  * ``quantize_fp8``, ``e4m3_value``, ``e4m3_code``, ``attention_fp8`` -- fp8
+    (E4M3) K/V with one scale per (key block, KV head), and the Main Branch
+    over such K/V (the atlas record of the report: the kernels "also support
+    fp8"; the format is a reading, see ``msa_oracle.c``).
 """
 from __future__ import annotations
 
@@ -30,6 +34,7 @@ _lib = None
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 
@@ -65,8 +70,20 @@ def _load(path: str | None = None):
             lib.msa_oracle_index.argtypes = [
                 ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _u16p, _u16p, ctypes.c_int, _i32p, _i32p, _f64p]
+            lib.msa_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.msa_oracle_e4m3_value.restype = ctypes.c_double
+            lib.msa_oracle_e4m3_code.argtypes = [ctypes.c_float]
+            lib.msa_oracle_e4m3_code.restype = ctypes.c_uint8
+            lib.msa_oracle_key_blocks.argtypes = [ctypes.c_int, _i32p, ctypes.c_int]
+            lib.msa_oracle_quantize_fp8.argtypes = [ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    _u16p, _u8p, _f32p]
+            lib.msa_oracle_attention_fp8.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_double, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, ctypes.c_int, _i32p,
+                _f64p, _f64p]
             for fn in (lib.msa_oracle_pooled, lib.msa_oracle_select, lib.msa_oracle_attention,
-                       lib.msa_oracle_forward, lib.msa_oracle_index):
+                       lib.msa_oracle_forward, lib.msa_oracle_index, lib.msa_oracle_key_blocks,
+                       lib.msa_oracle_quantize_fp8, lib.msa_oracle_attention_fp8):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -202,6 +219,73 @@ def forward(cu_q, cu_k, q, k, v, q_idx, k_idx, block: int, topk: int, scale: flo
                                     _ptr(gap, _f64p), _ptr(o, _f64p), _ptr(lse, _f64p))
     _check(rc, "forward")
     return {"idx": idx, "gap": gap, "o": o, "lse": lse}
+
+
+def e4m3_value(code: int) -> float:
+    """Value of one E4M3 code (NaN for the NaN codes)."""
+    return float(_load().msa_oracle_e4m3_value(int(code)))
+
+
+def e4m3_code(x: float) -> int:
+    """E4M3 code of an fp32 value: nearest, ties to the even code, saturated to +-448."""
+    return int(_load().msa_oracle_e4m3_code(float(np.float32(x))))
+
+
+def key_blocks(cu_k, block: int) -> int:
+    cu_k = _i32(cu_k)
+    return int(_load().msa_oracle_key_blocks(len(cu_k) - 1, _ptr(cu_k, _i32p), block))
+
+
+def _u8(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    a = np.asarray(a)
+    assert a.dtype == np.uint8, a.dtype
+    return np.ascontiguousarray(a)
+
+
+def _f32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def quantize_fp8(cu_k, x, block: int):
+    """fp8 copy of K or V ([total_k, Hkv, D] bf16): (codes uint8, same shape; scales fp32 [key blocks, Hkv])."""
+    cu_k = _i32(cu_k)
+    xb = _bits(x)
+    total_k, hkv, head_dim = xb.shape
+    codes = np.empty(xb.shape, np.uint8)
+    scales = np.empty((key_blocks(cu_k, block), hkv), np.float32)
+    rc = _load().msa_oracle_quantize_fp8(len(cu_k) - 1, _ptr(cu_k, _i32p), hkv, head_dim, block, _ptr(xb, _u16p),
+                                         _ptr(codes, _u8p), _ptr(scales, _f32p))
+    _check(rc, "quantize_fp8")
+    return codes, scales
+
+
+def attention_fp8(cu_q, cu_k, q, k8, v8, k_scale, v_scale, idx, block: int, scale: float | None = None, rows=None):
+    """Main Branch over fp8 K/V (codes and per-(key block, KV head) scales).  Returns (o f64, lse f64)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    qb = _bits(q)
+    k8a, v8a = _u8(k8), _u8(v8)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    total_q, hq, head_dim = qb.shape
+    hkv = k8a.shape[1]
+    idx_a = _i32(idx)
+    topk = idx_a.shape[-1]
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    assert idx_a.shape == (n_rows, hkv, topk)
+    assert ks.shape[0] >= key_blocks(cu_k, block) and vs.shape == ks.shape
+    scale = float(head_dim ** -0.5 if scale is None else scale)
+    o = np.empty((n_rows, hq, head_dim), np.float64)
+    lse = np.empty((n_rows, hq), np.float64)
+    rc = _load().msa_oracle_attention_fp8(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hq, hkv, head_dim,
+                                          block, topk, scale, _ptr(qb, _u16p), _ptr(k8a, _u8p), _ptr(v8a, _u8p),
+                                          _ptr(ks, _f32p), _ptr(vs, _f32p), _ptr(idx_a, _i32p), n_rows,
+                                          _ptr(rows_a, _i32p), _ptr(o, _f64p), _ptr(lse, _f64p))
+    _check(rc, "attention_fp8")
+    return o, lse
 
 
 def query_positions(cu_q, cu_k) -> np.ndarray:

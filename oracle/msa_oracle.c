@@ -374,3 +374,170 @@ int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   return msa_oracle_attention(num_seqs, cu_q, cu_k, hq, hkv, head_dim, block, topk, scale,
                               q, k, v, idx, n_rows, rows, o, lse);
 }
+
+/*
+ * fp8 K/V (the atlas record of the report, provenance of section 4.2: the
+ * kernels "also support fp8"; the pages give no format, so this follows the
+ * plainest reading, stated with the build's design notes):
+ *   * codes are OCP FP8 E4M3 ("E4M3FN"): sign, 4 exponent bits with bias 7,
+ *     3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); no infinities;
+ *     S.1111.111 is NaN; the largest finite value is 1.75 * 2^8 = 448;
+ *   * one fp32 scale per (key block of 128 tokens of a sequence, KV head), for
+ *     K and V separately: s = amax / 448 over the block's rows of that head
+ *     (s = 1 when amax = 0), code = round-to-nearest-even(x / s) with x / s
+ *     computed in fp32 and saturated to +-448;
+ *   * value = decode(code) * s.
+ * Scales are stored [n_key_blocks][hkv], key block b of sequence s at row
+ * sum_{s' < s} ceil(kv_len_s' / block) + b.
+ */
+
+/* Value of an E4M3 code, from the definition above (NaN for the NaN codes). */
+double msa_oracle_e4m3_value(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* E4M3 code of x: the nearest finite E4M3 value, ties to the even code (the
+ * one whose last mantissa bit is 0), magnitudes beyond 448 saturated to 448,
+ * NaN to 0x7F.  Written as a search over the ordered non-negative codes. */
+uint8_t msa_oracle_e4m3_code(float x) {
+  if (x != x) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+  int c = 0;  /* largest non-negative code whose value is <= a */
+  while (c + 1 <= 0x7E && msa_oracle_e4m3_value((uint8_t)(c + 1)) <= a) ++c;
+  const double lo = msa_oracle_e4m3_value((uint8_t)c);
+  if (lo == a) return (uint8_t)(sign | c);
+  const double hi = msa_oracle_e4m3_value((uint8_t)(c + 1));
+  int pick;
+  if (a - lo < hi - a) pick = c;
+  else if (hi - a < a - lo) pick = c + 1;
+  else pick = (c % 2 == 0) ? c : c + 1;
+  return (uint8_t)(sign | pick);
+}
+
+/* Number of key blocks of all sequences (rows of a scale array). */
+int msa_oracle_key_blocks(int num_seqs, const int32_t *cu_k, int block) {
+  int n = 0;
+  for (int s = 0; s < num_seqs; ++s) n += (cu_k[s + 1] - cu_k[s] + block - 1) / block;
+  return n;
+}
+
+/*
+ * Quantizes x (bf16 bits, [total_k][hkv][head_dim]) to codes (same shape) and
+ * scales ([n_key_blocks][hkv]) as described above.
+ */
+int msa_oracle_quantize_fp8(int num_seqs, const int32_t *cu_k, int hkv, int head_dim, int block,
+                            const uint16_t *x, uint8_t *codes, float *scales) {
+  if (num_seqs < 0 || !cu_k || hkv <= 0 || head_dim <= 0 || block <= 0 || !x || !codes || !scales)
+    return ORACLE_EINVAL;
+  if (cu_k[0] != 0) return ORACLE_EINVAL;
+  int row = 0;  /* scale row of the current block */
+  for (int s = 0; s < num_seqs; ++s) {
+    const int kv_len = cu_k[s + 1] - cu_k[s];
+    if (kv_len < 0) return ORACLE_EINVAL;
+    for (int b = 0; b * block < kv_len; ++b, ++row) {
+      const int j0 = cu_k[s] + b * block;
+      const int j1 = cu_k[s] + ((b + 1) * block < kv_len ? (b + 1) * block : kv_len);
+      for (int g = 0; g < hkv; ++g) {
+        float amax = 0.f;
+        for (int j = j0; j < j1; ++j)
+          for (int d = 0; d < head_dim; ++d) {
+            const float a = (float)fabs(bf16_bits_to_double(x[((size_t)j * hkv + g) * head_dim + d]));
+            if (a > amax) amax = a;
+          }
+        const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+        scales[(size_t)row * hkv + g] = sc;
+        for (int j = j0; j < j1; ++j)
+          for (int d = 0; d < head_dim; ++d) {
+            const size_t e = ((size_t)j * hkv + g) * head_dim + d;
+            const float xf = (float)bf16_bits_to_double(x[e]);
+            const float q = xf / sc;
+            codes[e] = msa_oracle_e4m3_code(q);
+          }
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * Step 3 with fp8 K and V: as msa_oracle_attention, every key and value
+ * element read as msa_oracle_e4m3_value(code) * scale of its (key block, KV
+ * head); everything in double.
+ */
+int msa_oracle_attention_fp8(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                             int hq, int hkv, int head_dim, int block, int topk, double scale,
+                             const uint16_t *q, const uint8_t *k8, const uint8_t *v8,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *idx, int n_rows, const int32_t *rows,
+                             double *o, double *lse) {
+  if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
+  if (hq <= 0 || hkv <= 0 || hq % hkv || head_dim <= 0 || block <= 0 || topk <= 0) return ORACLE_EINVAL;
+  if (!q || !k8 || !v8 || !k_scale || !v_scale || !idx || !o || !lse || n_rows < 0) return ORACLE_EINVAL;
+  const int total_q = cu_q[num_seqs];
+  if (!rows && n_rows != total_q) return ORACLE_EINVAL;
+  const int G = hq / hkv;
+  int *blk0 = (int *)malloc(sizeof(int) * (size_t)(num_seqs + 1));  /* first scale row of each sequence */
+  if (!blk0) return ORACLE_ENOMEM;
+  blk0[0] = 0;
+  for (int s = 0; s < num_seqs; ++s) blk0[s + 1] = blk0[s] + (cu_k[s + 1] - cu_k[s] + block - 1) / block;
+  int bad = 0;
+#pragma omp parallel reduction(| : bad)
+  {
+    double *x = (double *)malloc(sizeof(double) * (size_t)topk * block);
+    int32_t *key = (int32_t *)malloc(sizeof(int32_t) * (size_t)topk * block);
+    if (!x || !key) bad = 1;
+#pragma omp for schedule(dynamic, 1)
+    for (int r = 0; r < n_rows; ++r) {
+      if (!x || !key) continue;
+      const int i = rows ? rows[r] : r;
+      const int s = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
+      if (s < 0) { bad = 1; continue; }
+      const int q_len = cu_q[s + 1] - cu_q[s];
+      const int kv_len = cu_k[s + 1] - cu_k[s];
+      const int pos = kv_len - q_len + (i - cu_q[s]);
+      for (int h = 0; h < hq; ++h) {
+        const int g = h / G;
+        const int32_t *sel = idx + ((size_t)r * hkv + g) * topk;
+        int n = 0;
+        for (int e = 0; e < topk; ++e) {
+          const int b = sel[e];
+          if (b < 0) continue;
+          for (int j = b * block; j < (b + 1) * block && j <= pos; ++j) key[n++] = j;
+        }
+        const uint16_t *qh = q + ((size_t)i * hq + h) * head_dim;
+        double *oh = o + ((size_t)r * hq + h) * head_dim;
+        for (int d = 0; d < head_dim; ++d) oh[d] = 0.0;
+        if (n == 0) { lse[(size_t)r * hq + h] = -INFINITY; continue; }
+        double m = -INFINITY;
+        for (int t = 0; t < n; ++t) {
+          const double sk = k_scale[(size_t)(blk0[s] + key[t] / block) * hkv + g];
+          const uint8_t *kj = k8 + ((size_t)(cu_k[s] + key[t]) * hkv + g) * head_dim;
+          double acc = 0.0;
+          for (int d = 0; d < head_dim; ++d)
+            acc += bf16_bits_to_double(qh[d]) * (msa_oracle_e4m3_value(kj[d]) * sk);
+          x[t] = scale * acc;
+          if (x[t] > m) m = x[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < n; ++t) {
+          const double p = exp(x[t] - m);
+          l += p;
+          const double sv = v_scale[(size_t)(blk0[s] + key[t] / block) * hkv + g];
+          const uint8_t *vj = v8 + ((size_t)(cu_k[s] + key[t]) * hkv + g) * head_dim;
+          for (int d = 0; d < head_dim; ++d) oh[d] += p * (msa_oracle_e4m3_value(vj[d]) * sv);
+        }
+        for (int d = 0; d < head_dim; ++d) oh[d] /= l;
+        lse[(size_t)r * hq + h] = m + log(l);
+      }
+    }
+    free(x);
+    free(key);
+  }
+  free(blk0);
+  return bad ? ORACLE_EINVAL : ORACLE_OK;
+}

@@ -12,6 +12,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_fp8_pins as fp8_pins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
@@ -32,6 +33,15 @@ MUTANTS = {
     "index_dot_skips_last_dim": ("for (int d = 0; d < n; ++d)", "for (int d = 0; d + 1 < n; ++d)"),
     "value_from_wrong_row": ("const uint16_t *vj = v + ((size_t)(cu_k[s] + key[t]) * hkv + g)",
                              "const uint16_t *vj = v + ((size_t)(key[t]) * hkv + g)"),
+    # fp8 K/V
+    "e4m3_exponent_bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_ties_round_up": ("else pick = (c % 2 == 0) ? c : c + 1;", "else pick = c + 1;"),
+    "e4m3_no_saturation": ("if (a >= 448.0) return (uint8_t)(sign | 0x7E);", "if (a >= 448.0) return 0x7F;"),
+    "fp8_scale_for_max_240": ("amax > 0.f ? amax / 448.0f : 1.0f", "amax > 0.f ? amax / 240.0f : 1.0f"),
+    "fp8_scale_row_ignores_sequence": ("k_scale[(size_t)(blk0[s] + key[t] / block) * hkv + g]",
+                                       "k_scale[(size_t)(key[t] / block) * hkv + g]"),
+    "fp8_value_scale_dropped": ("oh[d] += p * (msa_oracle_e4m3_value(vj[d]) * sv);",
+                                "oh[d] += p * msa_oracle_e4m3_value(vj[d]);"),
 }
 
 PIN_TESTS = [
@@ -42,6 +52,11 @@ PIN_TESTS = [
     lambda: pins.test_forward_equals_dense_causal_when_k_covers_all_blocks(),
     lambda: pins.test_invariants_on_tiny_workload(),
     lambda: pins.test_token_budget_and_closed_forms(),
+    lambda: fp8_pins.test_e4m3_golden_table(),
+    lambda: fp8_pins.test_e4m3_values_match_torch_for_every_code(),
+    lambda: fp8_pins.test_e4m3_codes_match_torch_rounding(),
+    lambda: fp8_pins.test_quantizer_scale_and_error_bound(),
+    lambda: fp8_pins.test_attention_fp8_equals_bf16_attention_on_the_fp8_grid(),
 ]
 
 
