@@ -13,6 +13,9 @@ blocks", section "The mechanism, precisely", and its Figure 1):
   * ``attention`` -- exact softmax attention over the selected blocks' tokens;
   * ``index``     -- ``pooled`` then ``select`` (the Index Branch alone);
   * ``forward``   -- the three chained;
+  * ``index_prologue`` -- hidden states to index heads: projection, RMSNorm,
+    RoPE on the first 64 dims (Figure 1's Index Branch input; the reading is
+    stated in ``msa_oracle.c``);
   * ``quantize_fp8``, ``e4m3_value``, ``e4m3_code``, ``attention_fp8`` -- fp8
     (E4M3) K/V with one scale per (key block, KV head), and the Main Branch
     over such K/V (the atlas record of the report: the kernels "also support
@@ -81,9 +84,13 @@ def _load(path: str | None = None):
                 ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_double, _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, ctypes.c_int, _i32p,
                 _f64p, _f64p]
+            lib.msa_oracle_index_prologue.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_double, _u16p, _u16p, _u16p, _u16p, _u16p, ctypes.c_int, _i32p,
+                _f64p, _f64p]
             for fn in (lib.msa_oracle_pooled, lib.msa_oracle_select, lib.msa_oracle_attention,
                        lib.msa_oracle_forward, lib.msa_oracle_index, lib.msa_oracle_key_blocks,
-                       lib.msa_oracle_quantize_fp8, lib.msa_oracle_attention_fp8):
+                       lib.msa_oracle_quantize_fp8, lib.msa_oracle_attention_fp8, lib.msa_oracle_index_prologue):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -219,6 +226,28 @@ def forward(cu_q, cu_k, q, k, v, q_idx, k_idx, block: int, topk: int, scale: flo
                                     _ptr(gap, _f64p), _ptr(o, _f64p), _ptr(lse, _f64p))
     _check(rc, "forward")
     return {"idx": idx, "gap": gap, "o": o, "lse": lse}
+
+
+def index_prologue(cu_q, cu_k, x, wq, wk, gamma_q, gamma_k, rope_dim: int = 64, rope_base: float = 10000.0,
+                   eps: float = 1e-6, rows=None):
+    """Index query / key heads of the new tokens (query rows) from their hidden states x [total_q, d_model] bf16,
+    weights wq [hkv * d_idx, d_model], wk [d_idx, d_model], norm weights gamma_q, gamma_k [d_idx] (all bf16).
+    Returns (q_idx [n, hkv, d_idx] f64, k_idx [n, d_idx] f64), unrounded; token i's key row is k_start + pos(i)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    xb, wqb, wkb, gqb, gkb = _bits(x), _bits(wq), _bits(wk), _bits(gamma_q), _bits(gamma_k)
+    total_q, d_model = xb.shape
+    d_idx = wkb.shape[0]
+    hkv = wqb.shape[0] // d_idx
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    q_out = np.empty((n_rows, hkv, d_idx), np.float64)
+    k_out = np.empty((n_rows, d_idx), np.float64)
+    rc = _load().msa_oracle_index_prologue(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), d_model, hkv, d_idx,
+                                           rope_dim, float(rope_base), float(eps), _ptr(xb, _u16p), _ptr(wqb, _u16p),
+                                           _ptr(wkb, _u16p), _ptr(gqb, _u16p), _ptr(gkb, _u16p), n_rows,
+                                           _ptr(rows_a, _i32p), _ptr(q_out, _f64p), _ptr(k_out, _f64p))
+    _check(rc, "index_prologue")
+    return q_out, k_out
 
 
 def e4m3_value(code: int) -> float:

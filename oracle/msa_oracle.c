@@ -541,3 +541,77 @@ int msa_oracle_attention_fp8(int num_seqs, const int32_t *cu_q, const int32_t *c
   free(blk0);
   return bad ? ORACLE_EINVAL : ORACLE_OK;
 }
+
+/*
+ * Index prologue: hidden states -> index query and key heads.  "MiniMax Sparse
+ * Attention: let each query pick its own blocks", Figure 1: the Index Branch
+ * takes the hidden states through a linear projection, a norm and RoPE to the
+ * index query and key heads.  The atlas record of the report gives d_model =
+ * 3072 and a RoPE dimension of 64 on 128-dim heads (provenance of section
+ * 5.1); the norm type is not given.  Reading taken here, for each new token
+ * (query row i at key position pos(i)):
+ *   y_h = W_q[h] x_i  (h < hkv, d_idx each),  y_k = W_k x_i   (sums in double)
+ *   RMSNorm per head: z = y / sqrt(mean_d y^2 + eps) * gamma  (gamma_q shared by
+ *     the index query heads, gamma_k for the key head)
+ *   RoPE on dims [0, rope_dim): pairs (j, j + rope_dim/2), angle
+ *     pos(i) * base^(-2j / rope_dim), (a, b) -> (a cos - b sin, b cos + a sin);
+ *     dims rope_dim .. d_idx - 1 pass unchanged.
+ * Outputs are the unrounded values in double: q_out [n_rows][hkv][d_idx] and
+ * k_out [n_rows][d_idx] (the key row of token i is k_start + pos(i)).
+ */
+int msa_oracle_index_prologue(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                              int d_model, int hkv, int d_idx, int rope_dim, double rope_base, double eps,
+                              const uint16_t *x, const uint16_t *wq, const uint16_t *wk,
+                              const uint16_t *gamma_q, const uint16_t *gamma_k,
+                              int n_rows, const int32_t *rows, double *q_out, double *k_out) {
+  if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
+  if (d_model <= 0 || hkv <= 0 || d_idx <= 0 || rope_dim < 0 || rope_dim > d_idx || rope_dim % 2 ||
+      !(rope_base > 0) || !(eps >= 0) || !x || !wq || !wk || !gamma_q || !gamma_k || !q_out || !k_out ||
+      n_rows < 0)
+    return ORACLE_EINVAL;
+  const int total_q = cu_q[num_seqs];
+  if (!rows && n_rows != total_q) return ORACLE_EINVAL;
+  const int half = rope_dim / 2;
+  int bad = 0;
+#pragma omp parallel reduction(| : bad)
+  {
+    double *y = (double *)malloc(sizeof(double) * (size_t)d_idx);
+    if (!y) bad = 1;
+#pragma omp for schedule(dynamic, 16)
+    for (int r = 0; r < n_rows; ++r) {
+      if (!y) continue;
+      const int i = rows ? rows[r] : r;
+      const int s = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
+      if (s < 0) { bad = 1; continue; }
+      const int pos = (cu_k[s + 1] - cu_k[s]) - (cu_q[s + 1] - cu_q[s]) + (i - cu_q[s]);
+      const uint16_t *xi = x + (size_t)i * d_model;
+      for (int h = 0; h <= hkv; ++h) {  /* h == hkv: the key head */
+        const uint16_t *w = (h < hkv) ? wq + (size_t)h * d_idx * d_model : wk;
+        const uint16_t *gamma = (h < hkv) ? gamma_q : gamma_k;
+        double *out = (h < hkv) ? q_out + ((size_t)r * hkv + h) * d_idx : k_out + (size_t)r * d_idx;
+        /* projection */
+        for (int d = 0; d < d_idx; ++d) {
+          double acc = 0.0;
+          for (int c = 0; c < d_model; ++c)
+            acc += bf16_bits_to_double(xi[c]) * bf16_bits_to_double(w[(size_t)d * d_model + c]);
+          y[d] = acc;
+        }
+        /* RMSNorm */
+        double ss = 0.0;
+        for (int d = 0; d < d_idx; ++d) ss += y[d] * y[d];
+        const double inv = 1.0 / sqrt(ss / d_idx + eps);
+        for (int d = 0; d < d_idx; ++d) y[d] = y[d] * inv * bf16_bits_to_double(gamma[d]);
+        /* RoPE on the first rope_dim dims */
+        for (int d = 0; d < d_idx; ++d) out[d] = y[d];
+        for (int j = 0; j < half; ++j) {
+          const double ang = (double)pos * pow(rope_base, -2.0 * j / rope_dim);
+          const double c = cos(ang), sn = sin(ang);
+          out[j] = y[j] * c - y[j + half] * sn;
+          out[j + half] = y[j + half] * c + y[j] * sn;
+        }
+      }
+    }
+    free(y);
+  }
+  return bad ? ORACLE_EINVAL : ORACLE_OK;
+}

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_fp8_pins as fp8_pins
 import test_oracle_pins as pins
+import test_oracle_prologue_pins as prologue_pins
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
                    "msa_oracle.c")
@@ -42,6 +43,12 @@ MUTANTS = {
                                        "k_scale[(size_t)(key[t] / block) * hkv + g]"),
     "fp8_value_scale_dropped": ("oh[d] += p * (msa_oracle_e4m3_value(vj[d]) * sv);",
                                 "oh[d] += p * msa_oracle_e4m3_value(vj[d]);"),
+    # index prologue
+    "rope_rotation_sign": ("out[j] = y[j] * c - y[j + half] * sn;", "out[j] = y[j] * c + y[j + half] * sn;"),
+    "rope_frequency_exponent": ("pow(rope_base, -2.0 * j / rope_dim)", "pow(rope_base, -1.0 * j / rope_dim)"),
+    "rms_norm_sum_not_mean": ("sqrt(ss / d_idx + eps)", "sqrt(ss + eps)"),
+    "norm_weight_dropped": ("y[d] = y[d] * inv * bf16_bits_to_double(gamma[d]);", "y[d] = y[d] * inv;"),
+    "key_head_takes_query_norm_weight": ("(h < hkv) ? gamma_q : gamma_k", "gamma_q"),
 }
 
 PIN_TESTS = [
@@ -57,6 +64,10 @@ PIN_TESTS = [
     lambda: fp8_pins.test_e4m3_codes_match_torch_rounding(),
     lambda: fp8_pins.test_quantizer_scale_and_error_bound(),
     lambda: fp8_pins.test_attention_fp8_equals_bf16_attention_on_the_fp8_grid(),
+    lambda: prologue_pins.test_identity_projection_matches_torch_rms_norm(),
+    lambda: prologue_pins.test_rms_norm_is_scale_invariant_and_normalises_constants(),
+    lambda: prologue_pins.test_rope_is_a_complex_rotation_of_each_pair(4, 100.0),
+    lambda: prologue_pins.test_rope_position_zero_is_identity_and_dots_depend_on_offsets_only(),
 ]
 
 
