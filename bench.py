@@ -6,16 +6,25 @@ scores with fused top-k, schedule, Main Branch, combine -- or, for decode
 workloads, the index scan, top-k, split attention and combine) over one batch
 of seeded synthetic inputs already resident in HBM.
 
-Default workload: prefill_32k (one causal sequence of 32768 queries, 64/4
-heads, head dim 128, d_idx 128, block 128, k 16).  Prints one JSON line.
+Default workload: prefill_128k (one causal sequence of 131072 queries, 64/4
+heads, head dim 128, d_idx 128, block 128, k 16) -- the "prefill at 128K" of
+the metric.  The same JSON line carries a nested ``decode`` record for
+decode_1m (8 sequences decoding against 1,048,576-token caches), the metric's
+"decode at 1M", measured in the same process after the prefill arrays are
+freed.  Prints one JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl msa|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--decode-workload NAME|none]
+                  [--impl msa|reference]
 
 Under torchrun (N > 1) every rank runs its own copy of the workload on its own
 GPU (weak scaling, no data-path collective); the reported time is the max over
 ranks.  ``--impl reference`` times the CPU oracle (the plain reference
 implementation of the method) on the host cores, on a bounded sample of the
 same workload, and reports the same metric.
+
+The CPU-baseline leg times the oracle on a position-stratified sample of the
+workload's query rows; the same oracle outputs are compared with the GPU's
+rows of the timed step and reported as ``parity``.
 """
 from __future__ import annotations
 
@@ -93,9 +102,25 @@ def algorithmic_work(x, idx: torch.Tensor):
     # combine: read every valid partial (G x 128 bf16 + G fp32 LSE + G fp32 log weight), write O and LSE
     combine_bytes = float(n_slots * G * (cfg.head_dim * 2 + 8) + x.total_q * cfg.hq * (cfg.head_dim * 2 + 4) +
                           x.total_q * cfg.hkv * cfg.topk * 4)
+    T, D = x.total_q, cfg.head_dim
+    q_bytes = float(T * cfg.hq * D * 2)
+    o_bytes = float(T * cfg.hq * (D * 2 + 4))
+    # Main Branch HBM bytes of the KV-outer design with per-slot partials: Q read once, each (sequence, key block,
+    # group) that any query selected read once (K and V), every partial O (bf16) + LSE + log weight written by the
+    # attention and read back by the combine, O and LSE written
+    seq = torch.repeat_interleave(torch.arange(len(x.seqs), device=dev), (cu_q[1:] - cu_q[:-1]))
+    keyed = torch.where(valid, (seq[:, None, None] * (1 << 40) + b * cfg.hkv +
+                                torch.arange(cfg.hkv, device=dev)[None, :, None]), torch.full_like(b, -1))
+    n_blocks_sel = int(torch.unique(keyed[valid]).numel())
+    main_bytes = (q_bytes + n_blocks_sel * 2.0 * 128 * D * 2 + 2.0 * n_slots * G * (D * 2 + 8) + o_bytes)
+    decode_bytes = None
+    if cfg.is_decode:
+        decode_bytes = (k_idx_bytes + kv_bytes_selected + q_bytes + float(T * cfg.hkv * cfg.d_idx * 2) + o_bytes +
+                        float(T * cfg.hkv * cfg.topk * 4))
     return {"index_flops": index_flops, "attn_flops": attn_flops, "n_slots": n_slots,
             "kv_bytes_selected": kv_bytes_selected, "k_idx_bytes": k_idx_bytes,
-            "combine_bytes": combine_bytes, "ntok_total": float(ntok.double().sum().item())}
+            "combine_bytes": combine_bytes, "ntok_total": float(ntok.double().sum().item()),
+            "main_branch_model_bytes": main_bytes, "decode_step_bytes": decode_bytes}
 
 
 # ------------------------------------------------------------------ clocks
@@ -189,91 +214,74 @@ def ncu_traffic(workload: str, kernel_file: str, x):
     return rec["dram_bytes"] / rec["units"] * units_now
 
 
-# ------------------------------------------------------------------ CPU oracle timing
+# ------------------------------------------------------------------ CPU oracle timing (+ parity of its rows)
 def host_copy(x):
     return dict(cu_q=x.cu_q.cpu(), cu_k=x.cu_k.cpu(), q=x.q.cpu(), k=x.k.cpu(), v=x.v.cpu(),
                 q_idx=x.q_idx.cpu(), k_idx=x.k_idx.cpu())
 
 
-def oracle_rate(x, budget_s: float, max_rows: int = 100000, seed: int = 0, host=None):
-    """Query rows per second of the CPU oracle on a position-uniform sample of the workload's rows."""
-    import oracle
+def stratified_rows(total: int, n: int, seed: int) -> np.ndarray:
+    """n query rows, one drawn uniformly from each of n equal strata of [0, total) (all rows when n >= total)."""
+    if n >= total:
+        return np.arange(total, dtype=np.int32)
     rng = np.random.default_rng(seed)
+    edges = np.linspace(0, total, n + 1).astype(np.int64)
+    return np.array([rng.integers(edges[j], max(edges[j] + 1, edges[j + 1])) for j in range(n)], np.int32)
+
+
+def oracle_rate(x, budget_s: float, max_rows: int = 100000, seed: int = 0, host=None):
+    """Query rows per second of the CPU oracle on a position-stratified sample of the workload's rows.
+    Returns (rate, rows, seconds, cores, sampled row indices, the oracle's outputs for them)."""
+    import oracle
     host = host or host_copy(x)
     cfg = x.cfg
     ncores = os.cpu_count() or 1
 
     def run(rows):
         t0 = time.perf_counter()
-        oracle.forward(host["cu_q"], host["cu_k"], host["q"], host["k"], host["v"], host["q_idx"],
-                       host["k_idx"], block=cfg.block, topk=cfg.topk, rows=rows)
-        return time.perf_counter() - t0
+        out = oracle.forward(host["cu_q"], host["cu_k"], host["q"], host["k"], host["v"], host["q_idx"],
+                             host["k_idx"], block=cfg.block, topk=cfg.topk, rows=rows)
+        return time.perf_counter() - t0, out
 
     n0 = min(x.total_q, max(ncores, 8))
-    rows = np.sort(rng.choice(x.total_q, size=n0, replace=False)).astype(np.int32)
-    t = run(rows)
+    rows = stratified_rows(x.total_q, n0, seed)
+    t, out = run(rows)
     n = int(min(x.total_q, max_rows, max(n0, n0 * budget_s / max(t, 1e-6))))
     if n > n0:
-        rows = np.sort(rng.choice(x.total_q, size=n, replace=False)).astype(np.int32)
-        t = run(rows)
-    return n / t, n, t, ncores
+        rows = stratified_rows(x.total_q, n, seed + 1)
+        t, out = run(rows)
+    return len(rows) / t, len(rows), t, ncores, rows, out
 
 
-# ------------------------------------------------------------------ main
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="prefill_32k", choices=sorted(workloads.CONFIGS))
-    ap.add_argument("--impl", default="msa", choices=["msa", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+NEAR_TIE = 1e-5
 
-    world, rank, local = dist_env()
-    cfg = workloads.get(args.workload)
+
+def parity_of_rows(rows, ref, idx, o, lse, group):
+    """The GPU's outputs on the oracle's sampled rows against the oracle's: index rows that differ outside
+    the near-tie exemption, the near-tie count, and O / LSE errors over the non-exempt rows."""
+    r = torch.from_numpy(rows.astype(np.int64)).to(idx.device)
+    gi = idx[r].cpu().numpy()
+    go = o[r].float().cpu().numpy().astype(np.float64)
+    gl = lse[r].cpu().numpy().astype(np.float64)
+    tie = ref["gap"] < NEAR_TIE
+    mism = (gi != ref["idx"]).any(axis=-1) & ~tie
+    ok = np.repeat(~tie, group, axis=1)
+    err = np.abs(go - ref["o"])[ok]
+    lerr = np.abs(gl - ref["lse"])[ok]
+    n_pairs = int(tie.size)
+    return {"rows_checked": int(len(rows)), "query_group_rows": n_pairs, "mismatches": int(mism.sum()),
+            "near_tie_rows": int(tie.sum()), "near_tie_rate": float(tie.sum()) / max(n_pairs, 1),
+            "o_max_err": float(err.max()) if err.size else 0.0, "o_mean_err": float(err.mean()) if err.size else 0.0,
+            "lse_max_err": float(lerr.max()) if lerr.size else 0.0,
+            "tolerance": {"o_max": 1e-2, "o_mean": 1e-3, "lse_max": 1e-3, "near_tie_rate": 1e-3},
+            "rows": "position-stratified sample of the CPU-baseline leg; GPU outputs of the last timed step"}
+
+
+# ------------------------------------------------------------------ one workload
+def measure(msa, cfg, steps, warmup, args, dev, world, rank):
+    """Times `steps` msa_forward steps of `cfg` (device-resident inputs), then the end-to-end arm, the CPU
+    oracle baseline and the parity of its rows.  Returns the record (rank 0) and the kernel launch count."""
     unit = "tok/s" if cfg.is_decode else "query tok/s"
-    higher = True
-
-    if args.impl == "reference":
-        if rank != 0:
-            return 0
-        # inputs are drawn on the GPU when there is one (only to make them; the timed work is the oracle's)
-        x = workloads.generate(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
-        host = host_copy(x)
-        per_step = []
-        rows_done = 0
-        budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
-        for i in range(args.warmup + args.steps):
-            rate, n, t, cores = oracle_rate(x, budget_s=budget, seed=i, host=host)
-            if i >= args.warmup:
-                per_step.append((n, t))
-                rows_done += n
-        tot_t = sum(t for _, t in per_step)
-        value = rows_done / tot_t
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / len(per_step),
-                "higher_is_better": higher, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic",
-                "config": {"workload": f"{cfg.name}: {cfg.description}", "sample": "rows per step, position-uniform"},
-                "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
-                                 "sample": f"{rows_done} query rows of {cfg.name} over {args.steps} steps"},
-                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return 0
-
-    import block_sparse_attention_05_gb300 as msa
-
-    if world > 1:
-        torch.cuda.set_device(local)
-        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-
     x = workloads.generate(cfg, device=dev)
     prob = msa.Problem(x.cu_q, x.cu_k, x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq, cfg.hkv, cfg.d_idx,
                        cfg.topk)
@@ -287,7 +295,7 @@ def main():
     def step():
         msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, idx=idx, o=o, lse=lse, ws=ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
@@ -295,29 +303,37 @@ def main():
     if flags:
         raise RuntimeError(f"device status flags {flags} after warm-up")
 
-    # ---------------- timed region (device-resident inputs)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = {s: [] for s in msa.STAGES}
+    # ---------------- timed region (device-resident inputs): the steps are enqueued back to back, each
+    # bracketed by CUDA events on the library's stream, with the L2 flush between them outside the brackets
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = msa.kernel_launch_count()
     with ClockSampler(dev.index) as clk:
-        with timer:
-            for i in range(args.steps):
-                flush.zero_()
-                starts[i].record()
-                step()
-                ends[i].record()
-                ends[i].synchronize()
-                for k, v in timer.elapsed_ms().items():
-                    stage_ms[k].append(v)
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record()
+            step()
+            ends[i].record()
         torch.cuda.synchronize()
     launches = msa.kernel_launch_count() - launches0
     if world > 1:
         torch.distributed.barrier()
+    if msa.msa_read_device_status(ws):
+        raise RuntimeError("device status flags raised during the timed steps")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+    # ---------------- per-stage times: a second pass with the library's stage events (one step at a time)
+    stage_ms = {s: [] for s in msa.STAGES}
+    with timer:
+        for i in range(min(steps, 50)):
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
+            for k, v in timer.elapsed_ms().items():
+                stage_ms[k].append(v)
     ms = sum(step_ms) / len(step_ms)
     ms = max_over_ranks(ms, dev)
     units_per_gpu = x.total_q
@@ -332,25 +348,16 @@ def main():
                    "attn": "decode.cu" if cfg.is_decode else "sparse_attn.cu",
                    "combine": "combine.cu", "topk": "topk.cu", "schedule": "schedule.cu", "plan": "plan.cu"}
     if dominant == "attn" and not cfg.is_decode:
-        bound, unit_r, amount = "tensor", "TFLOP/s", work["attn_flops"]
-        achieved = amount / (stage_mean["attn"] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        bound, unit_r, amount, peak = "tensor", "TFLOP/s", work["attn_flops"], peaks["bf16_tflops"]
     elif dominant == "index" and not cfg.is_decode:
-        bound, unit_r, amount = "tensor", "TFLOP/s", work["index_flops"]
-        achieved = amount / (stage_mean["index"] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
+        bound, unit_r, amount, peak = "tensor", "TFLOP/s", work["index_flops"], peaks["bf16_tflops"]
     elif dominant == "index":
-        bound, unit_r, amount = "hbm", "GB/s", work["k_idx_bytes"]
-        achieved = amount / (stage_mean["index"] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
+        bound, unit_r, amount, peak = "hbm", "GB/s", work["k_idx_bytes"], peaks["hbm_gbs"]
     elif dominant == "combine":
-        bound, unit_r, amount = "hbm", "GB/s", work["combine_bytes"]
-        achieved = amount / (stage_mean["combine"] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
+        bound, unit_r, amount, peak = "hbm", "GB/s", work["combine_bytes"], peaks["hbm_gbs"]
     else:
-        bound, unit_r, amount = "hbm", "GB/s", work["kv_bytes_selected"]
-        achieved = amount / (stage_mean[dominant] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
+        bound, unit_r, amount, peak = "hbm", "GB/s", work["kv_bytes_selected"], peaks["hbm_gbs"]
+    achieved = amount / (stage_mean[dominant] * 1e-3) / (1e12 if unit_r == "TFLOP/s" else 1e9)
     traffic = ncu_traffic(cfg.name, kernel_file[dominant], x)
     roofline = {"bound": bound, "kernel": dominant, "achieved": achieved, "peak": peak, "unit": unit_r,
                 "frac": achieved / peak, "traffic": traffic,
@@ -373,6 +380,25 @@ def main():
             e["gbs"] = work["combine_bytes"] / (v * 1e-3) / 1e9
             e["frac_of_hbm_peak"] = e["gbs"] / peaks["hbm_gbs"]
         stages[k] = e
+    extra = {}
+    if not cfg.is_decode and "attn" in stage_mean and "combine" in stage_mean:
+        # the Main Branch as the sparse-attention gate measures it: its FLOPs over the attention and
+        # combine time together, beside the bound that the HBM bytes of this design put on it
+        t_ac = (stage_mean["attn"] + stage_mean["combine"]) * 1e-3
+        tf = work["attn_flops"] / t_ac / 1e12
+        bound_tf = work["attn_flops"] / (work["main_branch_model_bytes"] / (peaks["hbm_gbs"] * 1e9)) / 1e12
+        extra["sparse_attention"] = {
+            "stages": "attn + combine", "ms": t_ac * 1e3, "tflops": tf, "frac_of_tc_peak": tf / peaks["bf16_tflops"],
+            "traffic_model_bytes": work["main_branch_model_bytes"],
+            "traffic_model_bound_tflops": min(bound_tf, peaks["bf16_tflops"]),
+            "traffic_model_bound_frac": min(1.0, bound_tf / peaks["bf16_tflops"]),
+            "traffic_model": "HBM bytes of the design: Q read once, per-slot partial O (bf16) + LSE + log weight "
+                             "written and read back once, O and LSE written; bound = FLOPs / (bytes / HBM peak)"}
+    if cfg.is_decode:
+        gbs = work["decode_step_bytes"] / (ms * 1e-3) / 1e9
+        extra["whole_step"] = {"bytes": work["decode_step_bytes"], "gbs": gbs,
+                               "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+                               "bytes_are": "K_idx scan + selected K/V + q, q_idx read; o, lse, idx written"}
 
     # ---------------- end to end through the C ABI with host buffers
     # Every step copies its inputs in from pinned host memory and its outputs back, inside the timed
@@ -441,46 +467,172 @@ def main():
         t0.record(s_comp)
         s_in.wait_event(t0)
         s_out.wait_event(t0)
-        for n in range(args.steps):
+        for n in range(steps):
             e2e_step(n + 2 * nbuf)
         for ev in ev_out:
             s_comp.wait_event(ev)  # every step's outputs are back in host memory
         t1.record(s_comp)
         t1.synchronize()
-        e2e_ms = t0.elapsed_time(t1) / args.steps
+        e2e_ms = t0.elapsed_time(t1) / steps
         e2e_ms = max_over_ranks(e2e_ms, dev)
         e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "overlap": "two buffer sets: step n+1's inputs in and step n-1's outputs out during step n"}
         if cfg.is_decode:
             e2e["inputs"] = "q, q_idx and the new token's k, v, k_idx rows (appended on the device); KV cache resident"
+        del dev_in, dev_out, host_in, host_out
 
-    # ---------------- CPU oracle baseline (rank 0, N = 1 only)
-    cpu = None
+    # ---------------- CPU oracle baseline (rank 0, N = 1 only), and the parity of its rows
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, n, t, cores = oracle_rate(x, budget_s=args.cpu_budget)
+        rate, n, t, cores, rows, ref = oracle_rate(x, budget_s=args.cpu_budget)
         cpu = {"value": rate, "unit": unit, "cores": cores, "kind": "oracle",
-               "sample": f"{n} position-uniform query rows of {cfg.name} (all groups and heads), {t:.1f} s"}
+               "sample": f"{n} position-stratified query rows of {cfg.name} (all groups and heads), {t:.1f} s"}
+        parity = parity_of_rows(rows, ref, idx, o, lse, cfg.hq // cfg.hkv)
+
+    rec = None
+    if rank == 0:
+        rec = {"workload": f"{cfg.name}: {cfg.description}", "value": value, "unit": unit, "steps": steps,
+               "warmup": warmup, "ms_per_step": ms, "seqs": len(x.seqs), "total_q": x.total_q,
+               "total_k": x.total_k, "roofline": roofline, **extra, "stages": stages, "cpu_baseline": cpu,
+               "parity": parity, "e2e": e2e, "gpu_launches": launches, "clocks": clk.summary(),
+               "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
+                        "selected_slots": work["n_slots"], "attended_tokens": work["ntok_total"]}}
+    del x, ws, idx, o, lse, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+# ------------------------------------------------------------------ index prologue
+def measure_prologue(msa, cfg, steps, warmup, dev, d_model=3072):
+    """Times msa_index_prologue (hidden states -> Q_idx and the new tokens' K_idx rows) on the workload's tokens
+    with synthetic weights: CUDA events around each launch on the library's stream, inputs larger than L2."""
+    x = workloads.generate(cfg, device=dev)
+    prob = msa.Problem(x.cu_q, x.cu_k, x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq, cfg.hkv, cfg.d_idx,
+                       cfg.topk)
+    pin = workloads.prologue_inputs(x.total_q, cfg.hkv, cfg.d_idx, d_model=d_model, device=dev)
+    ws = msa.workspace(prob, msa.Op.INDEX_PROLOGUE)
+    q_idx = torch.empty_like(x.q_idx)
+    for _ in range(warmup):
+        msa.msa_index_prologue(prob, pin.x, pin.w_q, pin.w_k, pin.gamma_q, pin.gamma_k, x.k_idx, q_idx=q_idx, ws=ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        msa.msa_index_prologue(prob, pin.x, pin.w_q, pin.w_k, pin.gamma_q, pin.gamma_k, x.k_idx, q_idx=q_idx, ws=ws)
+        b.record()
+    torch.cuda.synchronize()
+    if msa.msa_read_device_status(ws):
+        raise RuntimeError("device status flags raised by the index prologue")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    flops = 2.0 * x.total_q * (cfg.hkv + 1) * cfg.d_idx * d_model
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    rec = {"workload": f"{cfg.name} tokens, d_model {d_model}, {cfg.hkv} index query heads + 1 key head of "
+                       f"{cfg.d_idx}", "ms": ms, "flops": flops, "tflops": tf,
+           "frac_of_tc_peak": tf / peaks["bf16_tflops"], "peak_source": f"{peaks['source']} (bf16 burst)",
+           "steps": steps, "data": "synthetic hidden states and weights (seeded)"}
+    del x, pin, ws, q_idx
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefill_128k", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--decode-workload", default="decode_1m", choices=sorted(workloads.CONFIGS) + ["none"],
+                    help="decode workload measured after the main one, reported as the nested 'decode' record")
+    ap.add_argument("--decode-steps", type=int, default=2500,
+                    help="timed steps of the nested decode record (about 1 s at decode_1m)")
+    ap.add_argument("--impl", default="msa", choices=["msa", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prologue", action="store_true", help="skip the index prologue measurement")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_env()
+    cfg = workloads.get(args.workload)
+    unit = "tok/s" if cfg.is_decode else "query tok/s"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        # inputs are drawn on the GPU when there is one (only to make them; the timed work is the oracle's)
+        x = workloads.generate(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+        host = host_copy(x)
+        per_step = []
+        rows_done = 0
+        cores = os.cpu_count() or 1
+        budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+        for i in range(args.warmup + args.steps):
+            rate, n, t, cores, _, _ = oracle_rate(x, budget_s=budget, seed=2 * i, host=host)
+            if i >= args.warmup:
+                per_step.append((n, t))
+                rows_done += n
+        tot_t = sum(t for _, t in per_step)
+        value = rows_done / tot_t
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * tot_t / len(per_step),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic",
+                "config": {"workload": f"{cfg.name}: {cfg.description}", "seqs": len(x.seqs),
+                           "total_q": x.total_q, "total_k": x.total_k,
+                           "sample": "rows per step, position-stratified"},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows_done} query rows of {cfg.name} over {args.steps} steps"},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    import block_sparse_attention_05_gb300 as msa
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    main_rec = measure(msa, cfg, args.steps, args.warmup, args, dev, world, rank)
+    pro_rec = None
+    if not cfg.is_decode and not args.no_prologue:
+        pro_rec = measure_prologue(msa, cfg, max(args.steps, 10), args.warmup, dev)
+    dec_rec = None
+    if args.decode_workload != "none" and args.decode_workload != args.workload:
+        dcfg = workloads.get(args.decode_workload)
+        dec_rec = measure(msa, dcfg, args.decode_steps, args.warmup, args, dev, world, rank)
 
     if rank == 0:
-        clocks = clk.summary()
+        m = main_rec
         line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": higher, "scaling": "weak",
+            "metric": METRIC, "value": m["value"] * 1.0, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{cfg.name}: {cfg.description}", "seqs": len(x.seqs),
-                       "total_q": x.total_q, "total_k": x.total_k,
+            "config": {"workload": m["workload"], "seqs": m["seqs"], "total_q": m["total_q"],
+                       "total_k": m["total_k"],
                        "l2": "inputs larger than L2; a 258 MB buffer is written between timed steps",
                        "parallelism": "replicas" if world > 1 else "single"},
-            "roofline": roofline,
-            "stages": stages,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clocks,
-            "work": {"index_flops": work["index_flops"], "attn_flops": work["attn_flops"],
-                     "selected_slots": work["n_slots"], "attended_tokens": work["ntok_total"]},
+            "roofline": m["roofline"],
         }
+        for key in ("sparse_attention", "whole_step"):
+            if key in m:
+                line[key] = m[key]
+        line.update({"stages": m["stages"], "cpu_baseline": m["cpu_baseline"], "parity": m["parity"],
+                     "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": m["clocks"], "work": m["work"]})
+        if pro_rec is not None:
+            line["index_prologue"] = pro_rec
+        if dec_rec is not None:
+            dec_rec = dict(dec_rec)
+            dec_rec["value"] = dec_rec["value"] * 1.0
+            line["decode"] = dec_rec
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -9,6 +9,9 @@ There is no CPU fallback: importing without the built library raises.
 Entry points (same names as the C functions):
   msa_index_pool, msa_topk_pooled, msa_index_topk,
   msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_forward,
+  msa_sparse_attn_decode_static, msa_forward_decode_paged,
+  msa_quantize_kv_fp8, msa_sparse_attn_prefill_fp8, msa_sparse_attn_decode_fp8, msa_forward_fp8,
+  msa_index_prologue,
   msa_workspace_size, msa_read_device_status.
 """
 from __future__ import annotations
@@ -40,12 +43,17 @@ class MsaError(RuntimeError):
 
 
 class Op(enum.IntEnum):
+    INDEX_PROLOGUE = 11
     INDEX_POOL = 1
     INDEX_TOPK = 2
     SPARSE_ATTN_PREFILL = 3
     SPARSE_ATTN_DECODE = 4
     FORWARD = 5
     TOPK_POOLED = 6
+    QUANTIZE_KV_FP8 = 7
+    SPARSE_ATTN_PREFILL_FP8 = 8
+    SPARSE_ATTN_DECODE_FP8 = 9
+    FORWARD_FP8 = 10
 
 
 DEVICE_TIMEOUT = 1
@@ -98,6 +106,15 @@ _lib.msa_forward.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _s
 _lib.msa_forward_decode_paged.restype = ctypes.c_int
 _lib.msa_forward_decode_paged.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, _i64, _vp, _vp, _vp, _vp,
                                           _sz, _vp]
+_lib.msa_quantize_kv_fp8.restype = ctypes.c_int
+_lib.msa_quantize_kv_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+for _fn in (_lib.msa_sparse_attn_prefill_fp8, _lib.msa_sparse_attn_decode_fp8):
+    _fn.restype = ctypes.c_int
+    _fn.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.msa_forward_fp8.restype = ctypes.c_int
+_lib.msa_forward_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.msa_index_prologue.restype = ctypes.c_int
+_lib.msa_index_prologue.argtypes = [_P, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
 _lib.msa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]
 _lib.msa_set_stage_events.restype = ctypes.c_int
@@ -108,7 +125,9 @@ _lib.msa_last_error_detail.restype = ctypes.c_char_p
 EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_index_topk",
             "msa_sparse_attn_prefill", "msa_sparse_attn_decode", "msa_forward",
             "msa_read_device_status", "msa_status_string", "msa_abi_version", "msa_set_stage_events",
-            "msa_kernel_launch_count", "msa_last_error_detail", "msa_sparse_attn_decode_static")
+            "msa_kernel_launch_count", "msa_last_error_detail", "msa_sparse_attn_decode_static",
+            "msa_forward_decode_paged", "msa_quantize_kv_fp8", "msa_sparse_attn_prefill_fp8",
+            "msa_sparse_attn_decode_fp8", "msa_forward_fp8", "msa_index_prologue")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 
@@ -314,7 +333,102 @@ def msa_forward_decode_paged(problem: Problem, q, k_cache, v_cache, q_idx, k_idx
     return idx, o, lse
 
 
-def msa_read_device_status(ws: torch.Tensor) -> int:
+# ---------------------------------------------------------------- index prologue
+def msa_index_prologue(problem: Problem, x, w_q, w_k, gamma_q, gamma_k, k_idx, q_idx=None, ws=None):
+    """Hidden states x [total_q, d_model] -> Q_idx [total_q, Hkv, 128] (returned) and the new tokens' rows
+    k_start + pos(i) of the index-key cache k_idx [total_k, 128] (written in place): projection, RMSNorm,
+    RoPE on dims 0..63."""
+    for t, n in ((x, "x"), (w_q, "w_q"), (w_k, "w_k"), (gamma_q, "gamma_q"), (gamma_k, "gamma_k"), (k_idx, "k_idx")):
+        _need(t, torch.bfloat16, n)
+    if q_idx is None:
+        q_idx = torch.empty((problem.total_q, problem.hkv, problem.d_idx), dtype=torch.bfloat16, device=x.device)
+    ws, nws = _ws(problem, Op.INDEX_PROLOGUE, ws)
+    _check(_lib.msa_index_prologue(ctypes.byref(problem.c()), _ptr(x), int(x.shape[1]), _ptr(w_q), _ptr(w_k),
+                                   _ptr(gamma_q), _ptr(gamma_k), _ptr(q_idx), _ptr(k_idx), _ptr(ws), nws, _stream()),
+           "msa_index_prologue")
+    return q_idx
+
+
+# ---------------------------------------------------------------- fp8 K/V
+def fp8_scale_rows(problem: Problem) -> int:
+    """Rows to allocate for a scale array: total_k / 128 + num_seqs bounds the number of key blocks."""
+    return problem.total_k // problem.block + problem.num_seqs
+
+
+def msa_quantize_kv_fp8(problem: Problem, k, v, k8=None, v8=None, k_scale=None, v_scale=None, ws=None):
+    """bf16 K, V -> E4M3 codes (uint8, same shape) and fp32 scales [key blocks, Hkv] (rows past the sequences'
+    key blocks are left as they were).  Returns (k8, v8, k_scale, v_scale)."""
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    dev = k.device
+    if k8 is None:
+        k8 = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    if v8 is None:
+        v8 = torch.empty(v.shape, dtype=torch.uint8, device=dev)
+    rows = (fp8_scale_rows(problem), problem.hkv)
+    if k_scale is None:
+        k_scale = torch.zeros(rows, dtype=torch.float32, device=dev)
+    if v_scale is None:
+        v_scale = torch.zeros(rows, dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.QUANTIZE_KV_FP8, ws)
+    _check(_lib.msa_quantize_kv_fp8(ctypes.byref(problem.c()), _ptr(k), _ptr(v), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(ws), nws, _stream()), "msa_quantize_kv_fp8")
+    return k8, v8, k_scale, v_scale
+
+
+def _attn_fp8(fn, op, where, problem, q, k8, v8, k_scale, v_scale, idx, o, lse, ws):
+    _need(q, torch.bfloat16, "q")
+    _need(k8, torch.uint8, "k8")
+    _need(v8, torch.uint8, "v8")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(idx, torch.int32, "idx")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=q.device)
+    ws, nws = _ws(problem, op, ws)
+    _check(fn(ctypes.byref(problem.c()), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale), _ptr(idx),
+              _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()), where)
+    return o, lse
+
+
+def msa_sparse_attn_prefill_fp8(problem: Problem, q, k8, v8, k_scale, v_scale, idx, o=None, lse=None, ws=None):
+    return _attn_fp8(_lib.msa_sparse_attn_prefill_fp8, Op.SPARSE_ATTN_PREFILL_FP8, "msa_sparse_attn_prefill_fp8",
+                     problem, q, k8, v8, k_scale, v_scale, idx, o, lse, ws)
+
+
+def msa_sparse_attn_decode_fp8(problem: Problem, q, k8, v8, k_scale, v_scale, idx, o=None, lse=None, ws=None):
+    return _attn_fp8(_lib.msa_sparse_attn_decode_fp8, Op.SPARSE_ATTN_DECODE_FP8, "msa_sparse_attn_decode_fp8",
+                     problem, q, k8, v8, k_scale, v_scale, idx, o, lse, ws)
+
+
+def msa_forward_fp8(problem: Problem, q, k8, v8, k_scale, v_scale, q_idx, k_idx, idx=None, o=None, lse=None,
+                    ws=None):
+    """msa_forward with fp8 K/V for the Main Branch.  Returns (idx, o, lse)."""
+    for t, n in ((q, "q"), (q_idx, "q_idx"), (k_idx, "k_idx")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((k8, "k8"), (v8, "v8")):
+        _need(t, torch.uint8, n)
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.FORWARD_FP8, ws)
+    _check(_lib.msa_forward_fp8(ctypes.byref(problem.c()), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale),
+                                _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()),
+           "msa_forward_fp8")
+    return idx, o, lse
+
+
+def msa_read_device_status(ws: Optional[torch.Tensor]) -> int:
+    """MSA_DEVICE_* flags of the last call on workspace ``ws`` (None: of the last
+    msa_sparse_attn_decode_static call on the current device).  Synchronises the stream."""
     flags = ctypes.c_uint32(0)
     _check(_lib.msa_read_device_status(_ptr(ws), ctypes.byref(flags), _stream()), "msa_read_device_status")
     return int(flags.value)

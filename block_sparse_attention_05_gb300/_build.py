@@ -47,7 +47,8 @@ def build(verbose: bool = False, extra_flags=None) -> str:
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     exe = nvcc()
-    flags = FLAGS + list(extra_flags or [])
+    # MSA_EXTRA_NVCC_FLAGS adds flags to every compile (e.g. "-DMSA_CHECKED=1" for the checked build)
+    flags = FLAGS + os.environ.get("MSA_EXTRA_NVCC_FLAGS", "").split() + list(extra_flags or [])
     # objects built with other flags are stale
     stamp = os.path.join(LIB_DIR, "obj", "flags.txt")
     key = " ".join(ARCH + flags)

@@ -58,7 +58,7 @@ struct Derived {
 
 struct Layout {
   size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, count, bstart, bcursor, nchunk, cstart,
-      entries, chunks, scan_tmp, v16, part_o, part_lse, part_ow, total;
+      entries, chunks, scan_tmp, v16, k16, part_o, part_lse, part_ow, total;
 };
 
 msa_status_t derive(const msa_problem_t* p, Derived& d) {
@@ -71,7 +71,7 @@ msa_status_t derive(const msa_problem_t* p, Derived& d) {
   if (!(p->softmax_scale == p->softmax_scale)) return MSA_ERR_INVALID_ARG;  // NaN
   if (p->head_dim != 128 || p->block_size != 128) return MSA_ERR_UNSUPPORTED;
   if (p->index_dim != 64 && p->index_dim != 128) return MSA_ERR_UNSUPPORTED;
-  if (p->topk > 16) return MSA_ERR_UNSUPPORTED;
+  if (p->topk > 64) return MSA_ERR_UNSUPPORTED;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (!is_pow2(G) || G < 8 || G > 128) return MSA_ERR_UNSUPPORTED;
   if (128 % p->num_kv_heads) return MSA_ERR_UNSUPPORTED;
@@ -99,21 +99,33 @@ msa_status_t derive(const msa_problem_t* p, Derived& d) {
   d.max_chunks = (d.n_inc + d.qpc - 1) / d.qpc + d.n_buckets;
   d.decode = (p->max_seqlen_q <= 1);
   d.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
-  if (d.n_buckets > 0x7FFFFFFFLL || d.n_inc > (1LL << 31) || p->total_q >= (1 << 26)) return MSA_ERR_UNSUPPORTED;
+  // schedule entries hold (query << kSlotBits) | slot in an int32
+  if (d.n_buckets > 0x7FFFFFFFLL || d.n_inc > (1LL << 31) || p->total_q >= (1 << (31 - kSlotBits)))
+    return MSA_ERR_UNSUPPORTED;
   return MSA_OK;
 }
 
+bool op_is_forward(msa_op_t op) { return op == MSA_OP_FORWARD || op == MSA_OP_FORWARD_FP8; }
 bool op_uses_index_prefill(msa_op_t op, const Derived& d) {
-  return op == MSA_OP_INDEX_POOL || ((op == MSA_OP_INDEX_TOPK || op == MSA_OP_FORWARD) && !d.decode);
+  return op == MSA_OP_INDEX_POOL || ((op == MSA_OP_INDEX_TOPK || op_is_forward(op)) && !d.decode);
 }
 bool op_uses_decode_index(msa_op_t op, const Derived& d) {
-  return (op == MSA_OP_INDEX_TOPK || op == MSA_OP_FORWARD) && d.decode;
+  return (op == MSA_OP_INDEX_TOPK || op_is_forward(op)) && d.decode;
+}
+// The index epilogue keeps a top-(k-1) register list per row for k up to this;
+// larger k pool the scores into the workspace and select with a separate kernel.
+constexpr int kFusedTopkMax = 16;
+bool op_uses_pooled_prefill(msa_op_t op, const Derived& d) {
+  return (op == MSA_OP_INDEX_TOPK || op_is_forward(op)) && !d.decode && d.topk > kFusedTopkMax;
 }
 bool op_uses_prefill_attn(msa_op_t op, const Derived& d) {
-  return op == MSA_OP_SPARSE_ATTN_PREFILL || (op == MSA_OP_FORWARD && !d.decode);
+  return op == MSA_OP_SPARSE_ATTN_PREFILL || op == MSA_OP_SPARSE_ATTN_PREFILL_FP8 || (op_is_forward(op) && !d.decode);
 }
 bool op_uses_decode_attn(msa_op_t op, const Derived& d) {
-  return op == MSA_OP_SPARSE_ATTN_DECODE || (op == MSA_OP_FORWARD && d.decode);
+  return op == MSA_OP_SPARSE_ATTN_DECODE || op == MSA_OP_SPARSE_ATTN_DECODE_FP8 || (op_is_forward(op) && d.decode);
+}
+bool op_is_fp8(msa_op_t op) {
+  return op == MSA_OP_SPARSE_ATTN_PREFILL_FP8 || op == MSA_OP_SPARSE_ATTN_DECODE_FP8 || op == MSA_OP_FORWARD_FP8;
 }
 
 Layout layout(const Derived& d, msa_op_t op) {
@@ -131,7 +143,8 @@ Layout layout(const Derived& d, msa_op_t op) {
   L.hist = take(sizeof(int32_t) * (d.max_nb + 2));
   L.cursor = take(sizeof(int32_t) * (d.max_nb + 2));
   if (op_uses_index_prefill(op, d)) L.tiles = take(sizeof(int2) * d.max_tiles);
-  if (op_uses_decode_index(op, d)) L.pooled = take(sizeof(float) * static_cast<size_t>(d.T) * d.hkv * d.max_nb);
+  if (op_uses_decode_index(op, d) || op_uses_pooled_prefill(op, d))
+    L.pooled = take(sizeof(float) * static_cast<size_t>(d.T) * d.hkv * d.max_nb);
   if (op_uses_prefill_attn(op, d)) {
     L.count = take(sizeof(int32_t) * d.n_buckets);
     L.bstart = take(sizeof(int32_t) * (d.n_buckets + 1));
@@ -142,6 +155,7 @@ Layout layout(const Derived& d, msa_op_t op) {
     L.chunks = take(sizeof(int4) * (d.max_chunks > 0 ? d.max_chunks : 1));
     L.scan_tmp = take(sizeof(int32_t) * scan_tmp_ints(static_cast<int>(d.n_buckets)));
     L.v16 = take(sizeof(__half) * static_cast<size_t>(d.N) * d.hkv * kHeadDim);
+    if (op_is_fp8(op)) L.k16 = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.N) * d.hkv * kHeadDim);
   }
   if (op_uses_prefill_attn(op, d) || op_uses_decode_attn(op, d)) {
     L.part_o = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.n_inc) * d.G * kHeadDim);
@@ -232,6 +246,14 @@ bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_hea
   return make_map(m, ptr, 3, dims, strides, box, dtype);
 }
 
+// E4M3 codes [n, heads, 128] (one byte each), box = 128 codes x 1 head x 128 rows
+bool map_3d_u8(CUtensorMap& m, const void* ptr, long long n, int heads) {
+  cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(n > 0 ? n : 1)};
+  cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(heads) * 128};
+  cuuint32_t box[3] = {128, 1, 128};
+  return make_map(m, ptr, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 // Q [n, hq, 128] seen per (query, group) with the group's G heads split into
 // 8-row groups and each row into its two 64-dim halves: dims {64 dims, 8 heads,
 // 2 halves, G / 8 row groups, n * hkv query-groups}.  One box = one query's
@@ -257,6 +279,10 @@ struct Ctx {
   const int32_t* block_table = nullptr;
   int bt_stride = 0;
   long long n_pages = 0;
+  // fp8 K/V: k and v are E4M3 codes with these scales [n_key_blocks, hkv]
+  bool fp8 = false;
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
   long long cache_rows() const { return block_table ? n_pages * 128 : d.N; }
 };
 
@@ -266,11 +292,11 @@ msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_byte
   t_error_detail[0] = 0;
   msa_status_t st = derive(p, c.d);
   if (st != MSA_OK) return st;
-  if ((op == MSA_OP_SPARSE_ATTN_DECODE) && !c.d.decode) return MSA_ERR_INVALID_ARG;
+  if ((op == MSA_OP_SPARSE_ATTN_DECODE || op == MSA_OP_SPARSE_ATTN_DECODE_FP8) && !c.d.decode)
+    return MSA_ERR_INVALID_ARG;
   // decode batches: exactly one query per sequence
   if ((op_uses_decode_index(op, c.d) || op_uses_decode_attn(op, c.d)) && c.d.T != c.d.S) return MSA_ERR_INVALID_ARG;
   if (op_uses_decode_index(op, c.d) && c.d.hkv > 8) return MSA_ERR_UNSUPPORTED;
-  if (op_uses_decode_attn(op, c.d) && c.d.G != 16) return MSA_ERR_UNSUPPORTED;
   c.L = layout(c.d, op);
   if (!ws || ws_bytes < c.L.total) return MSA_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MSA_ERR_ALIGNMENT;
@@ -396,6 +422,18 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   return run_topk_pooled(p, c, pooled, c.d.max_nb, idx);
 }
 
+// Index Branch of a prefill batch: scores, max-pool and top-k in one kernel
+// (k <= kFusedTopkMax), or pooled scores into the workspace, then top-k.
+msa_status_t run_index_select_prefill(const msa_problem_t* p, Ctx& c, const void* q_idx, const void* k_idx,
+                                      int32_t* idx) {
+  if (c.d.topk <= kFusedTopkMax) return run_index_prefill(p, c, q_idx, k_idx, true, nullptr, 0, idx);
+  if (c.d.T == 0) return MSA_OK;
+  float* pooled = at<float>(c.ws, c.L.pooled);
+  msa_status_t st = run_index_prefill(p, c, q_idx, k_idx, false, pooled, c.d.max_nb, nullptr);
+  if (st != MSA_OK) return st;
+  return run_topk_pooled(p, c, pooled, c.d.max_nb, idx);
+}
+
 PartialBuffers partials(Ctx& c) {
   PartialBuffers pb;
   pb.o = at<__nv_bfloat16>(c.ws, c.L.part_o);
@@ -458,8 +496,10 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
   if (st != MSA_OK) return st;
 
   __half* v16 = at<__half>(c.ws, c.L.v16);
+  // fp8 K/V: the Main Branch reads exact 16-bit copies of the codes (K bf16, V fp16)
+  __nv_bfloat16* k16 = c.fp8 ? at<__nv_bfloat16>(c.ws, c.L.k16) : nullptr;
   CUtensorMap tq, tk, tv;
-  if (!map_q_groups(tq, q, c.d.T, c.d.hkv, c.d.G) || !map_3d(tk, k, c.d.N, c.d.hkv, 1, 128) ||
+  if (!map_q_groups(tq, q, c.d.T, c.d.hkv, c.d.G) || !map_3d(tk, c.fp8 ? k16 : k, c.d.N, c.d.hkv, 1, 128) ||
       !map_3d(tv, v16, c.d.N, c.d.hkv, 1, 128, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
     return MSA_ERR_CUDA;
   AttnParams ap{};
@@ -474,10 +514,18 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
   ap.topk = c.d.topk;
   ap.qpt = c.d.qpt;
   ap.scale_log2 = c.d.scale * 1.4426950408889634f;
+  ap.k_scale = c.k_scale;
+  ap.v_scale = c.v_scale;
+  ap.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);
-    st = cuda_status(launch_v_prep(static_cast<const __nv_bfloat16*>(v), v16,
-                                   static_cast<long long>(c.d.N) * c.d.hkv * kHeadDim, c.hdr, c.dev.sms, c.stream));
+    const long long n_elems = static_cast<long long>(c.d.N) * c.d.hkv * kHeadDim;
+    if (c.fp8)
+      st = cuda_status(launch_kv8_widen(static_cast<const uint8_t*>(k), static_cast<const uint8_t*>(v), k16, v16,
+                                        n_elems, c.hdr, c.dev.sms, c.stream));
+    else
+      st = cuda_status(launch_v_prep(static_cast<const __nv_bfloat16*>(v), v16, n_elems, c.hdr, c.dev.sms,
+                                     c.stream));
     if (st == MSA_OK) st = cuda_status(launch_sparse_attn(tq, tk, tv, ap, c.dev.sms, c.stream));
   }
   if (st != MSA_OK) return st;
@@ -488,8 +536,9 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
                              const int32_t* idx, void* o, float* lse) {
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tq, tk, tv;
-  if (!map_3d(tq, q, c.d.T, c.d.hq, 16, 1) || !map_3d(tk, k, c.cache_rows(), c.d.hkv, 1, 128) ||
-      !map_3d(tv, v, c.cache_rows(), c.d.hkv, 1, 128))
+  if (!map_3d(tq, q, c.d.T, c.d.hq, c.d.G < 16 ? c.d.G : 16, 1)) return MSA_ERR_CUDA;
+  if (c.fp8 ? (!map_3d_u8(tk, k, c.cache_rows(), c.d.hkv) || !map_3d_u8(tv, v, c.cache_rows(), c.d.hkv))
+            : (!map_3d(tk, k, c.cache_rows(), c.d.hkv, 1, 128) || !map_3d(tv, v, c.cache_rows(), c.d.hkv, 1, 128)))
     return MSA_ERR_CUDA;
   DecodeAttnParams dp{};
   dp.num_seqs = c.d.S;
@@ -505,10 +554,13 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
   dp.block_table = c.block_table;
   dp.bt_stride = c.bt_stride;
   dp.n_pages = c.n_pages;
+  dp.k_scale = c.k_scale;
+  dp.v_scale = c.v_scale;
+  dp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   msa_status_t st;
   {
     StageScope scope(MSA_STAGE_ATTN, c.stream);
-    st = cuda_status(launch_decode_attn(tq, tk, tv, dp, c.stream));
+    st = cuda_status(launch_decode_attn(tq, tk, tv, dp, c.fp8, c.stream));
   }
   if (st != MSA_OK) return st;
   return run_combine(p, c, idx, o, lse);
@@ -527,16 +579,46 @@ static __device__ __align__(256) uint8_t msa_static_scratch[MSA_STATIC_SCRATCH_B
 namespace msa {
 namespace {
 
+// Identifier of the calling thread's current CUDA context (unique for the
+// life of the process, never reused), or 0 when it cannot be read.
+unsigned long long current_context_id() {
+  using GetCtx = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCtx get_ctx = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_ctx = reinterpret_cast<GetCtx>(a);
+      get_id = reinterpret_cast<GetId>(b);
+    }
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 // Device address of msa_static_scratch on the current device.  In host code
 // the array's name only stands in for the symbol, so the address is looked up
-// once per device with that device current, then cached.
+// with that device current and cached per device, together with the context it
+// belongs to: after a device reset (a new primary context) it is looked up
+// again.
 msa_status_t static_scratch_address(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MSA_ERR_DEVICE;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!addr[dev] || (ctx != 0 && ctx != ctx_of[dev])) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, msa_static_scratch);
     if (e != cudaSuccess || !ptr) {
@@ -545,6 +627,7 @@ msa_status_t static_scratch_address(void** out) {
       return MSA_ERR_CUDA;
     }
     addr[dev] = ptr;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return MSA_OK;
@@ -591,7 +674,7 @@ const char* msa_status_string(msa_status_t s) {
 
 msa_status_t msa_workspace_size(const msa_problem_t* problem, msa_op_t op, size_t* bytes) {
   if (!bytes) return MSA_ERR_INVALID_ARG;
-  if (op < MSA_OP_INDEX_POOL || op > MSA_OP_TOPK_POOLED) return MSA_ERR_INVALID_ARG;
+  if (op < MSA_OP_INDEX_POOL || op > MSA_OP_INDEX_PROLOGUE) return MSA_ERR_INVALID_ARG;
   Derived d;
   msa_status_t st = derive(problem, d);
   if (st != MSA_OK) return st;
@@ -642,7 +725,7 @@ msa_status_t msa_index_topk(const msa_problem_t* problem, const void* q_idx, con
     return run_index_decode(problem, c, q_idx, k_idx, idx);
   }
   if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
-  return run_index_prefill(problem, c, q_idx, k_idx, true, nullptr, 0, idx);
+  return run_index_select_prefill(problem, c, q_idx, k_idx, idx);
 }
 
 static msa_status_t check_attn_args(const void* q, const void* k, const void* v, const int32_t* idx,
@@ -724,7 +807,7 @@ msa_status_t msa_forward(const msa_problem_t* problem, const void* q, const void
     return run_attn_decode(problem, c, q, k, v, idx, o, lse);
   }
   if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
-  if ((st = run_index_prefill(problem, c, q_idx, k_idx, true, nullptr, 0, idx)) != MSA_OK) return st;
+  if ((st = run_index_select_prefill(problem, c, q_idx, k_idx, idx)) != MSA_OK) return st;
   return run_attn_prefill(problem, c, q, k, v, idx, o, lse);
 }
 
@@ -753,8 +836,154 @@ msa_status_t msa_forward_decode_paged(const msa_problem_t* problem, const void* 
   return run_attn_decode(problem, c, q, k_cache, v_cache, idx, o, lse);
 }
 
+// ---------------------------------------------------------------- index prologue
+msa_status_t msa_index_prologue(const msa_problem_t* problem, const void* x, int32_t d_model, const void* w_q,
+                                const void* w_k, const void* gamma_q, const void* gamma_k, void* q_idx,
+                                void* k_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!x || !w_q || !w_k || !gamma_q || !gamma_k || !q_idx || !k_idx) return MSA_ERR_INVALID_ARG;
+  if (d_model <= 0) return MSA_ERR_INVALID_ARG;
+  if (d.d_idx != 128 || d_model % 64 || d_model > (1 << 16)) return MSA_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w_q) || !aligned16(w_k) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      (reinterpret_cast<uintptr_t>(gamma_q) & 1u) || (reinterpret_cast<uintptr_t>(gamma_k) & 1u))
+    return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_INDEX_PROLOGUE, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  if (c.d.T == 0) return MSA_OK;
+  CUtensorMap tx, twq, twk;
+  if (!map_2d(tx, x, c.d.T, d_model, 128) || !map_2d(twq, w_q, static_cast<long long>(c.d.hkv) * 128, d_model, 128) ||
+      !map_2d(twk, w_k, 128, d_model, 128))
+    return MSA_ERR_CUDA;
+  PrologueParams pp{};
+  pp.num_seqs = c.d.S;
+  pp.total_q = c.d.T;
+  pp.hkv = c.d.hkv;
+  pp.d_model = d_model;
+  pp.n_row_tiles = (c.d.T + 127) / 128;
+  pp.cu_q = problem->cu_seqlens_q;
+  pp.seq = c.seq;
+  pp.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
+  pp.gamma_k = static_cast<const __nv_bfloat16*>(gamma_k);
+  pp.q_idx = static_cast<__nv_bfloat16*>(q_idx);
+  pp.k_idx = static_cast<__nv_bfloat16*>(k_idx);
+  for (int j = 0; j < 32; ++j) pp.rope_turns[j] = std::pow(10000.0, -j / 32.0) / (2.0 * 3.14159265358979323846);
+  pp.hdr = c.hdr;
+  StageScope scope(MSA_STAGE_INDEX, c.stream);
+  return cuda_status(launch_index_prologue(tx, twq, twk, pp, c.dev.sms, c.stream));
+}
+
+// ---------------------------------------------------------------- fp8 K/V
+static msa_status_t check_fp8_args(const void* k8, const void* v8, const float* k_scale, const float* v_scale) {
+  if (!k8 || !v8 || !k_scale || !v_scale) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k8) || !aligned16(v8) || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return MSA_ERR_ALIGNMENT;
+  return MSA_OK;
+}
+
+msa_status_t msa_quantize_kv_fp8(const msa_problem_t* problem, const void* k, const void* v, void* k8, void* v8,
+                                 float* k_scale, float* v_scale, void* workspace, size_t workspace_bytes,
+                                 msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!k || !v) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return MSA_ERR_ALIGNMENT;
+  if ((st = check_fp8_args(k8, v8, k_scale, v_scale)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_QUANTIZE_KV_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  QuantParams qp{};
+  qp.num_seqs = c.d.S;
+  qp.hkv = c.d.hkv;
+  qp.seq = c.seq;
+  qp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
+  qp.k = static_cast<const __nv_bfloat16*>(k);
+  qp.v = static_cast<const __nv_bfloat16*>(v);
+  qp.k8 = static_cast<uint8_t*>(k8);
+  qp.v8 = static_cast<uint8_t*>(v8);
+  qp.k_scale = k_scale;
+  qp.v_scale = v_scale;
+  qp.hdr = c.hdr;
+  return cuda_status(launch_quantize_kv_fp8(qp, c.d.N > 0 ? c.d.total_blocks : 0, c.stream));
+}
+
+msa_status_t msa_sparse_attn_prefill_fp8(const msa_problem_t* problem, const void* q, const void* k8,
+                                         const void* v8, const float* k_scale, const float* v_scale,
+                                         const int32_t* idx, void* o, float* lse, void* workspace,
+                                         size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k8, v8, idx, o, lse)) != MSA_OK) return st;
+  if ((st = check_fp8_args(k8, v8, k_scale, v_scale)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_SPARSE_ATTN_PREFILL_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK)
+    return st;
+  c.fp8 = true;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  return run_attn_prefill(problem, c, q, k8, v8, idx, o, lse);
+}
+
+msa_status_t msa_sparse_attn_decode_fp8(const msa_problem_t* problem, const void* q, const void* k8,
+                                        const void* v8, const float* k_scale, const float* v_scale,
+                                        const int32_t* idx, void* o, float* lse, void* workspace,
+                                        size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k8, v8, idx, o, lse)) != MSA_OK) return st;
+  if ((st = check_fp8_args(k8, v8, k_scale, v_scale)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_SPARSE_ATTN_DECODE_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK)
+    return st;
+  c.fp8 = true;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  return run_attn_decode(problem, c, q, k8, v8, idx, o, lse);
+}
+
+msa_status_t msa_forward_fp8(const msa_problem_t* problem, const void* q, const void* k8, const void* v8,
+                             const float* k_scale, const float* v_scale, const void* q_idx, const void* k_idx,
+                             int32_t* idx, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                             msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k8, v8, idx, o, lse)) != MSA_OK) return st;
+  if ((st = check_fp8_args(k8, v8, k_scale, v_scale)) != MSA_OK) return st;
+  if (!q_idx || !k_idx) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_FORWARD_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  c.fp8 = true;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  if (c.d.decode) {
+    if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+    if ((st = run_index_decode(problem, c, q_idx, k_idx, idx)) != MSA_OK) return st;
+    return run_attn_decode(problem, c, q, k8, v8, idx, o, lse);
+  }
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  if ((st = run_index_select_prefill(problem, c, q_idx, k_idx, idx)) != MSA_OK) return st;
+  return run_attn_prefill(problem, c, q, k8, v8, idx, o, lse);
+}
+
 msa_status_t msa_read_device_status(const void* workspace, uint32_t* flags, msa_stream_t stream) {
-  if (!workspace || !flags) return MSA_ERR_INVALID_ARG;
+  if (!flags) return MSA_ERR_INVALID_ARG;
+  t_error_detail[0] = 0;
+  if (!workspace) {  // the fixed scratch of msa_sparse_attn_decode_static on the current device
+    void* scratch = nullptr;
+    const msa_status_t st = static_scratch_address(&scratch);
+    if (st != MSA_OK) return st;
+    workspace = scratch;
+  }
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return MSA_ERR_ALIGNMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   uint32_t v = 0;

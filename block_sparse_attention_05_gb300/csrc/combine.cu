@@ -13,7 +13,7 @@
 //
 // One warp per two heads of a query (same group, G >= 8): each half-warp
 // owns a head, its lanes 8 of the 128 output columns and, for the slot
-// loads, one slot each.  Every load -- the slots' block indices, LSEs, log
+// loads, one slot each (slots hl, hl + 16, ... when k > 16).  Every load -- the slots' block indices, LSEs, log
 // weights and all k partial rows -- is issued before any is used, so a row
 // costs one memory round trip; the sequence lookup that decides which slots
 // are valid runs alongside.  Slots whose block index is -1 or past the
@@ -34,7 +34,6 @@ namespace msa {
 namespace {
 
 constexpr int kCombineWarps = 8;
-constexpr int kMaxTopk = 16;
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -55,6 +54,9 @@ __device__ __forceinline__ PairRef pair_ref(const CombineParams& p, int64_t pair
   return r;
 }
 
+// NG groups of 16 slots (topk <= 16 NG): lane hl of a half-warp holds slots hl, hl + 16, ... for the
+// log-sum-exp, and the partial rows are loaded and accumulated 16 slots at a time.
+template <int NG>
 __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineParams p) {
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -63,67 +65,97 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kCombineWarps;
   const int64_t slot_stride = static_cast<int64_t>(p.group) * kHeadDim;
   for (int64_t pair = static_cast<int64_t>(blockIdx.x) * kCombineWarps + warp; pair < n_pairs; pair += stride) {
-    // the next item's rows: lane (half, hl) covers slot hl of head 2 * pair + half, 256 bytes = 2 lines
-    if (pair + stride < n_pairs && hl < p.topk) {
+    // the next item's rows: lane (half, hl) covers slots hl + 16 j of head 2 * pair + half, 256 bytes = 2 lines
+    if (pair + stride < n_pairs) {
       const PairRef nx = pair_ref(p, pair + stride, half);
-      const __nv_bfloat16* row = p.part.o + ((nx.sel_base + hl) * p.group + nx.hh) * kHeadDim;
-      prefetch_l2(row);
-      prefetch_l2(row + 64);
+#pragma unroll
+      for (int j = 0; j < NG; ++j)
+        if (hl + 16 * j < p.topk) {
+          const __nv_bfloat16* row = p.part.o + ((nx.sel_base + hl + 16 * j) * p.group + nx.hh) * kHeadDim;
+          prefetch_l2(row);
+          prefetch_l2(row + 64);
+        }
     }
     const PairRef r = pair_ref(p, pair, half);
     const int i = r.i, h = r.h, hh = r.hh;
     const int64_t sel_base = r.sel_base;
 
-    int b = -1;
-    float l_s = -INFINITY, w_s = -INFINITY;
-    if (hl < p.topk) {
-      b = p.idx[sel_base + hl];
-      l_s = p.part.lse[(sel_base + hl) * p.group + hh];
-      w_s = p.part.ow[(sel_base + hl) * p.group + hh];
+    int b[NG];
+    float l_s[NG], w_s[NG];
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      const int sl = hl + 16 * j;
+      b[j] = -1;
+      l_s[j] = -INFINITY;
+      w_s[j] = -INFINITY;
+      if (sl < p.topk) {
+        b[j] = p.idx[sel_base + sl];
+        l_s[j] = p.part.lse[(sel_base + sl) * p.group + hh];
+        w_s[j] = p.part.ow[(sel_base + sl) * p.group + hh];
+      }
     }
     const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
-    uint4 raw[kMaxTopk];
+    uint4 raw[16];
 #pragma unroll
-    for (int sl = 0; sl < kMaxTopk; ++sl)
+    for (int sl = 0; sl < 16; ++sl)
       raw[sl] = (sl < p.topk) ? __ldcs(reinterpret_cast<const uint4*>(base + sl * slot_stride))
                               : make_uint4(0, 0, 0, 0);
 
     const int s = find_seq(p.cu_q, p.num_seqs, i);
     const SeqInfo si = p.seq[s];
     const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
-    const bool valid = hl < p.topk && b >= 0 && b <= local;
-    if (!valid) l_s = -INFINITY;
-
-    float m = l_s;
+    bool valid[NG];
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NG; ++j) {
+      valid[j] = hl + 16 * j < p.topk && b[j] >= 0 && b[j] <= local;
+      if (!valid[j]) l_s[j] = -INFINITY;
+      m = fmaxf(m, l_s[j]);
+    }
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float sum = valid ? expf(l_s - m) : 0.f;
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < NG; ++j) sum += valid[j] ? expf(l_s[j] - m) : 0.f;
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
     const float L = m + logf(sum);
-    const float w = valid ? expf(w_s - L) : 0.f;
+    float w[NG];
+#pragma unroll
+    for (int j = 0; j < NG; ++j) w[j] = valid[j] ? expf(w_s[j] - L) : 0.f;
 
     // acc[j] holds columns 2j, 2j + 1: one packed fma per bf16 pair (the same single rounding per
     // element as two scalar fmas); a bf16 widens to fp32 by moving its bits to the high half
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int sl = 0; sl < kMaxTopk; ++sl) {
-      const float ws = __shfl_sync(0xFFFFFFFFu, w, (lane & 16) | sl);
-      if (sl < p.topk && ws != 0.f) {
-        const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
-        const float2 w2 = make_float2(ws, ws);
+    for (int j = 0; j < NG; ++j) {
+      if (j > 0) {  // the next 16 slots' rows (the first 16 were issued before the weights)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          acc[j] = ffma2(w2, make_float2(__uint_as_float(v[j] << 16), __uint_as_float(v[j] & 0xFFFF0000u)), acc[j]);
+        for (int sl = 0; sl < 16; ++sl)
+          raw[sl] = (16 * j + sl < p.topk)
+                        ? __ldcs(reinterpret_cast<const uint4*>(base + (16 * j + sl) * slot_stride))
+                        : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int sl = 0; sl < 16; ++sl) {
+        const float ws = __shfl_sync(0xFFFFFFFFu, w[j], (lane & 16) | sl);
+        if (16 * j + sl < p.topk && ws != 0.f) {
+          const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
+          const float2 w2 = make_float2(ws, ws);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            acc[c] = ffma2(w2, make_float2(__uint_as_float(v[c] << 16), __uint_as_float(v[c] & 0xFFFF0000u)),
+                           acc[c]);
+        }
       }
     }
     const bool empty = (m == -INFINITY);
     uint4 out;
     uint32_t* ow = &out.x;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 t = __floats2bfloat162_rn(acc[j].x, acc[j].y);
-      ow[j] = *reinterpret_cast<const uint32_t*>(&t);
+    for (int c = 0; c < 4; ++c) {
+      const __nv_bfloat162 t = __floats2bfloat162_rn(acc[c].x, acc[c].y);
+      ow[c] = *reinterpret_cast<const uint32_t*>(&t);
     }
     const int64_t orow = static_cast<int64_t>(i) * p.hq + h;
     *reinterpret_cast<uint4*>(p.o + orow * kHeadDim + hl * 8) = out;
@@ -138,7 +170,12 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (pairs == 0) return cudaSuccess;
   int64_t grid = (pairs + kCombineWarps - 1) / kCombineWarps;
   if (grid > 2LL * p.sms) grid = 2LL * p.sms;
-  combine_kernel<<<static_cast<unsigned>(grid), 32 * kCombineWarps, 0, stream>>>(p);
+  const unsigned g = static_cast<unsigned>(grid);
+  const int ng = (p.topk + 15) / 16;
+  if (ng <= 1) combine_kernel<1><<<g, 32 * kCombineWarps, 0, stream>>>(p);
+  else if (ng == 2) combine_kernel<2><<<g, 32 * kCombineWarps, 0, stream>>>(p);
+  else if (ng == 3) combine_kernel<3><<<g, 32 * kCombineWarps, 0, stream>>>(p);
+  else combine_kernel<4><<<g, 32 * kCombineWarps, 0, stream>>>(p);
   note_launches(1);
   return cudaGetLastError();
 }

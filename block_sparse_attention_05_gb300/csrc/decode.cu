@@ -13,11 +13,13 @@
 // instruction count per byte low so the issue slots never limit the stream.
 //
 // Attention: persistent CTAs (two per SM) over the (sequence, group, selected
-// block) items: a producer thread streams each item's Q rows, K block and V
-// block by TMA, four warps compute it (the group's 16 heads as the M = 16 rows
-// of mma.sync tiles, 32 keys per warp) and merge in shared memory, then write
-// a normalised partial output and its LSE per slot.  combine.cu merges the
+// block, 16-head slice) items: a producer thread streams each item's Q rows,
+// K block and V block by TMA, four warps compute it (16 heads of the group as
+// the M = 16 rows of mma.sync tiles, 32 keys per warp) and merge in shared
+// memory, then write a normalised partial output and its LSE per slot.  combine.cu merges the
 // slots (split-KV with a log-sum-exp combine).
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -244,7 +246,34 @@ constexpr int kOsumStride = 128 + 8;
 // Per CTA (two per SM): K and V buffers (32 KB each), the item's Q (4 KB),
 // the merge slices and per-warp (max, sum), the item hand-over, barriers.
 constexpr size_t kDecSmemBytes = 1024 + 65536 + 4096 + 4 * 16 * kOsumStride * sizeof(float) +
-                                 4 * 16 * 2 * sizeof(float) + 16 + (4 + 3) * 8 + 16;
+                                 4 * 16 * 2 * sizeof(float) + 32 + (4 + 5) * 8 + 16;
+// fp8 K/V: the E4M3 codes of the item's K and V blocks (16 KB each) land in a
+// staging area and the compute warps widen them into the bf16 K and V buffers
+// (one CTA per SM at this size).
+constexpr size_t kDec8Staging = 32768;
+
+// Widens one 128-byte row of E4M3 codes (TMA 128-byte swizzled, 16-byte chunks
+// XOR row % 8) into row `row` of a bf16 tile in the layout the bf16 loads give
+// (64-dim halves 16 KB apart, 128-byte swizzle).  Exact: an E4M3 value has 4
+// significant bits and fits bf16's exponent range.
+__device__ __forceinline__ void widen_e4m3_row(const uint8_t* src, uint8_t* dst, int row) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c + 15
+    const uint4 w = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>((ws[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, __NV_E4M3);
+      const __half2 h = *reinterpret_cast<const __half2*>(&hr);
+      const __nv_bfloat162 b = __floats2bfloat162_rn(__low2float(h), __high2float(h));
+      o[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(dst + sw128_off(row, 2 * c)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + sw128_off(row, 2 * c + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -279,7 +308,9 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 struct DecodeItem {
   long long sel;  // (sequence * hkv + group) * topk + slot, or -1 after the last item
   int lim;        // last visible key of the block (kv_len - 1 - block * 128)
-  int pad;
+  int hs;         // head slice: heads 16 hs .. 16 hs + 15 of the group
+  float sk, sv;   // fp8 K/V: the block's scales (1 for bf16 K/V)
+  int pad[2];
 };
 
 // Byte offset of (row, 8-element chunk) in the 16-row Q tile: 128-byte
@@ -288,13 +319,18 @@ __device__ __forceinline__ uint32_t q_off(int row, int chunk) {
   return (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
 }
 
+// FP8: K and V are E4M3 codes with per-(key block, KV head) scales (tm_k and
+// tm_v map the codes); the logits take the K scale and the partial output the
+// V scale.
+template <bool FP8>
 __global__ void __launch_bounds__(kDecThreads + 32)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, DecodeAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   if (hdr->status & kFlagBadSeqlens) return;
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage8 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = stage8 + (FP8 ? kDec8Staging : 0);                       // fp8: K codes 16 KB | V codes 16 KB
   uint8_t* ring = base;                                                    // K 32 KB | V 32 KB
   uint8_t* qbuf = base + 65536;                                            // Q 16 heads x 128 (4 KB)
   float* osum = reinterpret_cast<float*>(base + 65536 + 4096);             // [4 warps][16 heads][kOsumStride]
@@ -302,19 +338,30 @@ __global__ void __launch_bounds__(kDecThreads + 32)
   DecodeItem* info = reinterpret_cast<DecodeItem*>(red + 4 * 16 * 2);
   uint64_t* full = reinterpret_cast<uint64_t*>(info + 1);                  // [0] Q + K landed, [1] V landed
   uint64_t* empty = full + 2;                                              // [0] K read, [1] V read
-  uint64_t* mrg = empty + 2;  // per item: red written, partial sums added, merged output read
-  int* abort_flag = reinterpret_cast<int*>(mrg + 3);
+  // per item: red written, partial sums added, merged output read; fp8: K and V codes widened
+  uint64_t* mrg = empty + 2;
+  int* abort_flag = reinterpret_cast<int*>(mrg + 5);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = p.group;  // 16
-  const long long n_items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
+  const int G = p.group;
+  // a group's heads are taken 16 at a time (G >= 16: G / 16 head slices per (sequence, group, slot));
+  // with G = 8 the tile's last 8 rows are zeros and nothing of theirs is stored
+  const int nhs = G >= 16 ? G / 16 : 1;
+  const int rows = G >= 16 ? 16 : G;
+  const long long n_items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk * nhs;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 4);  // one arrival per compute warp
     }
-    for (int i = 0; i < 3; ++i) mbar_init(&mrg[i], 4);
+    for (int i = 0; i < 5; ++i) mbar_init(&mrg[i], 4);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (rows < 16) {  // Q rows 8..15 of both 64-dim halves (the loads fill rows 0..7 only)
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+      reinterpret_cast<uint4*>(qbuf + 1024)[i] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(qbuf + 3072)[i] = make_uint4(0, 0, 0, 0);
+    }
   }
   __syncthreads();
 
@@ -334,7 +381,9 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     if (lane == 0) {
       uint32_t nk = 0, nv = 0;  // Q + K and V fills issued
       bool stopped = false, ended = false;
-      for (long long it = blockIdx.x; it < n_items; it += gridDim.x) {
+      for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const long long it = item / nhs;  // (sequence, group, slot)
+        const int hs = static_cast<int>(item % nhs);
         int s, g, b;
         item_block(it, s, g, b);
         if (b < 0) continue;
@@ -346,21 +395,38 @@ __global__ void __launch_bounds__(kDecThreads + 32)
           break;
         }
         info->sel = it;
+        info->hs = hs;
         info->lim = p.seq[s].kv_len - 1 - b * kBlock;
-        mbar_arrive_expect_tx(&full[0], 32768 + 4096);
-        tma_load_3d(qbuf, &tm_q, &full[0], 0, g * 16, s);
-        tma_load_3d(qbuf + 2048, &tm_q, &full[0], 64, g * 16, s);
-        tma_load_3d(ring, &tm_k, &full[0], 0, g, krow);
-        tma_load_3d(ring + 16384, &tm_k, &full[0], 64, g, krow);
+        info->sk = 1.f;
+        info->sv = 1.f;
+        if constexpr (FP8) {
+          const long long srow = (static_cast<long long>(p.blk_off[s]) + b) * p.hkv + g;
+          info->sk = p.k_scale[srow];
+          info->sv = p.v_scale[srow];
+        }
+        mbar_arrive_expect_tx(&full[0], (FP8 ? 16384 : 32768) + rows * 256);
+        tma_load_3d(qbuf, &tm_q, &full[0], 0, g * G + hs * 16, s);
+        tma_load_3d(qbuf + 2048, &tm_q, &full[0], 64, g * G + hs * 16, s);
+        if constexpr (FP8) {
+          tma_load_3d(stage8, &tm_k, &full[0], 0, g, krow);
+        } else {
+          tma_load_3d(ring, &tm_k, &full[0], 0, g, krow);
+          tma_load_3d(ring + 16384, &tm_k, &full[0], 64, g, krow);
+        }
         ++nk;
         if (nv >= 1 && !mbar_wait(&empty[1], (nv - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 323);
           stopped = true;
           break;
         }
-        mbar_arrive_expect_tx(&full[1], 32768);
-        tma_load_3d(ring + 32768, &tm_v, &full[1], 0, g, krow);
-        tma_load_3d(ring + 49152, &tm_v, &full[1], 64, g, krow);
+        if constexpr (FP8) {
+          mbar_arrive_expect_tx(&full[1], 16384);
+          tma_load_3d(stage8 + 16384, &tm_v, &full[1], 0, g, krow);
+        } else {
+          mbar_arrive_expect_tx(&full[1], 32768);
+          tma_load_3d(ring + 32768, &tm_v, &full[1], 0, g, krow);
+          tma_load_3d(ring + 49152, &tm_v, &full[1], 64, g, krow);
+        }
         ++nv;
       }
       if (!stopped) {
@@ -401,7 +467,15 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     }
     const long long sel = vinfo->sel;
     const int lim = vinfo->lim;
+    const int hs = vinfo->hs;
+    const float sk = vinfo->sk, sv = vinfo->sv;
     if (sel < 0) break;
+    if constexpr (FP8) {
+      // the previous item's K buffer is free (every compute warp arrived on empty[0] before these codes landed)
+      widen_e4m3_row(stage8, ring, threadIdx.x);
+      if (!meet(3, n)) break;
+    }
+    const float scale_log2 = p.scale_log2 * sk;
     const uint32_t kt = smem_u32(ring), vt = kt + 32768, qt = smem_u32(qbuf);
     const int mtx = lane >> 3, mr = lane & 7;
     // Q fragments (16 heads x 128 dims) for the m16n8k16 A operand
@@ -439,7 +513,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = c0 + (j & 1);
-        const float x = (c <= lim) ? sacc[nt][j] * p.scale_log2 : -INFINITY;
+        const float x = (c <= lim) ? sacc[nt][j] * scale_log2 : -INFINITY;
         sacc[nt][j] = x;
       }
       m0 = fmaxf(m0, fmaxf(sacc[nt][0], sacc[nt][1]));
@@ -469,6 +543,10 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     if (!mbar_wait_warp(&full[1], n & 1, abort_flag)) {
       if (lane == 0) report_timeout(abort_flag, hdr, 324);
       break;
+    }
+    if constexpr (FP8) {
+      widen_e4m3_row(stage8 + 16384, ring + 32768, threadIdx.x);
+      if (!meet(4, n)) break;
     }
     // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
     float oacc[16][4];
@@ -523,8 +601,9 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       L0 += (mw0 == -INFINITY) ? 0.f : red[(w * 16 + h0) * 2 + 1] * exp2f(mw0 - R0);
       L1 += (mw1 == -INFINITY) ? 0.f : red[(w * 16 + h0 + 8) * 2 + 1] * exp2f(mw1 - R1);
     }
-    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0;
-    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1;
+    // the V scale (fp8) multiplies the normalised partial
+    const float f0 = (m0 == -INFINITY || L0 == 0.f) ? 0.f : exp2f(m0 - R0) / L0 * sv;
+    const float f1 = (m1 == -INFINITY || L1 == 0.f) ? 0.f : exp2f(m1 - R1) / L1 * sv;
     // each warp's scaled partial into its own slice, then a 4-way sum per element
     float* mine = osum + warp * 16 * kOsumStride;
 #pragma unroll
@@ -535,8 +614,8 @@ __global__ void __launch_bounds__(kDecThreads + 32)
           make_float2(oacc[nt][2] * f1, oacc[nt][3] * f1);
     }
     if (!meet(1, n - 1)) break;
-    __nv_bfloat16* out = p.part.o + sel * G * kHeadDim;
-    for (int i = threadIdx.x * 8; i < 16 * 128; i += kDecThreads * 8) {
+    __nv_bfloat16* out = p.part.o + (sel * G + hs * 16) * kHeadDim;
+    for (int i = threadIdx.x * 8; i < rows * 128; i += kDecThreads * 8) {
       const int at = (i >> 7) * kOsumStride + (i & 127);  // head i / 128, column i % 128
       float acc[8];
 #pragma unroll
@@ -562,7 +641,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       v.w = pack_bf16x2(acc[6], acc[7]);
       *reinterpret_cast<uint4*>(out + i) = v;
     }
-    if (threadIdx.x < 16) {
+    if (threadIdx.x < rows) {
       const int h = threadIdx.x;
       float M = -INFINITY;
       for (int w = 0; w < 4; ++w) M = fmaxf(M, red[(w * 16 + h) * 2]);
@@ -572,8 +651,8 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         if (mw != -INFINITY) L += red[(w * 16 + h) * 2 + 1] * exp2f(mw - M);
       }
       const float lse = (M == -INFINITY) ? -INFINITY : (M + log2f(L)) * kLn2;
-      p.part.lse[sel * G + h] = lse;
-      p.part.ow[sel * G + h] = lse;  // o is stored normalised
+      p.part.lse[sel * G + hs * 16 + h] = lse;
+      p.part.ow[sel * G + hs * 16 + h] = lse;  // o is stored normalised
     }
     if (!meet(2, n - 1)) break;  // red and osum are reused by the next item
   }
@@ -582,14 +661,17 @@ __global__ void __launch_bounds__(kDecThreads + 32)
 size_t decode_attn_smem_bytes() { return kDecSmemBytes; }
 
 cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeAttnParams& p, cudaStream_t stream) {
-  const long long items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk;
+                               const DecodeAttnParams& p, bool fp8, cudaStream_t stream) {
+  const long long items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk * (p.group >= 16 ? p.group / 16 : 1);
   if (items == 0) return cudaSuccess;
-  const long long grid = items < 2LL * p.sms ? items : 2LL * p.sms;  // persistent: two CTAs per SM
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kDecSmemBytes));
+  // persistent: two CTAs per SM (one with the fp8 staging area)
+  const long long per_sm = fp8 ? 1 : 2;
+  const long long grid = items < per_sm * p.sms ? items : per_sm * p.sms;
+  const size_t smem = kDecSmemBytes + (fp8 ? kDec8Staging : 0);
+  auto* fn = fp8 ? decode_attn_kernel<true> : decode_attn_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  decode_attn_kernel<<<static_cast<unsigned>(grid), kDecThreads + 32, kDecSmemBytes, stream>>>(tq, tk, tv, p);
+  fn<<<static_cast<unsigned>(grid), kDecThreads + 32, smem, stream>>>(tq, tk, tv, p);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -107,6 +107,10 @@ cudaError_t launch_v_prep(const __nv_bfloat16* v, __half* v16, long long n_elems
 // Main Branch work item: at most this many tiles (of qpt <= 16 queries each).
 constexpr int kTilesPerChunk = 16;
 
+// A schedule entry packs one incidence as (query << kSlotBits) | slot (slot < topk <= 64).
+constexpr int kSlotBits = 6;
+constexpr int kSlotMask = (1 << kSlotBits) - 1;
+
 struct ScheduleParams {
   int num_seqs, total_q, hkv, topk, window, total_blocks, n_windows, qpc;
   const int32_t* cu_q;
@@ -118,7 +122,7 @@ struct ScheduleParams {
   int32_t* cursor;        // [n_buckets]
   int32_t* nchunk;        // [n_buckets]
   int32_t* chunk_start;   // [n_buckets + 1]
-  int32_t* entries;       // [total_q * hkv * topk]
+  int32_t* entries;       // [total_q * hkv * topk]: (query << kSlotBits) | slot
   int4* chunks;           // [max_chunks] (begin, count, g | block << 8, seq)
   int32_t* scan_tmp;
   WsHeader* hdr;
@@ -135,6 +139,11 @@ struct AttnParams {
   WsHeader* hdr;
   int hkv, group, topk, qpt;
   float scale_log2;       // softmax scale * log2(e)
+  // fp8 K/V (tk / tv then map the 16-bit copies of the codes): scales [n_key_blocks, hkv], first key block of
+  // each sequence; null for bf16 K/V
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* blk_off;
 };
 size_t sparse_attn_smem_bytes();
 cudaError_t launch_sparse_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -145,16 +154,57 @@ struct DecodeAttnParams {
   int sms;                 // persistent grid size
   const SeqInfo* seq;
   const int32_t* idx;      // [num_seqs, hkv, topk]
-  PartialBuffers part;     // Q [num_seqs, hq, 128] comes through a tensor map (16 heads x 64 dims boxes)
+  PartialBuffers part;     // Q [num_seqs, hq, 128] comes through a tensor map (min(G, 16) heads x 64 dims boxes)
   float scale_log2;
   WsHeader* hdr;
   const int32_t* block_table;  // as in DecodeScanParams
   int bt_stride;
   long long n_pages;
+  // fp8 K/V (launch with fp8 = true; tk / tv then map E4M3 codes): scales [n_key_blocks, hkv] and the first key
+  // block of each sequence
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* blk_off;
 };
 size_t decode_attn_smem_bytes();
 cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeAttnParams& p, cudaStream_t stream);
+                               const DecodeAttnParams& p, bool fp8, cudaStream_t stream);
+
+// ---------------------------------------------------------------- index prologue
+// Hidden states -> Q_idx and the new tokens' K_idx rows (projection, RMSNorm, RoPE on dims 0..63).
+struct PrologueParams {
+  int num_seqs, total_q, hkv, d_model, n_row_tiles;
+  const int32_t* cu_q;
+  const SeqInfo* seq;
+  const __nv_bfloat16* gamma_q;  // [128]
+  const __nv_bfloat16* gamma_k;  // [128]
+  __nv_bfloat16* q_idx;          // [total_q, hkv, 128]
+  __nv_bfloat16* k_idx;          // [total_k, 128]: row k_start + pos(i) of token i
+  double rope_turns[32];         // theta_j / (2 pi), theta_j = 10000^(-j/32)
+  WsHeader* hdr;
+};
+size_t index_prologue_smem_bytes();
+cudaError_t launch_index_prologue(const CUtensorMap& tx, const CUtensorMap& twq, const CUtensorMap& twk,
+                                  const PrologueParams& p, int sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- fp8 K/V
+// Quantization of bf16 K and V to E4M3 codes with one scale per (key block, KV head).
+struct QuantParams {
+  int num_seqs, hkv;
+  const SeqInfo* seq;
+  const int32_t* blk_off;       // [num_seqs + 1] first key block of each sequence (plan)
+  const __nv_bfloat16* k;       // [total_k, hkv, 128]
+  const __nv_bfloat16* v;
+  uint8_t* k8;                  // [total_k, hkv, 128] E4M3 codes
+  uint8_t* v8;
+  float* k_scale;               // [n_key_blocks, hkv]
+  float* v_scale;
+  WsHeader* hdr;
+};
+cudaError_t launch_quantize_kv_fp8(const QuantParams& p, long long max_blocks, cudaStream_t stream);
+// 16-bit copies of fp8 K (bf16) and V (fp16) for the prefill Main Branch; exact.
+cudaError_t launch_kv8_widen(const uint8_t* k8, const uint8_t* v8, __nv_bfloat16* k16, __half* v16,
+                             long long n_elems, const WsHeader* hdr, int sms, cudaStream_t stream);
 
 struct CombineParams {
   int total_q, hq, hkv, group, topk, num_seqs;

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kSchedThreads) sched_fill_kernel(ScheduleParam
   for_each_incidence(p, cq, [&](int bucket, int i, int slot) {
     const int h = table_find(t, bucket);
     const int at = h >= 0 ? atomicAdd(&t.val[h], 1) : p.bucket_start[bucket] + atomicAdd(&p.cursor[bucket], 1);
-    p.entries[at] = (i << 5) | slot;
+    p.entries[at] = (i << kSlotBits) | slot;
   });
 }
 

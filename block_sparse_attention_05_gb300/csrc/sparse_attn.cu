@@ -23,6 +23,9 @@
 //                             fp16 copy of V, MN-major in smem
 //   U / l, LSE, log weight    written per (query, group, slot, head); the log
 //                             weight W = LSE + e ln 2 undoes V's 2^-e scale
+// fp8 K/V (E4M3 codes with one scale per key block and KV head) run on exact
+// 16-bit copies of the codes: the tile's K scale multiplies its logits and the
+// log of its V scale is added to the log weight.
 // The tile covers exactly one key block, so no running rescale of U is needed.
 //
 // Warp roles (512 threads): warp 0 = producer (chunk claiming, K and Q
@@ -122,8 +125,8 @@ __device__ __forceinline__ RowInfo row_info(const AttnParams& p, const ChunkInfo
   if (e < ci.begin + ci.count) {
     const int ent = p.entries[e];
     ri.valid = true;
-    ri.qi = ent >> 5;
-    ri.slot = ent & 31;
+    ri.qi = ent >> kSlotBits;
+    ri.slot = ent & kSlotMask;
     const SeqInfo si = p.seq[ci.s];
     const int pos = si.kv_len - si.q_len + (ri.qi - si.q_start);
     ri.lim = pos - ci.b * kBlock;  // keys 0..lim of this block are visible
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto prefetch_q = [&](const ChunkInfo& c, int buf, int tt) {
       const int e = tt * p.qpt + lane;
       if (lane < p.qpt && e < c.count) {
-        const int qi = sm.ent[buf][e] >> 5;
+        const int qi = sm.ent[buf][e] >> kSlotBits;
         bulk_prefetch_l2(p.q + (static_cast<int64_t>(qi) * p.hkv + c.g) * G * kHeadDim, G * kHeadDim * 2);
       }
     };
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (lane < p.qpt) {  // one lane per query of the tile
           int e = tt * p.qpt + lane;
           if (e >= ci.count) e = 0;  // pad the last tile with a real row
-          const int qg = (sm.ent[buf][e] >> 5) * p.hkv + ci.g;
+          const int qg = (sm.ent[buf][e] >> kSlotBits) * p.hkv + ci.g;
           tma_load_5d(q_buf + qs * kQTileBytes + lane * G * 256, &tm_q, &sm.q_full[qs], qg);
         }
         ++q_iter;
@@ -469,6 +472,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (lane == 0) mbar_arrive(&sm.work_empty[slot]);
       ++w_iter;
       if (item < 0) break;
+      // the tile's logit scale and the log of V's scale: fp8 K/V carry one scale per (key block, KV head),
+      // a bf16 V copy the power of two 2^v_shift
+      float sc_log2 = p.scale_log2, lnv = v_shift * kLn2;
+      if (p.k_scale) {
+        const long long srow = (static_cast<long long>(p.blk_off[ci.s]) + ci.b) * p.hkv + ci.g;
+        sc_log2 *= p.k_scale[srow];
+        lnv = logf(p.v_scale[srow]);
+      }
       for (int tt = 0; tt < ci.ntile; ++tt, ++t) {
         if ((t & 1) != static_cast<uint32_t>(wg)) continue;
         const uint32_t n = t >> 1;
@@ -509,20 +520,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float cm = fmaxf(fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
                                          fmax3(t8[6], t8[7], t8[8])),
                                    fmaxf(t8[9], t8[10]));
-            if (c == 0) m_ref = (cm == -INFINITY) ? 0.f : cm * p.scale_log2;
+            if (c == 0) m_ref = (cm == -INFINITY) ? 0.f : cm * sc_log2;
             // The rescale uses warp-collective TMEM loads and stores, so the
             // whole warp enters it when any of its rows needs it; the other rows
             // scale by exactly 1.
-            const bool need = cm != -INFINITY && cm * p.scale_log2 - m_ref > 15.f;
+            const bool need = cm != -INFINITY && cm * sc_log2 - m_ref > 15.f;
             if (__any_sync(0xFFFFFFFFu, need)) {
-              const float kexp = need ? ceilf(cm * p.scale_log2 - m_ref) : 0.f;
+              const float kexp = need ? ceilf(cm * sc_log2 - m_ref) : 0.f;
               const float f = exp2f(-kexp);
               rescale_p(lane_addr, 2 * c, f);
               l2.x *= f;
               l2.y *= f;
               m_ref += kexp;
             }
-            const float2 sc = make_float2(p.scale_log2, p.scale_log2), nm = make_float2(-m_ref, -m_ref);
+            const float2 sc = make_float2(sc_log2, sc_log2), nm = make_float2(-m_ref, -m_ref);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t pk[8];
@@ -585,7 +596,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const bool empty = lim < 0;
           const float lse2 = m_ref + log2f(l);
           p.part.lse[at] = empty ? -INFINITY : lse2 * kLn2;
-          p.part.ow[at] = empty ? -INFINITY : (lse2 + v_shift) * kLn2;
+          p.part.ow[at] = empty ? -INFINITY : lse2 * kLn2 + lnv;
         }
       }
     }

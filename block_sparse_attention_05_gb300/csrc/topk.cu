@@ -11,6 +11,10 @@
 // One CTA of W warps per row.  Warp w scans a contiguous slice of the row, each
 // lane keeping the CAP best (score, block) keys of its strided subset; k-1
 // rounds of warp max extract the warp's best k-1; warp 0 merges the W lists.
+// That needs registers for k-1 keys per lane, so it serves k <= 16; larger k
+// (up to 64) take topk_radix_kernel below: a radix selection of the (k-1)-th
+// best key, eight bits of the 64-bit key per pass over the row, then every
+// key at or above it, written in block order by a compaction scan.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -85,11 +89,122 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
     write_selection<CAP>(p.idx + static_cast<int64_t>(row) * p.topk, p.topk, chosen, local);
 }
 
+constexpr int kRadixThreads = 256;
+
+// Selection of one row by radix select.  The candidates are the non-local
+// causal blocks b < local; want = min(k - 1, local) of them are kept.  Keys
+// are distinct (they embed the block index), so the want-th largest key T is
+// unique and the kept set is exactly {b : key(b) >= T}.  Each pass takes the
+// next 8 bits of T: a histogram of that byte over the keys that agree with T
+// on the bytes already fixed, then the byte whose bin holds the rank still
+// wanted.  When that bin holds exactly the rank still wanted, every key in it
+// is kept and the remaining bytes need not be fixed.
+__global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p) {
+  __shared__ uint32_t hist[256];
+  __shared__ int s_digit, s_rem, s_exact;
+  __shared__ int s_warp_tot[kRadixThreads / 32];
+  if (p.hdr->status & kFlagBadSeqlens) return;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 511)) return;
+  const int i = row / p.hkv;
+  const int s = find_seq(p.cu_q, p.num_seqs, i);
+  const SeqInfo si = p.seq[s];
+  const int pos = si.kv_len - si.q_len + (i - si.q_start);
+  const int local = pos >> 7;  // also the number of non-local causal blocks
+  const int want = min(p.topk - 1, local);
+  if (!index_ok(p.hdr, local, p.max_nb, 512)) return;
+  const float* pr = p.pooled + static_cast<int64_t>(row) * p.pooled_stride;
+
+  uint64_t prefix = 0, mask = 0;
+  if (want > 0 && want < local) {
+    int remaining = want;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int h = tid; h < 256; h += kRadixThreads) hist[h] = 0u;
+      __syncthreads();
+      for (int b = tid; b < local; b += kRadixThreads) {
+        const uint64_t key = topk_key(pr[b], b);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane l holds bins 255 - 8l .. 248 - 8l (descending); counts above each lane by a shuffle scan
+        uint32_t c[8];
+        uint32_t tot = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[255 - 8 * lane - j];
+          tot += c[j];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t above = incl - tot;  // keys in bins above this lane's
+        const bool here = above < static_cast<uint32_t>(remaining) && incl >= static_cast<uint32_t>(remaining);
+        if (here) {
+          uint32_t cum = above;
+          int j = 0;
+          while (cum + c[j] < static_cast<uint32_t>(remaining)) cum += c[j++];
+          s_digit = 255 - 8 * lane - j;
+          s_rem = remaining - static_cast<int>(cum);
+          s_exact = (c[j] == static_cast<uint32_t>(remaining) - cum) ? 1 : 0;
+        }
+      }
+      __syncthreads();
+      const int d = s_digit;
+      remaining = s_rem;
+      const bool exact = s_exact != 0;
+      __syncthreads();  // every thread has read the decision before the next pass clears the histogram
+      prefix |= static_cast<uint64_t>(d) << shift;
+      mask |= static_cast<uint64_t>(0xFFu) << shift;
+      if (exact) break;
+    }
+  }
+
+  // kept blocks, written in ascending order: thread t owns the contiguous blocks [t * per, (t + 1) * per)
+  const int per = (local + kRadixThreads - 1) / kRadixThreads;
+  const int lo = tid * per, hi = min(local, lo + per);
+  auto kept = [&](int b) {
+    if (want == 0) return false;
+    return (topk_key(pr[b], b) & mask) >= prefix;
+  };
+  int cnt = 0;
+  for (int b = lo; b < hi; ++b) cnt += kept(b) ? 1 : 0;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_warp_tot[warp] = incl;
+  __syncthreads();
+  int base = incl - cnt;
+  for (int w = 0; w < warp; ++w) base += s_warp_tot[w];
+  int32_t* out = p.idx + static_cast<int64_t>(row) * p.topk;
+  for (int b = lo; b < hi; ++b)
+    if (kept(b)) {
+      if (index_ok(p.hdr, base, p.topk - 1, 513)) out[base] = b;
+      ++base;
+    }
+  if (tid == 0) {
+    out[want] = local;
+    for (int j = want + 1; j < p.topk; ++j) out[j] = -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk_pooled(const TopkParams& p, int max_nb, cudaStream_t stream) {
   const int rows = p.total_q * p.hkv;
   if (rows == 0) return cudaSuccess;
+  if (p.topk > 16) {
+    topk_radix_kernel<<<rows, kRadixThreads, 0, stream>>>(p);
+    note_launches(1);
+    return cudaGetLastError();
+  }
   int warps = max_nb / 256;
   warps = warps < 1 ? 1 : (warps > kTopkMaxWarps ? kTopkMaxWarps : warps);
   const dim3 grid(rows), block(32 * warps);

@@ -40,10 +40,20 @@
  * Every tensor pointer must be 16-byte aligned; the workspace 256-byte aligned.
  *
  * Supported shapes: head_dim = 128, block_size = 128, index_dim in {64, 128},
- * 1 <= topk <= 16, num_kv_heads dividing 128, group size num_q_heads /
- * num_kv_heads a power of two in [8, 128]; decode batches also need
- * num_kv_heads <= 8 and a group size of 16.  Other values return
- * MSA_ERR_UNSUPPORTED.
+ * 1 <= topk <= 64, num_kv_heads dividing 128, group size num_q_heads /
+ * num_kv_heads a power of two in [8, 128], total_q < 2^25; decode batches
+ * also need num_kv_heads <= 8.  Other values return MSA_ERR_UNSUPPORTED.
+ *
+ * Size of a prefill call: the workspace holds one partial output per (query,
+ * group, selected block) until the combine, so it grows with total_q * topk:
+ * about total_q * num_q_heads * topk * 264 bytes, plus total_k * num_kv_heads
+ * * 256 bytes (an fp16 copy of V) and the schedule (msa_workspace_size gives
+ * the exact figure).  At 64 query / 4 KV heads and topk 16 that is about 270 KB
+ * per query row: 35 GB for a 131,072-query prefill, so one call on a 288 GB
+ * GB300 takes up to roughly 1M query rows with nothing else resident.  Longer
+ * prefills go in chunks of queries (each call's sequences with q_len <
+ * kv_len: the queries are the last q_len positions), which select and attend
+ * exactly as one call would.
  *
  * Execution: every call validates its arguments on the host, then enqueues
  * kernels on `stream` and returns without synchronising.  Nothing is
@@ -97,7 +107,7 @@ typedef struct msa_problem {
   int32_t head_dim;              /* 128 */
   int32_t index_dim;             /* 64 or 128 */
   int32_t block_size;            /* 128 */
-  int32_t topk;                  /* 1..16, counts the local block */
+  int32_t topk;                  /* 1..64, counts the local block */
   float softmax_scale;           /* <= 0 selects 1/sqrt(head_dim) */
 } msa_problem_t;
 
@@ -107,7 +117,12 @@ typedef enum msa_op {
   MSA_OP_SPARSE_ATTN_PREFILL = 3,/* msa_sparse_attn_prefill */
   MSA_OP_SPARSE_ATTN_DECODE = 4, /* msa_sparse_attn_decode */
   MSA_OP_FORWARD = 5,            /* msa_forward */
-  MSA_OP_TOPK_POOLED = 6         /* msa_topk_pooled */
+  MSA_OP_TOPK_POOLED = 6,        /* msa_topk_pooled */
+  MSA_OP_QUANTIZE_KV_FP8 = 7,    /* msa_quantize_kv_fp8 */
+  MSA_OP_SPARSE_ATTN_PREFILL_FP8 = 8, /* msa_sparse_attn_prefill_fp8 */
+  MSA_OP_SPARSE_ATTN_DECODE_FP8 = 9,  /* msa_sparse_attn_decode_fp8 */
+  MSA_OP_FORWARD_FP8 = 10,       /* msa_forward_fp8 */
+  MSA_OP_INDEX_PROLOGUE = 11     /* msa_index_prologue */
 } msa_op_t;
 
 /* Workspace bytes that `op` needs for `problem` (host-only; no CUDA call).
@@ -148,8 +163,14 @@ msa_status_t msa_sparse_attn_prefill(const msa_problem_t *problem, const void *q
                                      void *workspace, size_t workspace_bytes,
                                      msa_stream_t stream);
 
-/* Main Branch for decode batches (every q_len == 1): split over the selected
- * blocks, then a log-sum-exp combine.  Same arguments as the prefill call. */
+/* Main Branch for decode batches (every q_len == 1): "MiniMax Sparse
+ * Attention: let each query pick its own blocks", section "The mechanism,
+ * precisely", second bullet -- exact attention of the one new query of each
+ * sequence (at pos = kv_len - 1) over the blocks in idx; the groundtruth.day
+ * article on the llama.cpp merge ("Key facts") gives the effect: about 2,048
+ * KV tokens read per decode step whatever the context length.  Split over the
+ * selected blocks (one partial result per (sequence, group, block)), then a
+ * log-sum-exp combine.  Same arguments and results as the prefill call. */
 msa_status_t msa_sparse_attn_decode(const msa_problem_t *problem, const void *q, const void *k,
                                     const void *v, const int32_t *idx, void *o, float *lse,
                                     void *workspace, size_t workspace_bytes,
@@ -173,17 +194,24 @@ msa_status_t msa_sparse_attn_decode(const msa_problem_t *problem, const void *q,
  * return MSA_ERR_WORKSPACE, and msa_last_error_detail() states the bytes
  * needed and available.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress, with that device current) and caches
- * it; make that first call before any stream capture.  Every call uses the
+ * it; make that first call before any stream capture.  The cached address
+ * belongs to the context it was looked up in: after a device reset (a new
+ * primary context) the next call looks it up again.  Every call uses the
  * same array and leaves its contents behind (each call clears what must start
  * at zero), so calls whose kernels may overlap on the GPU -- on different
  * streams, or from several host threads -- race and must be serialised by the
- * caller. */
+ * caller.  Device-side errors of a call (MSA_DEVICE_* flags) are kept in the
+ * array's header: read them with msa_read_device_status(NULL, ...). */
 msa_status_t msa_sparse_attn_decode_static(const msa_problem_t *problem, const void *q,
                                            const void *k, const void *v, const int32_t *idx,
                                            void *o, float *lse, msa_stream_t stream);
 
-/* Both branches: msa_index_topk then the matching Main Branch call.  Writes
- * idx (the selection), o and lse. */
+/* The whole MSA layer forward ("MiniMax Sparse Attention: let each query pick
+ * its own blocks", section "The mechanism, precisely", both bullets, and
+ * Figure 1: Index Branch -> top-k block indices -> Main Branch):
+ * msa_index_topk, then msa_sparse_attn_prefill, or msa_sparse_attn_decode when
+ * every q_len is 1, on one workspace (size: op MSA_OP_FORWARD).  Writes idx
+ * (the selection), o and lse. */
 msa_status_t msa_forward(const msa_problem_t *problem, const void *q, const void *k,
                          const void *v, const void *q_idx, const void *k_idx, int32_t *idx,
                          void *o, float *lse, void *workspace, size_t workspace_bytes,
@@ -221,8 +249,83 @@ msa_status_t msa_forward_decode_paged(const msa_problem_t *problem, const void *
                                       int64_t num_pages, int32_t *idx, void *o, float *lse,
                                       void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/* Index prologue: hidden states -> index heads ("MiniMax Sparse Attention:
+ * let each query pick its own blocks", Figure 1: the Index Branch takes the
+ * hidden states through a linear projection, a norm and RoPE to the index
+ * query and key heads; the atlas record gives d_model 3072 and a RoPE
+ * dimension of 64 on 128-dim heads, and names no norm).  For every new token
+ * (query row i at key position pos(i)):
+ *   y_h = W_q[h] x_i (h < num_kv_heads), y_k = W_k x_i      (fp32 accumulation)
+ *   z = y / sqrt(mean(y^2) + 1e-6) * gamma   per head (gamma_q for the index
+ *       query heads, gamma_k for the key head)
+ *   RoPE on dims 0..63: pairs (j, j + 32) rotated by pos(i) * 10000^(-j/32)
+ *   Q_idx[i, h, :] = z_h;  K_idx[k_start + pos(i), :] = z_k   (bf16)
+ * so a prefill writes its tokens' rows of the index-key cache and a decode
+ * step appends one row per sequence.
+ *   x        [total_q, d_model] bf16; d_model a multiple of 64 (at most 65536)
+ *   w_q      [num_kv_heads * 128, d_model] bf16 (a linear layer's weight)
+ *   w_k      [128, d_model] bf16
+ *   gamma_q, gamma_k  [128] bf16
+ *   q_idx    [total_q, num_kv_heads, 128] bf16 (written)
+ *   k_idx    [total_k, 128] bf16 (the new tokens' rows written, others kept)
+ * Needs index_dim = 128 (else MSA_ERR_UNSUPPORTED); workspace: op
+ * MSA_OP_INDEX_PROLOGUE.  Pointers 16-byte aligned (gamma 2-byte). */
+msa_status_t msa_index_prologue(const msa_problem_t *problem, const void *x, int32_t d_model, const void *w_q,
+                                const void *w_k, const void *gamma_q, const void *gamma_k, void *q_idx,
+                                void *k_idx, void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8 K and V.  The atlas record of the report (provenance of section 4.2)
+ * says the kernels "also support fp8" and gives no format; this library reads
+ * it as OCP E4M3 codes ("E4M3FN": bias 7, 3 mantissa bits, largest finite
+ * 448, no infinities) with one fp32 scale per (key block of 128 tokens of a
+ * sequence, KV head), for K and for V separately:
+ *   scale = max |x| over the block's rows of that head / 448 (1 when 0),
+ *   code  = round-to-nearest-even(x / scale) in fp32, saturated to +-448,
+ *   value = code * scale.
+ *   k8, v8            [total_k, num_kv_heads, 128] uint8 codes, 16-byte aligned
+ *   k_scale, v_scale  [n_key_blocks, num_kv_heads] fp32, 4-byte aligned, where
+ *                     n_key_blocks = sum over sequences of ceil(kv_len / 128)
+ *                     (at most total_k / 128 + num_seqs); key block b of
+ *                     sequence s is row (key blocks of sequences 0..s-1) + b.
+ * The Index Branch stays bf16 (a quantized index selects other blocks).  The
+ * fp8 Main Branch computes exactly the bf16 one over the dequantized values
+ * (value = code * scale); results differ from bf16 K/V by the quantization.
+ * Decode reads the codes directly (half the K/V bytes); prefill widens them
+ * once per call into exact 16-bit copies in the workspace.  Paged caches are
+ * bf16 only.
+ * ------------------------------------------------------------------------ */
+
+/* bf16 K and V -> E4M3 codes and scales as above (msa_workspace_size op
+ * MSA_OP_QUANTIZE_KV_FP8).  Only the rows of the sequences' key blocks are
+ * written. */
+msa_status_t msa_quantize_kv_fp8(const msa_problem_t *problem, const void *k, const void *v, void *k8, void *v8,
+                                 float *k_scale, float *v_scale, void *workspace, size_t workspace_bytes,
+                                 msa_stream_t stream);
+
+/* msa_sparse_attn_prefill over fp8 K and V (op MSA_OP_SPARSE_ATTN_PREFILL_FP8). */
+msa_status_t msa_sparse_attn_prefill_fp8(const msa_problem_t *problem, const void *q, const void *k8,
+                                         const void *v8, const float *k_scale, const float *v_scale,
+                                         const int32_t *idx, void *o, float *lse, void *workspace,
+                                         size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_sparse_attn_decode over fp8 K and V (op MSA_OP_SPARSE_ATTN_DECODE_FP8). */
+msa_status_t msa_sparse_attn_decode_fp8(const msa_problem_t *problem, const void *q, const void *k8,
+                                        const void *v8, const float *k_scale, const float *v_scale,
+                                        const int32_t *idx, void *o, float *lse, void *workspace,
+                                        size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_forward with fp8 K and V for the Main Branch and bf16 Q_idx / K_idx for
+ * the Index Branch (op MSA_OP_FORWARD_FP8). */
+msa_status_t msa_forward_fp8(const msa_problem_t *problem, const void *q, const void *k8, const void *v8,
+                             const float *k_scale, const float *v_scale, const void *q_idx, const void *k_idx,
+                             int32_t *idx, void *o, float *lse, void *workspace, size_t workspace_bytes,
+                             msa_stream_t stream);
+
 /* Waits for `stream`, then returns in *flags the MSA_DEVICE_* bits that the
- * last call on this workspace raised (0 = none).  The only synchronising call. */
+ * last call on this workspace raised (0 = none).  workspace = NULL reads the
+ * flags of the last msa_sparse_attn_decode_static call on the current device.
+ * The only synchronising call. */
 msa_status_t msa_read_device_status(const void *workspace, uint32_t *flags, msa_stream_t stream);
 
 /* Stages of a call, for msa_set_stage_events. */

@@ -57,7 +57,7 @@ def ws_size(msa, prob, op):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(topk=17), -2), (dict(topk=0), -1), (dict(head_dim=64), -2), (dict(block_size=64), -2),
+    (dict(topk=65), -2), (dict(topk=0), -1), (dict(head_dim=64), -2), (dict(block_size=64), -2),
     (dict(index_dim=96), -2), (dict(num_q_heads=62), -1), (dict(num_q_heads=60), -2), (dict(num_q_heads=12, num_kv_heads=4), -2),
     (dict(num_kv_heads=3, num_q_heads=48), -2), (dict(num_seqs=0), -1), (dict(cu_seqlens_q=None), -1),
     (dict(total_q=-1), -1), (dict(max_seqlen_k=2048), -1), (dict(softmax_scale=float("nan")), -1),
@@ -65,6 +65,12 @@ def ws_size(msa, prob, op):
 def test_invalid_problems_are_rejected(msa, kw, status):
     st, _ = ws_size(msa, base_problem(msa, **kw), msa.Op.FORWARD)
     assert st == status
+
+
+@pytest.mark.parametrize("topk", [1, 16, 17, 32, 64])
+def test_topk_range_is_accepted(msa, topk):
+    st, n = ws_size(msa, base_problem(msa, topk=topk), msa.Op.FORWARD)
+    assert st == 0 and n >= 1024 * 4 * topk * 16 * 128 * 2
 
 
 def test_workspace_sizes_grow_with_the_problem(msa):
@@ -97,8 +103,8 @@ def test_calls_reject_bad_arguments_before_touching_the_device(msa):
     assert lib.msa_sparse_attn_decode(p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None) == -1
     # pooled stride too small
     assert lib.msa_index_pool(p, FAKE, FAKE, FAKE, 7, FAKE, 1 << 40, None) == -1
-    # decode path with a group size the decode kernel does not take
-    dec = base_problem(msa, num_seqs=4, total_q=4, max_seqlen_q=1, num_q_heads=32)
+    # decode path with more index heads than the decode scan takes (8)
+    dec = base_problem(msa, num_seqs=4, total_q=4, max_seqlen_q=1, num_q_heads=128, num_kv_heads=16)
     assert lib.msa_forward(ctypes.byref(dec), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40,
                            None) == -2
 

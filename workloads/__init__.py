@@ -6,6 +6,6 @@ without sharing any computation.  See ``configs.py`` for the shapes and
 ``generate.py`` for the recipe.
 """
 from .configs import CONFIGS, Workload, get
-from .generate import Inputs, generate
+from .generate import Inputs, PrologueInputs, generate, prologue_inputs
 
-__all__ = ["CONFIGS", "Workload", "get", "Inputs", "generate"]
+__all__ = ["CONFIGS", "Workload", "get", "Inputs", "PrologueInputs", "generate", "prologue_inputs"]

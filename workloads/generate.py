@@ -112,3 +112,29 @@ def generate(cfg: Workload, device="cpu") -> Inputs:
     k = _normal_bf16((N, cfg.hkv, cfg.head_dim), gen, device)
     v = _normal_bf16((N, cfg.hkv, cfg.head_dim), gen, device)
     return Inputs(cfg, q, k, v, q_idx, k_idx, cu_q.to(device), cu_k.to(device), seqs)
+
+
+@dataclasses.dataclass
+class PrologueInputs:
+    x: torch.Tensor        # [T, d_model] bf16 hidden states of the new tokens
+    w_q: torch.Tensor      # [hkv * d_idx, d_model] bf16
+    w_k: torch.Tensor      # [d_idx, d_model] bf16
+    gamma_q: torch.Tensor  # [d_idx] bf16
+    gamma_k: torch.Tensor  # [d_idx] bf16
+
+
+def prologue_inputs(total_q: int, hkv: int, d_idx: int = 128, d_model: int = 3072, seed: int = 2000,
+                    device="cpu") -> PrologueInputs:
+    """Synthetic index-projection inputs (no trained weights exist here): hidden states N(0, 1), projection
+    weights N(0, 1 / d_model) so the projected heads are about N(0, 1), norm weights 1 + 0.1 N(0, 1); all
+    rounded to bf16, drawn from one seeded generator in this order."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    x = _normal_bf16((total_q, d_model), gen, device)
+    std = d_model ** -0.5
+    w_q = (torch.randn((hkv * d_idx, d_model), generator=gen, device=device) * std).to(torch.bfloat16)
+    w_k = (torch.randn((d_idx, d_model), generator=gen, device=device) * std).to(torch.bfloat16)
+    gamma_q = (1 + 0.1 * torch.randn((d_idx,), generator=gen, device=device)).to(torch.bfloat16)
+    gamma_k = (1 + 0.1 * torch.randn((d_idx,), generator=gen, device=device)).to(torch.bfloat16)
+    return PrologueInputs(x, w_q, w_k, gamma_q, gamma_k)
