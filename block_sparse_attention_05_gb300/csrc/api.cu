@@ -158,7 +158,7 @@ Layout layout(const Derived& d, msa_op_t op) {
     if (op_is_fp8(op)) L.k16 = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.N) * d.hkv * kHeadDim);
   }
   if (op_uses_prefill_attn(op, d) || op_uses_decode_attn(op, d)) {
-    L.part_o = take(sizeof(__nv_bfloat16) * static_cast<size_t>(d.n_inc) * d.G * kHeadDim);
+    L.part_o = take(sizeof(uint16_t) * static_cast<size_t>(d.n_inc) * d.G * kHeadDim);
     L.part_lse = take(sizeof(float) * static_cast<size_t>(d.n_inc) * d.G);
     L.part_ow = take(sizeof(float) * static_cast<size_t>(d.n_inc) * d.G);
   }
@@ -436,13 +436,14 @@ msa_status_t run_index_select_prefill(const msa_problem_t* p, Ctx& c, const void
 
 PartialBuffers partials(Ctx& c) {
   PartialBuffers pb;
-  pb.o = at<__nv_bfloat16>(c.ws, c.L.part_o);
+  pb.o = at<uint16_t>(c.ws, c.L.part_o);
   pb.lse = at<float>(c.ws, c.L.part_lse);
   pb.ow = at<float>(c.ws, c.L.part_ow);
   return pb;
 }
 
-msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, void* o, float* lse) {
+msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, void* o, float* lse,
+                         bool f16_partials) {
   CombineParams cp{};
   cp.total_q = c.d.T;
   cp.hq = c.d.hq;
@@ -459,7 +460,7 @@ msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, voi
   cp.lse = lse;
   cp.hdr = c.hdr;
   StageScope scope(MSA_STAGE_COMBINE, c.stream);
-  return cuda_status(launch_combine(cp, c.stream));
+  return cuda_status(launch_combine(cp, f16_partials, c.stream));
 }
 
 msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, const void* k, const void* v,
@@ -529,7 +530,7 @@ msa_status_t run_attn_prefill(const msa_problem_t* p, Ctx& c, const void* q, con
     if (st == MSA_OK) st = cuda_status(launch_sparse_attn(tq, tk, tv, ap, c.dev.sms, c.stream));
   }
   if (st != MSA_OK) return st;
-  return run_combine(p, c, idx, o, lse);
+  return run_combine(p, c, idx, o, lse, true);
 }
 
 msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, const void* k, const void* v,
@@ -563,7 +564,7 @@ msa_status_t run_attn_decode(const msa_problem_t* p, Ctx& c, const void* q, cons
     st = cuda_status(launch_decode_attn(tq, tk, tv, dp, c.fp8, c.stream));
   }
   if (st != MSA_OK) return st;
-  return run_combine(p, c, idx, o, lse);
+  return run_combine(p, c, idx, o, lse, false);
 }
 
 }  // namespace

@@ -56,7 +56,8 @@ __device__ __forceinline__ PairRef pair_ref(const CombineParams& p, int64_t pair
 
 // NG groups of 16 slots (topk <= 16 NG): lane hl of a half-warp holds slots hl, hl + 16, ... for the
 // log-sum-exp, and the partial rows are loaded and accumulated 16 slots at a time.
-template <int NG>
+// F16: the partial rows are fp16 (prefill), else bf16 (decode).
+template <int NG, bool F16>
 __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineParams p) {
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -71,7 +72,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
 #pragma unroll
       for (int j = 0; j < NG; ++j)
         if (hl + 16 * j < p.topk) {
-          const __nv_bfloat16* row = p.part.o + ((nx.sel_base + hl + 16 * j) * p.group + nx.hh) * kHeadDim;
+          const uint16_t* row = p.part.o + ((nx.sel_base + hl + 16 * j) * p.group + nx.hh) * kHeadDim;
           prefetch_l2(row);
           prefetch_l2(row + 64);
         }
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
         w_s[j] = p.part.ow[(sel_base + sl) * p.group + hh];
       }
     }
-    const __nv_bfloat16* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
+    const uint16_t* base = p.part.o + (sel_base * p.group + hh) * kHeadDim + hl * 8;
     uint4 raw[16];
 #pragma unroll
     for (int sl = 0; sl < 16; ++sl)
@@ -124,8 +125,9 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
 #pragma unroll
     for (int j = 0; j < NG; ++j) w[j] = valid[j] ? expf(w_s[j] - L) : 0.f;
 
-    // acc[j] holds columns 2j, 2j + 1: one packed fma per bf16 pair (the same single rounding per
-    // element as two scalar fmas); a bf16 widens to fp32 by moving its bits to the high half
+    // acc[j] holds columns 2j, 2j + 1: one packed fma per 16-bit pair (the same single rounding per
+    // element as two scalar fmas); a bf16 widens to fp32 by moving its bits to the high half, an fp16 pair
+    // by conversion
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int j = 0; j < NG; ++j) {
@@ -143,9 +145,12 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
           const uint32_t v[4] = {raw[sl].x, raw[sl].y, raw[sl].z, raw[sl].w};
           const float2 w2 = make_float2(ws, ws);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            acc[c] = ffma2(w2, make_float2(__uint_as_float(v[c] << 16), __uint_as_float(v[c] & 0xFFFF0000u)),
-                           acc[c]);
+          for (int c = 0; c < 4; ++c) {
+            float2 x;
+            if constexpr (F16) x = __half22float2(*reinterpret_cast<const __half2*>(&v[c]));
+            else x = make_float2(__uint_as_float(v[c] << 16), __uint_as_float(v[c] & 0xFFFF0000u));
+            acc[c] = ffma2(w2, x, acc[c]);
+          }
         }
       }
     }
@@ -165,17 +170,18 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineParams& p, bool f16_partials, cudaStream_t stream) {
   const int64_t pairs = static_cast<int64_t>(p.total_q) * (p.hq >> 1);  // hq is a multiple of 8
   if (pairs == 0) return cudaSuccess;
   int64_t grid = (pairs + kCombineWarps - 1) / kCombineWarps;
   if (grid > 2LL * p.sms) grid = 2LL * p.sms;
   const unsigned g = static_cast<unsigned>(grid);
   const int ng = (p.topk + 15) / 16;
-  if (ng <= 1) combine_kernel<1><<<g, 32 * kCombineWarps, 0, stream>>>(p);
-  else if (ng == 2) combine_kernel<2><<<g, 32 * kCombineWarps, 0, stream>>>(p);
-  else if (ng == 3) combine_kernel<3><<<g, 32 * kCombineWarps, 0, stream>>>(p);
-  else combine_kernel<4><<<g, 32 * kCombineWarps, 0, stream>>>(p);
+  auto* fn = f16_partials ? (ng <= 1 ? combine_kernel<1, true> : ng == 2 ? combine_kernel<2, true>
+                             : ng == 3 ? combine_kernel<3, true> : combine_kernel<4, true>)
+                         : (ng <= 1 ? combine_kernel<1, false> : ng == 2 ? combine_kernel<2, false>
+                             : ng == 3 ? combine_kernel<3, false> : combine_kernel<4, false>);
+  fn<<<g, 32 * kCombineWarps, 0, stream>>>(p);
   note_launches(1);
   return cudaGetLastError();
 }

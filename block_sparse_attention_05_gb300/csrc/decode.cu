@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
           make_float2(oacc[nt][2] * f1, oacc[nt][3] * f1);
     }
     if (!meet(1, n - 1)) break;
-    __nv_bfloat16* out = p.part.o + (sel * G + hs * 16) * kHeadDim;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.part.o) + (sel * G + hs * 16) * kHeadDim;
     for (int i = threadIdx.x * 8; i < rows * 128; i += kDecThreads * 8) {
       const int at = (i >> 7) * kOsumStride + (i & 127);  // head i / 128, column i % 128
       float acc[8];

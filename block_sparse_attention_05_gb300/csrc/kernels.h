@@ -89,12 +89,15 @@ size_t decode_scan_smem_bytes();
 cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- main branch
-// Partial results of one (query, group, slot): G rows of 128 bf16 + G lse + G
-// log weights.  The true partial output (normalised within the block) is
-// o * exp(ow - lse): the decode kernel stores it as is (ow = lse), the prefill
-// kernel over V scaled by 2^-e (ow = lse + e ln 2).
+// Partial results of one (query, group, slot): G rows of 128 16-bit values + G
+// lse + G log weights.  The true partial output (normalised within the block)
+// is o * exp(ow - lse): the decode kernel stores it as is in bf16 (ow = lse),
+// the prefill kernel in fp16 over V scaled by 2^-e, whose magnitude stays below
+// 2^14 (ow = lse + e ln 2; for fp8 V, ow = lse + ln of the V scale): fp16's 11
+// significant bits keep the partial's rounding well under the output's own
+// bf16 rounding.
 struct PartialBuffers {
-  __nv_bfloat16* o;   // [total_q, hkv, topk, G, 128]
+  uint16_t* o;        // [total_q, hkv, topk, G, 128]: fp16 (prefill) or bf16 (decode)
   float* lse;         // [total_q, hkv, topk, G]
   float* ow;          // [total_q, hkv, topk, G]
 };
@@ -217,6 +220,7 @@ struct CombineParams {
   float* lse;
   WsHeader* hdr;
 };
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+// f16_partials: the partial outputs are fp16 (prefill) rather than bf16 (decode).
+cudaError_t launch_combine(const CombineParams& p, bool f16_partials, cudaStream_t stream);
 
 }  // namespace msa

@@ -21,8 +21,9 @@
 //                             as fp16, m a per-row reference (below)
 //   U = P V16                 tcgen05 (fp16) with A read from TMEM, V16 = the
 //                             fp16 copy of V, MN-major in smem
-//   U / l, LSE, log weight    written per (query, group, slot, head); the log
-//                             weight W = LSE + e ln 2 undoes V's 2^-e scale
+//   U / l, LSE, log weight    written per (query, group, slot, head), U / l in
+//                             fp16 (below 2^14 in V16 units); the log weight
+//                             W = LSE + e ln 2 undoes V's 2^-e scale
 // fp8 K/V (E4M3 codes with one scale per key block and KV head) run on exact
 // 16-bit copies of the codes: the tile's K scale multiplies its logits and the
 // log of its V scale is added to the log weight.
@@ -101,8 +102,8 @@ __device__ __forceinline__ ChunkInfo decode_chunk(const AttnParams& p, int item)
   return ci;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
+  __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -647,13 +648,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const float2 il = make_float2(inv_l, inv_l);
             float2 z;
             z = fmul2(make_float2(__uint_as_float(o[8 * c + 0]), __uint_as_float(o[8 * c + 1])), il);
-            pk[c].x = pack_bf16(z.x, z.y);
+            pk[c].x = pack_f16(z.x, z.y);
             z = fmul2(make_float2(__uint_as_float(o[8 * c + 2]), __uint_as_float(o[8 * c + 3])), il);
-            pk[c].y = pack_bf16(z.x, z.y);
+            pk[c].y = pack_f16(z.x, z.y);
             z = fmul2(make_float2(__uint_as_float(o[8 * c + 4]), __uint_as_float(o[8 * c + 5])), il);
-            pk[c].z = pack_bf16(z.x, z.y);
+            pk[c].z = pack_f16(z.x, z.y);
             z = fmul2(make_float2(__uint_as_float(o[8 * c + 6]), __uint_as_float(o[8 * c + 7])), il);
-            pk[c].w = pack_bf16(z.x, z.y);
+            pk[c].w = pack_f16(z.x, z.y);
             *reinterpret_cast<uint4*>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = pk[c];
           }
           __syncwarp();
@@ -661,7 +662,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int k = 0; k < 4; ++k) {
             const int R = 8 * k + (lane >> 2);
             const uint4 v = *reinterpret_cast<const uint4*>(stg + R * 64 + ((ck ^ ((R >> 1) & 3)) << 4));
-            if (rowp[k]) *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(rowp[k]) + quarter * 32 + ck * 8) = v;
+            if (rowp[k]) *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(rowp[k]) + quarter * 32 + ck * 8) = v;
           }
           __syncwarp();
         };

@@ -6,9 +6,12 @@ the oracle's unrounded values.
 Tolerance: the kernel accumulates the projection in fp32 on the tensor cores
 and rounds each output once to bf16, the oracle works in double, so every
 output is within one bf16 unit in the last place (2^-7 relative to the power
-of two below it) of the oracle's value, plus 1e-6 absolute for outputs near
-zero, and at least 99 % of the outputs equal the oracle's value rounded to
-bf16.  K_idx rows other than the new tokens' must be left untouched.
+of two below it) of the oracle's value plus the fp32 accumulation error, which
+matters only for outputs near zero: about k u sum_c |x_c w_c| with u = 2^-24,
+a partial-sum depth k of about 16 and sum_c |x_c w_c| of about 36 at d_model
+3072 (|x| ~ 0.8, |w| ~ 0.8 / sqrt(3072)), so 5e-5 absolute is allowed on top;
+at least 99 % of the outputs must equal the oracle's value rounded to bf16.
+K_idx rows other than the new tokens' must be left untouched.
 """
 import types
 
@@ -45,7 +48,7 @@ def _bf16_ulp(v):
 def _check(got, ref, what):
     got = got.astype(np.float64)
     err = np.abs(got - ref)
-    bound = _bf16_ulp(ref) + 1e-6
+    bound = _bf16_ulp(ref) + 5e-5
     bad = err > bound
     assert not bad.any(), f"{what}: {int(bad.sum())} outputs beyond one bf16 ulp, worst {err[bad].max():.3e}"
     same = got == torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
