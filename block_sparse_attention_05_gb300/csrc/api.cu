@@ -57,7 +57,7 @@ struct Derived {
 };
 
 struct Layout {
-  size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, count, bstart, bcursor, nchunk, cstart,
+  size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, cand, count, bstart, bcursor, nchunk, cstart,
       entries, chunks, scan_tmp, v16, k16, part_o, part_lse, part_ow, total;
 };
 
@@ -145,6 +145,10 @@ Layout layout(const Derived& d, msa_op_t op) {
   if (op_uses_index_prefill(op, d)) L.tiles = take(sizeof(int2) * d.max_tiles);
   if (op_uses_decode_index(op, d) || op_uses_pooled_prefill(op, d))
     L.pooled = take(sizeof(float) * static_cast<size_t>(d.T) * d.hkv * d.max_nb);
+  if (op_uses_decode_index(op, d) || op == MSA_OP_TOPK_POOLED) {
+    const int ns = topk_splits(d.max_nb, d.topk);
+    if (ns > 1) L.cand = take(sizeof(uint64_t) * static_cast<size_t>(d.T) * d.hkv * ns * 16);
+  }
   if (op_uses_prefill_attn(op, d)) {
     L.count = take(sizeof(int32_t) * d.n_buckets);
     L.bstart = take(sizeof(int32_t) * (d.n_buckets + 1));
@@ -318,8 +322,6 @@ msa_status_t cuda_status(cudaError_t e) {
 
 msa_status_t run_plan(const msa_problem_t* p, Ctx& c, int qt) {
   StageScope scope(MSA_STAGE_PLAN, c.stream);
-  note_launches(1);
-  if (cudaMemsetAsync(c.hdr, 0, sizeof(WsHeader), c.stream) != cudaSuccess) return MSA_ERR_CUDA;
   PlanParams pp{};
   pp.num_seqs = c.d.S;
   pp.cu_q = p->cu_seqlens_q;
@@ -379,6 +381,8 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
   tp.pooled_stride = stride;
   tp.idx = idx;
   tp.hdr = c.hdr;
+  tp.nsplit = topk_splits(c.d.max_nb, c.d.topk);
+  tp.cand = tp.nsplit > 1 ? at<uint64_t>(c.ws, c.L.cand) : nullptr;
   StageScope scope(MSA_STAGE_TOPK, c.stream);
   return cuda_status(launch_topk_pooled(tp, c.d.max_nb, c.stream));
 }
@@ -870,7 +874,11 @@ msa_status_t msa_index_prologue(const msa_problem_t* problem, const void* x, int
   pp.gamma_k = static_cast<const __nv_bfloat16*>(gamma_k);
   pp.q_idx = static_cast<__nv_bfloat16*>(q_idx);
   pp.k_idx = static_cast<__nv_bfloat16*>(k_idx);
-  for (int j = 0; j < 32; ++j) pp.rope_turns[j] = std::pow(10000.0, -j / 32.0) / (2.0 * 3.14159265358979323846);
+  for (int j = 0; j < 32; ++j) {
+    const double turns = std::pow(10000.0, -j / 32.0) / (2.0 * 3.14159265358979323846);
+    pp.rope_turns_hi[j] = static_cast<float>(turns);
+    pp.rope_turns_lo[j] = static_cast<float>(turns - static_cast<double>(pp.rope_turns_hi[j]));
+  }
   pp.hdr = c.hdr;
   StageScope scope(MSA_STAGE_INDEX, c.stream);
   return cuda_status(launch_index_prologue(tx, twq, twk, pp, c.dev.sms, c.stream));

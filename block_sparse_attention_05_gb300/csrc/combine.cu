@@ -59,6 +59,7 @@ __device__ __forceinline__ PairRef pair_ref(const CombineParams& p, int64_t pair
 // F16: the partial rows are fp16 (prefill), else bf16 (decode).
 template <int NG, bool F16>
 __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineParams p) {
+  griddep_wait();  // the partials come from the Main Branch kernel
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, hl = lane & 15;
@@ -181,9 +182,9 @@ cudaError_t launch_combine(const CombineParams& p, bool f16_partials, cudaStream
                              : ng == 3 ? combine_kernel<3, true> : combine_kernel<4, true>)
                          : (ng <= 1 ? combine_kernel<1, false> : ng == 2 ? combine_kernel<2, false>
                              : ng == 3 ? combine_kernel<3, false> : combine_kernel<4, false>);
-  fn<<<g, 32 * kCombineWarps, 0, stream>>>(p);
+  const cudaError_t e = launch_pdl(fn, dim3(g), dim3(32 * kCombineWarps), 0, stream, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

@@ -66,6 +66,20 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream serialization attribute may start while the previous kernel on the
+// stream drains; griddep_wait() returns once that kernel has completed and its
+// writes are visible (immediately when the kernel was launched without the
+// attribute).  Every such kernel calls it before touching memory the previous
+// kernel writes or reads.  griddep_launch_dependents() lets the next kernel's
+// CTAs be scheduled before this one finishes (they still wait in griddep_wait).
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     decode_scan_kernel(const __grid_constant__ CUtensorMap tm_k, DecodeScanParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
+  griddep_wait();  // sequence facts and the header come from the plan kernel
+  griddep_launch_dependents();
   if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   ScanSmem& sm = *reinterpret_cast<ScanSmem*>(base + kScanStages * kScanTile);
@@ -229,9 +231,9 @@ cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p,
   cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kScanSmemBytes));
   if (e != cudaSuccess) return e;
-  decode_scan_kernel<<<grid, kScanThreads, kScanSmemBytes, stream>>>(tk, p);
+  e = launch_pdl(decode_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmemBytes, stream, tk, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 // ----------------------------------------------------------------------------
@@ -328,6 +330,8 @@ __global__ void __launch_bounds__(kDecThreads + 32)
                        const __grid_constant__ CUtensorMap tm_v, DecodeAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
+  griddep_wait();  // the selection comes from the top-k kernel
+  griddep_launch_dependents();
   if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* stage8 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* base = stage8 + (FP8 ? kDec8Staging : 0);                       // fp8: K codes 16 KB | V codes 16 KB
@@ -671,9 +675,9 @@ cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, con
   auto* fn = fp8 ? decode_attn_kernel<true> : decode_attn_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<static_cast<unsigned>(grid), kDecThreads + 32, smem, stream>>>(tq, tk, tv, p);
+  e = launch_pdl(fn, dim3(static_cast<unsigned>(grid)), dim3(kDecThreads + 32), smem, stream, tq, tk, tv, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

@@ -1,7 +1,7 @@
 // fp8.cu -- fp8 (E4M3) K/V: quantization, and the widening copies the prefill
 // Main Branch reads.
 //
-// The atlas record of the report notes that the kernels "also support fp8"
+// The atlas record of the report states that the kernels handle fp8 as well
 // (provenance of section 4.2) without giving a format.  This library reads it
 // as OCP E4M3 codes with one fp32 scale per (key block of 128 tokens of a
 // sequence, KV head), for K and V separately: scale = amax / 448 over the

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace msa {
 
 struct WsHeader;
@@ -15,6 +17,24 @@ struct SeqInfo;
 
 // Adds n to the library's count of enqueued kernels (msa_kernel_launch_count).
 void note_launches(int n);
+
+// Launches `kernel` with programmatic dependent launch allowed (see griddep_wait in common.cuh): the kernel
+// must call griddep_wait() before it touches memory of the kernel before it on the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- planning
 struct PlanParams {
@@ -65,7 +85,13 @@ struct TopkParams {
   int64_t pooled_stride;
   int32_t* idx;
   WsHeader* hdr;
+  // long rows split over nsplit CTAs (k <= 16): each writes its best k - 1 keys to cand
+  // [rows, nsplit, 16] and a merge kernel selects from those; nsplit = 1: one CTA per row
+  int nsplit;
+  uint64_t* cand;
 };
+// CTAs per row for the top-k of rows of up to max_nb blocks (1 for short rows or k > 16).
+int topk_splits(int max_nb, int topk);
 cudaError_t launch_topk_pooled(const TopkParams& p, int max_nb, cudaStream_t stream);
 
 // Decode index scan: pooled scores of the single query of each sequence.
@@ -183,7 +209,8 @@ struct PrologueParams {
   const __nv_bfloat16* gamma_k;  // [128]
   __nv_bfloat16* q_idx;          // [total_q, hkv, 128]
   __nv_bfloat16* k_idx;          // [total_k, 128]: row k_start + pos(i) of token i
-  double rope_turns[32];         // theta_j / (2 pi), theta_j = 10000^(-j/32)
+  float rope_turns_hi[32];       // theta_j / (2 pi) = hi + lo, theta_j = 10000^(-j/32)
+  float rope_turns_lo[32];
   WsHeader* hdr;
 };
 size_t index_prologue_smem_bytes();

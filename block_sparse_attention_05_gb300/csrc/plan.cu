@@ -47,6 +47,10 @@ __device__ __forceinline__ int tile_cost(const SeqInfo& si, int t0, int qt) {
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
   __shared__ int sh[32];
   __shared__ int s_bad;
+  // a call starts from a clear workspace header (status flags, work counters)
+  static_assert(sizeof(WsHeader) % 4 == 0, "header cleared as 32-bit words");
+  for (int w = threadIdx.x; w < static_cast<int>(sizeof(WsHeader) / 4); w += blockDim.x)
+    reinterpret_cast<uint32_t*>(p.hdr)[w] = 0u;
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
 

@@ -16,9 +16,12 @@
 // ring, tcgen05 MMAs into a double-buffered TMEM accumulator.  The epilogue
 // warps (one TMEM lane = one token row per thread) make two passes over each
 // head's 128 columns: the sum of squares, then normalisation, RoPE and the bf16
-// store.  The RoPE angle is reduced to a fraction of a turn in double
-// (pos * (theta_j / 2 pi) minus its integer part), so its sine and cosine are
-// accurate at positions up to millions.
+// store.  The RoPE angle is reduced to a fraction of a turn before its sine
+// and cosine are taken: theta_j / 2 pi is held as a sum of two floats hi + lo,
+// pos * hi is split exactly into a rounded product and its error (one fma),
+// the product's integer part drops out exactly, and the small terms are added
+// back -- accurate to about 1e-9 turns at positions up to millions, where an
+// fp32 product pos * theta would be off by 0.06 radians.
 // Token i (query row i, key position pos(i)) writes Q_idx[i, h, :] and the key
 // row k_start + pos(i) of K_idx: the new tokens' rows of the index-key cache.
 #include "common.cuh"
@@ -226,9 +229,13 @@ __global__ void __launch_bounds__(kProThreads, 1)
             float cs[2], sn[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              // fraction of a turn of pos * theta_j, theta_j = 10000^(-j/32), reduced in double
-              const double turns = static_cast<double>(pos) * p.rope_turns[jj + u];
-              const float f = static_cast<float>(turns - rint(turns));
+              // fraction of a turn of pos * theta_j / (2 pi), with theta_j / (2 pi) = hi + lo (two floats):
+              // pos * hi = t + e exactly (fma), t - rint(t) is exact, and pos * lo is below 0.01 turns
+              const float fp = static_cast<float>(pos);
+              const float hi = p.rope_turns_hi[jj + u], lo = p.rope_turns_lo[jj + u];
+              const float t = fp * hi;
+              const float e = fmaf(fp, hi, -t);
+              const float f = (t - rintf(t)) + fmaf(fp, lo, e);
               sincospif(2.0f * f, &sn[u], &cs[u]);
             }
             const float a0 = __uint_as_float(a[jj]) * inv * gamma[jj];

@@ -276,7 +276,7 @@ msa_status_t msa_index_prologue(const msa_problem_t *problem, const void *x, int
 
 /* ------------------------------------------------------------------------
  * fp8 K and V.  The atlas record of the report (provenance of section 4.2)
- * says the kernels "also support fp8" and gives no format; this library reads
+ * says the kernels handle fp8 as well and gives no format; this library reads
  * it as OCP E4M3 codes ("E4M3FN": bias 7, 3 mantissa bits, largest finite
  * 448, no infinities) with one fp32 scale per (key block of 128 tokens of a
  * sequence, KV head), for K and for V separately:

@@ -26,8 +26,8 @@
  *
  *  3. msa_oracle_attention -- Main Branch: exact softmax attention of every
  *     query head over only the tokens of its group's selected blocks.  Same
- *     section, second bullet ("exact attention over only those blocks",
- *     "every head in a group reuses the same block set").
+ *     section, second bullet: attention stays exact but covers only the
+ *     selected blocks, and all heads of a group share one block set.
  *
  * Precision.  The pages fix no precision.  Token index scores are formed in
  * double from the exact bf16 inputs and rounded once to fp32; pooling and
@@ -377,7 +377,7 @@ int msa_oracle_forward(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
 
 /*
  * fp8 K/V (the atlas record of the report, provenance of section 4.2: the
- * kernels "also support fp8"; the pages give no format, so this follows the
+ * kernels handle fp8 as well; the pages give no format, so this follows the
  * plainest reading, stated with the build's design notes):
  *   * codes are OCP FP8 E4M3 ("E4M3FN"): sign, 4 exponent bits with bias 7,
  *     3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6); no infinities;

@@ -1,5 +1,5 @@
 """GPU parity of the fp8 K/V path (E4M3 codes, one scale per key block and KV
-head; the atlas record of the report: the kernels "also support fp8", format
+head; the atlas record of the report: the kernels handle fp8 as well, format
 read as stated in include/msa.h) against the CPU oracle:
 
   * quantization: codes and scales bit-exact against oracle.quantize_fp8 (an

@@ -278,7 +278,9 @@ DECODE_CASES = [(8, 3000, 16, 128, 64, 4), (5, 700, 16, 64, 64, 4), (3, 128, 4, 
                 (16, 20000, 16, 128, 64, 4), (40, 60000, 16, 128, 64, 4),
                 (6, 9000, 32, 128, 64, 4), (4, 20000, 64, 128, 64, 4), (3, 1000, 64, 64, 64, 4),
                 (7, 5000, 16, 128, 32, 4), (5, 7000, 16, 128, 128, 4), (4, 6000, 24, 128, 128, 2),
-                (3, 4000, 16, 64, 128, 1)]
+                (3, 4000, 16, 64, 128, 1),
+                # long rows: the decode top-k splits each row over 2 (and 4) CTAs and merges their candidates
+                (3, 300000, 16, 128, 64, 4), (2, 600000, 8, 128, 64, 4)]
 
 
 @pytest.mark.parametrize("n,ctx,topk,d_idx,hq,hkv", DECODE_CASES)

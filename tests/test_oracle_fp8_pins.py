@@ -9,7 +9,7 @@ KV head), against facts fixed outside the oracle:
     equal the bf16 Main Branch when K and V already lie on the fp8 grid with a
     power-of-two scale.
 The fp8 support itself: the atlas record of the report, provenance of section
-4.2 (the kernels "also support fp8"; no format is given, the reading is stated
+4.2 (the kernels handle fp8 as well; no format is given, the reading is stated
 in the oracle).  No GPU is needed.
 """
 import json
