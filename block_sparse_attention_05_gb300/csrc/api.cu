@@ -57,7 +57,7 @@ struct Derived {
 };
 
 struct Layout {
-  size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, cand, count, bstart, bcursor, nchunk, cstart,
+  size_t hdr, seq, blk_off, tile_base, hist, cursor, tiles, pooled, count, bstart, bcursor, nchunk, cstart,
       entries, chunks, scan_tmp, v16, k16, part_o, part_lse, part_ow, total;
 };
 
@@ -145,10 +145,6 @@ Layout layout(const Derived& d, msa_op_t op) {
   if (op_uses_index_prefill(op, d)) L.tiles = take(sizeof(int2) * d.max_tiles);
   if (op_uses_decode_index(op, d) || op_uses_pooled_prefill(op, d))
     L.pooled = take(sizeof(float) * static_cast<size_t>(d.T) * d.hkv * d.max_nb);
-  if (op_uses_decode_index(op, d) || op == MSA_OP_TOPK_POOLED) {
-    const int ns = topk_splits(d.max_nb, d.topk);
-    if (ns > 1) L.cand = take(sizeof(uint64_t) * static_cast<size_t>(d.T) * d.hkv * ns * 16);
-  }
   if (op_uses_prefill_attn(op, d)) {
     L.count = take(sizeof(int32_t) * d.n_buckets);
     L.bstart = take(sizeof(int32_t) * (d.n_buckets + 1));
@@ -381,8 +377,6 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
   tp.pooled_stride = stride;
   tp.idx = idx;
   tp.hdr = c.hdr;
-  tp.nsplit = topk_splits(c.d.max_nb, c.d.topk);
-  tp.cand = tp.nsplit > 1 ? at<uint64_t>(c.ws, c.L.cand) : nullptr;
   StageScope scope(MSA_STAGE_TOPK, c.stream);
   return cuda_status(launch_topk_pooled(tp, c.d.max_nb, c.stream));
 }

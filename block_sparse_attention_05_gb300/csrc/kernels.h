@@ -85,13 +85,7 @@ struct TopkParams {
   int64_t pooled_stride;
   int32_t* idx;
   WsHeader* hdr;
-  // long rows split over nsplit CTAs (k <= 16): each writes its best k - 1 keys to cand
-  // [rows, nsplit, 16] and a merge kernel selects from those; nsplit = 1: one CTA per row
-  int nsplit;
-  uint64_t* cand;
 };
-// CTAs per row for the top-k of rows of up to max_nb blocks (1 for short rows or k > 16).
-int topk_splits(int max_nb, int topk);
 cudaError_t launch_topk_pooled(const TopkParams& p, int max_nb, cudaStream_t stream);
 
 // Decode index scan: pooled scores of the single query of each sequence.

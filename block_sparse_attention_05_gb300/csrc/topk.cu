@@ -11,9 +11,6 @@
 // One CTA of W warps per row.  Warp w scans a contiguous slice of the row, each
 // lane keeping the CAP best (score, block) keys of its strided subset; k-1
 // rounds of warp max extract the warp's best k-1; warp 0 merges the W lists.
-// Long rows (decode at 1M: 8192 blocks, 32 rows) are split over several CTAs
-// of about 1024 blocks each, whose best k-1 keys a one-warp-per-row merge
-// kernel selects from, so that more than one SM per row takes part.
 // That needs registers for k-1 keys per lane, so it serves k <= 16; larger k
 // (up to 64) take topk_radix_kernel below: a radix selection of the (k-1)-th
 // best key, eight bits of the 64-bit key per pass over the row, then every
@@ -34,7 +31,6 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   griddep_launch_dependents();
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int row = blockIdx.x;
-  const int split = blockIdx.y, nsplit = gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 502)) return;
   const int nwarps = blockDim.x >> 5;
@@ -47,11 +43,9 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   const int want = min(p.topk - 1, nb - 1);
   const float* pr = p.pooled + static_cast<int64_t>(row) * p.pooled_stride;
 
-  // this CTA's part of the non-local blocks [0, local), then this warp's slice of it
-  const int per_cta = (local + nsplit - 1) / nsplit;
-  const int c_lo = split * per_cta, c_hi = min(local, c_lo + per_cta);
-  const int per = (c_hi - c_lo + nwarps - 1) / nwarps;
-  const int lo = c_lo + warp * per, hi = min(c_hi, lo + per);
+  // this warp's slice of the non-local blocks [0, local)
+  const int per = (local + nwarps - 1) / nwarps;
+  const int lo = warp * per, hi = min(local, lo + per);
   TopkList<CAP> lst;
   lst.clear();
   // eight loads in flight per lane before any insertion (one memory round
@@ -91,46 +85,9 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
       const uint64_t best = warp_max_u64(fin.k[0]);
       if (best != 0ull && fin.k[0] == best) fin.pop();
       if (best != 0ull) chosen[r] = topk_key_block(best);
-      if (nsplit > 1 && lane == 0) p.cand[(static_cast<int64_t>(row) * nsplit + split) * 16 + r] = best;
     }
   }
-  if (nsplit == 1 && lane == 0 && index_ok(p.hdr, local, p.max_nb, 503))
-    write_selection<CAP>(p.idx + static_cast<int64_t>(row) * p.topk, p.topk, chosen, local);
-}
-
-// Second step of a split row: one warp per row merges the nsplit CTAs' best
-// k - 1 keys (0 = none) and writes the selection.
-constexpr int kMergeRowsPerCta = 4;
-
-template <int CAP>
-__global__ void __launch_bounds__(32 * kMergeRowsPerCta) topk_merge_kernel(TopkParams p) {
-  griddep_wait();  // the candidates come from the kernel before
-  griddep_launch_dependents();
-  if (p.hdr->status & kFlagBadSeqlens) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kMergeRowsPerCta + warp;
-  if (row >= p.total_q * p.hkv) return;
-  const int i = row / p.hkv;
-  const int s = find_seq(p.cu_q, p.num_seqs, i);
-  const SeqInfo si = p.seq[s];
-  const int pos = si.kv_len - si.q_len + (i - si.q_start);
-  const int local = pos >> 7;
-  const int want = min(p.topk - 1, local);
-  const uint64_t* c = p.cand + static_cast<int64_t>(row) * p.nsplit * 16;
-  TopkList<CAP> fin;
-  fin.clear();
-  for (int j = lane; j < p.nsplit * want; j += 32) fin.insert(c[(j / want) * 16 + j % want]);
-  int chosen[CAP];
-#pragma unroll
-  for (int r = 0; r < CAP; ++r) {
-    chosen[r] = -1;
-    if (r < want) {
-      const uint64_t best = warp_max_u64(fin.k[0]);
-      if (best != 0ull && fin.k[0] == best) fin.pop();
-      if (best != 0ull) chosen[r] = topk_key_block(best);
-    }
-  }
-  if (lane == 0 && index_ok(p.hdr, local, p.max_nb, 504))
+  if (lane == 0 && index_ok(p.hdr, local, p.max_nb, 503))
     write_selection<CAP>(p.idx + static_cast<int64_t>(row) * p.topk, p.topk, chosen, local);
 }
 
@@ -244,23 +201,12 @@ __global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p)
 
 }  // namespace
 
-int topk_splits(int max_nb, int topk) {
-  if (topk > 16) return 1;
-  const int n = max_nb / 1024;  // about 1024 blocks per CTA
-  return n < 2 ? 1 : (n > 16 ? 16 : n);
-}
-
 template <int CAP>
 static cudaError_t launch_topk_cap(const TopkParams& p, int max_nb, cudaStream_t stream) {
   const int rows = p.total_q * p.hkv;
-  const int slice = (max_nb + p.nsplit - 1) / p.nsplit;
-  int warps = slice / 128;
+  int warps = max_nb / 256;
   warps = warps < 1 ? 1 : (warps > kTopkMaxWarps ? kTopkMaxWarps : warps);
-  cudaError_t e = launch_pdl(topk_pooled_kernel<CAP>, dim3(rows, p.nsplit), dim3(32 * warps), 0, stream, p);
-  note_launches(1);
-  if (e != cudaSuccess || p.nsplit == 1) return e;
-  e = launch_pdl(topk_merge_kernel<CAP>, dim3((rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta),
-                 dim3(32 * kMergeRowsPerCta), 0, stream, p);
+  const cudaError_t e = launch_pdl(topk_pooled_kernel<CAP>, dim3(rows), dim3(32 * warps), 0, stream, p);
   note_launches(1);
   return e;
 }
