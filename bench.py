@@ -539,6 +539,74 @@ def measure_prologue(msa, cfg, steps, warmup, dev, d_model=3072):
     return rec
 
 
+# ------------------------------------------------------------------ fp8 K/V
+def measure_fp8(msa, cfg, steps, warmup, dev):
+    """The same step with fp8 (E4M3, per-block scales) K and V for the Main Branch (msa_forward_fp8), after one
+    msa_quantize_kv_fp8 of the workload's K and V (timed separately): step time, stage times and, for decode,
+    the Main Branch's K/V bytes per second (one byte per element)."""
+    x = workloads.generate(cfg, device=dev)
+    prob = msa.Problem(x.cu_q, x.cu_k, x.total_q, x.total_k, x.max_q, x.max_k, cfg.hq, cfg.hkv, cfg.d_idx,
+                       cfg.topk)
+    qws = msa.workspace(prob, msa.Op.QUANTIZE_KV_FP8)
+    k8, v8, ks, vs = msa.msa_quantize_kv_fp8(prob, x.k, x.v, ws=qws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    msa.msa_quantize_kv_fp8(prob, x.k, x.v, k8=k8, v8=v8, k_scale=ks, v_scale=vs, ws=qws)
+    b.record()
+    torch.cuda.synchronize()
+    quant_ms = a.elapsed_time(b)
+    ws = msa.workspace(prob, msa.Op.FORWARD_FP8)
+    idx = torch.empty((x.total_q, cfg.hkv, cfg.topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((x.total_q, cfg.hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(max(2 * L2_BYTES, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        msa.msa_forward_fp8(prob, x.q, k8, v8, ks, vs, x.q_idx, x.k_idx, idx=idx, o=o, lse=lse, ws=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s_, e_ in ev:
+        flush.zero_()
+        s_.record()
+        step()
+        e_.record()
+    torch.cuda.synchronize()
+    if msa.msa_read_device_status(ws):
+        raise RuntimeError("device status flags raised by the fp8 forward")
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in ev) / steps
+    timer = msa.StageTimer()
+    stage = {}
+    with timer:
+        for _ in range(min(steps, 20)):
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
+            for k_, v_ in timer.elapsed_ms().items():
+                stage[k_] = stage.get(k_, 0.0) + v_ / min(steps, 20)
+    work = algorithmic_work(x, idx)
+    peaks = measured_peaks()
+    unit = "tok/s" if cfg.is_decode else "query tok/s"
+    rec = {"workload": f"{cfg.name}, fp8 K/V", "value": x.total_q / (ms * 1e-3), "unit": unit, "ms_per_step": ms,
+           "steps": steps, "stages_ms": stage, "quantize_ms": quant_ms,
+           "quantize_gbs": 3.0 * x.total_k * cfg.hkv * cfg.head_dim * 2 / (quant_ms * 1e-3) / 1e9}
+    if "attn" in stage:
+        if cfg.is_decode:
+            kv8 = work["kv_bytes_selected"] / 2  # one byte per K and V element
+            rec["attn_kv_gbs"] = kv8 / (stage["attn"] * 1e-3) / 1e9
+            rec["attn_kv_bytes"] = kv8
+        else:
+            rec["attn_tflops"] = work["attn_flops"] / (stage["attn"] * 1e-3) / 1e12
+            rec["attn_frac_of_tc_peak"] = rec["attn_tflops"] / peaks["bf16_tflops"]
+    del x, ws, idx, o, lse, flush, k8, v8, ks, vs, qws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 # ------------------------------------------------------------------ main
 def main():
     ap = argparse.ArgumentParser()
@@ -555,6 +623,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prologue", action="store_true", help="skip the index prologue measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the fp8 K/V measurements")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -606,9 +675,14 @@ def main():
     if not cfg.is_decode and not args.no_prologue:
         pro_rec = measure_prologue(msa, cfg, max(args.steps, 10), args.warmup, dev)
     dec_rec = None
+    fp8_rec = {}
+    if not args.no_fp8:
+        fp8_rec[cfg.name] = measure_fp8(msa, cfg, args.steps, args.warmup, dev)
     if args.decode_workload != "none" and args.decode_workload != args.workload:
         dcfg = workloads.get(args.decode_workload)
         dec_rec = measure(msa, dcfg, args.decode_steps, args.warmup, args, dev, world, rank)
+        if not args.no_fp8:
+            fp8_rec[dcfg.name] = measure_fp8(msa, dcfg, args.decode_steps, args.warmup, dev)
 
     if rank == 0:
         m = main_rec
@@ -629,6 +703,8 @@ def main():
                      "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": m["clocks"], "work": m["work"]})
         if pro_rec is not None:
             line["index_prologue"] = pro_rec
+        if fp8_rec:
+            line["fp8_kv"] = fp8_rec
         if dec_rec is not None:
             dec_rec = dict(dec_rec)
             dec_rec["value"] = dec_rec["value"] * 1.0

@@ -96,7 +96,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   griddep_wait();  // sequence facts and the header come from the plan kernel
-  griddep_launch_dependents();
   if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   ScanSmem& sm = *reinterpret_cast<ScanSmem*>(base + kScanStages * kScanTile);
@@ -331,7 +330,6 @@ __global__ void __launch_bounds__(kDecThreads + 32)
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   griddep_wait();  // the selection comes from the top-k kernel
-  griddep_launch_dependents();
   if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* stage8 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* base = stage8 + (FP8 ? kDec8Staging : 0);                       // fp8: K codes 16 KB | V codes 16 KB

@@ -47,6 +47,7 @@ __device__ __forceinline__ int tile_cost(const SeqInfo& si, int t0, int qt) {
 __global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
   __shared__ int sh[32];
   __shared__ int s_bad;
+  griddep_wait();  // the kernel before may still read this workspace's header
   // a call starts from a clear workspace header (status flags, work counters)
   static_assert(sizeof(WsHeader) % 4 == 0, "header cleared as 32-bit words");
   for (int w = threadIdx.x; w < static_cast<int>(sizeof(WsHeader) / 4); w += blockDim.x)
@@ -201,9 +202,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_down_kernel(const int32_t* 
 }  // namespace
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
-  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  const cudaError_t e = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, stream, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 int scan_tmp_ints(int n) { return (n + kScanTile - 1) / kScanTile + 1; }

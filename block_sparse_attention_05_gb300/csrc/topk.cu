@@ -28,7 +28,6 @@ template <int CAP>
 __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkParams p) {
   __shared__ uint64_t cand[kTopkMaxWarps][CAP];
   griddep_wait();  // the pooled rows come from the kernel before
-  griddep_launch_dependents();
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -106,7 +105,6 @@ __global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p)
   __shared__ int s_digit, s_rem, s_exact;
   __shared__ int s_warp_tot[kRadixThreads / 32];
   griddep_wait();  // the pooled rows come from the kernel before
-  griddep_launch_dependents();
   if (p.hdr->status & kFlagBadSeqlens) return;
   const int row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
