@@ -15,6 +15,14 @@
 // (up to 64) take topk_radix_kernel below: a radix selection of the (k-1)-th
 // best key, eight bits of the 64-bit key per pass over the row, then every
 // key at or above it, written in block order by a compaction scan.
+//
+// Long rows in small batches (decode: a few rows of thousands of blocks) take
+// topk_threshold_kernel: 1024 threads per row, each reducing its strided share
+// of the row to one maximum; a bitonic sort of those maxima gives the want-th
+// largest, T.  At least want keys reach T (the want threads whose maxima do)
+// and at most want x (keys per thread) do, so the keys >= T are a small
+// candidate set holding the answer; each candidate's rank among them is
+// counted directly, and the want best are written in block order.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -197,6 +205,86 @@ __global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p)
   }
 }
 
+constexpr int kThrThreads = 1024;
+constexpr int kThrMaxPerThread = 32;  // rows of up to 32 x 1024 blocks
+constexpr int kThrCandMax = 63 * kThrMaxPerThread;
+
+__global__ void __launch_bounds__(kThrThreads) topk_threshold_kernel(TopkParams p) {
+  __shared__ uint64_t tmax[kThrThreads];
+  __shared__ uint64_t cand[kThrCandMax];
+  __shared__ int chosen[64];
+  __shared__ int n_cand;
+  griddep_wait();  // the pooled rows come from the kernel before
+  if (p.hdr->status & kFlagBadSeqlens) return;
+  const int row = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 521)) return;
+  const int i = row / p.hkv;
+  const int s = find_seq(p.cu_q, p.num_seqs, i);
+  const SeqInfo si = p.seq[s];
+  const int pos = si.kv_len - si.q_len + (i - si.q_start);
+  const int local = pos >> 7;  // also the number of non-local causal blocks
+  const int want = min(p.topk - 1, local);
+  if (!index_ok(p.hdr, local, p.max_nb, 522) || local > kThrThreads * kThrMaxPerThread) return;
+  const float* pr = p.pooled + static_cast<int64_t>(row) * p.pooled_stride;
+  int32_t* out = p.idx + static_cast<int64_t>(row) * p.topk;
+  if (want > 0) {
+    uint64_t mx = 0ull;
+    for (int b = tid; b < local; b += kThrThreads) {
+      const uint64_t key = topk_key(pr[b], b);
+      mx = key > mx ? key : mx;
+    }
+    tmax[tid] = mx;
+    if (tid == 0) n_cand = 0;
+    __syncthreads();
+    // bitonic sort of the maxima, descending
+    for (int k = 2; k <= kThrThreads; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int o = tid ^ j;
+        if (o > tid) {
+          const uint64_t a = tmax[tid], b = tmax[o];
+          if (((tid & k) == 0) ? (a < b) : (a > b)) {
+            tmax[tid] = b;
+            tmax[o] = a;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // want <= min(local, 63) threads hold a key, so T > 0 is a real key
+    const uint64_t T = tmax[want - 1];
+    for (int b = tid; b < local; b += kThrThreads) {
+      const uint64_t key = topk_key(pr[b], b);
+      if (key >= T) {
+        // at most want x kThrMaxPerThread keys reach T; the guard only makes that explicit
+        const int c = atomicAdd(&n_cand, 1);
+        if (c < kThrCandMax) cand[c] = key;
+      }
+    }
+    __syncthreads();
+    const int nc = min(n_cand, kThrCandMax);
+    // rank of each candidate among the candidates (keys are distinct); the want best are kept
+    for (int c = tid; c < nc; c += kThrThreads) {
+      const uint64_t key = cand[c];
+      int rank = 0;
+      for (int j = 0; j < nc; ++j) rank += cand[j] > key ? 1 : 0;
+      if (rank < want) chosen[rank] = topk_key_block(key);
+    }
+    __syncthreads();
+    // in block order: the position of a kept block is the number of kept blocks below it
+    if (tid < want) {
+      const int b = chosen[tid];
+      int at = 0;
+      for (int j = 0; j < want; ++j) at += chosen[j] < b ? 1 : 0;
+      out[at] = b;
+    }
+  }
+  if (tid == 0) {
+    out[want] = local;
+    for (int j = want + 1; j < p.topk; ++j) out[j] = -1;
+  }
+}
+
 }  // namespace
 
 template <int CAP>
@@ -212,6 +300,12 @@ static cudaError_t launch_topk_cap(const TopkParams& p, int max_nb, cudaStream_t
 cudaError_t launch_topk_pooled(const TopkParams& p, int max_nb, cudaStream_t stream) {
   const int rows = p.total_q * p.hkv;
   if (rows == 0) return cudaSuccess;
+  // a few long rows (decode batches): one 1024-thread CTA per row
+  if (max_nb >= 2048 && max_nb <= kThrThreads * kThrMaxPerThread && rows <= 1024) {
+    cudaError_t e = launch_pdl(topk_threshold_kernel, dim3(rows), dim3(kThrThreads), 0, stream, p);
+    note_launches(1);
+    return e;
+  }
   if (p.topk > 16) {
     cudaError_t e = launch_pdl(topk_radix_kernel, dim3(rows), dim3(kRadixThreads), 0, stream, p);
     note_launches(1);

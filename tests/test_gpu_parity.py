@@ -69,7 +69,8 @@ def test_index_pool_matches_oracle(msa, name):
 # ------------------------------------------------------------------ a2: top-k over given pooled rows
 @pytest.mark.parametrize("nb_max,topk,seed", [(40, 4, 0), (600, 16, 1), (1024, 16, 2), (5000, 8, 3),
                                               (8192, 16, 4), (3, 16, 5), (600, 32, 6), (8192, 64, 7),
-                                              (40, 64, 8), (300, 17, 9), (2000, 48, 10)])
+                                              (40, 64, 8), (300, 17, 9), (2000, 48, 10), (20000, 16, 11),
+                                              (32768, 64, 12), (40000, 16, 13), (2048, 1, 14), (3000, 2, 15)])
 def test_topk_pooled_matches_oracle_select(msa, nb_max, topk, seed):
     rng = np.random.default_rng(seed)
     # one sequence whose queries sit at positions spread over the whole context
