@@ -246,21 +246,28 @@ constexpr int kDecThreads = 128;  // compute warps; one more warp streams Q, K a
 constexpr int kOsumStride = 128 + 8;
 // Per CTA (two per SM): K and V buffers (32 KB each), the item's Q (4 KB),
 // the merge slices and per-warp (max, sum), the item hand-over, barriers.
+// fp8 K/V: the E4M3 codes of the item's K and V blocks (16 KB each) land in
+// the second half of the K and V buffers and are widened there in place.
 constexpr size_t kDecSmemBytes = 1024 + 65536 + 4096 + 4 * 16 * kOsumStride * sizeof(float) +
                                  4 * 16 * 2 * sizeof(float) + 32 + (4 + 5) * 8 + 16;
-// fp8 K/V: the E4M3 codes of the item's K and V blocks (16 KB each) land in a
-// staging area and the compute warps widen them into the bf16 K and V buffers
-// (one CTA per SM at this size).
-constexpr size_t kDec8Staging = 32768;
 
 // Widens one 128-byte row of E4M3 codes (TMA 128-byte swizzled, 16-byte chunks
-// XOR row % 8) into row `row` of a bf16 tile in the layout the bf16 loads give
-// (64-dim halves 16 KB apart, 128-byte swizzle).  Exact: an E4M3 value has 4
-// significant bits and fits bf16's exponent range.
-__device__ __forceinline__ void widen_e4m3_row(const uint8_t* src, uint8_t* dst, int row) {
+// XOR row % 8, at tile + 16 KB) into row `row` of the bf16 tile in the layout
+// the bf16 loads give (64-dim halves 16 KB apart, 128-byte swizzle).  The
+// codes sit where the tile's second half goes: row `row` of the widened
+// second half overwrites exactly the 128 bytes of that row's codes, so the
+// whole code row is read before anything is written, and each row belongs to
+// one thread.  Exact: an E4M3 value has 4 significant bits and fits bf16's
+// exponent range.
+__device__ __forceinline__ void widen_e4m3_row(uint8_t* tile, int row) {
+  const uint8_t* src = tile + 16384;
+  uint4 wr[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) wr[c] = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+  uint8_t* dst = tile;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c + 15
-    const uint4 w = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ (row & 7)) << 4));
+    const uint4 w = wr[c];
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
     uint32_t o[8];
 #pragma unroll
@@ -331,8 +338,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
   WsHeader* hdr = p.hdr;
   griddep_wait();  // the selection comes from the top-k kernel
   if (hdr->status & kFlagBadSeqlens) return;
-  uint8_t* stage8 = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* base = stage8 + (FP8 ? kDec8Staging : 0);                       // fp8: K codes 16 KB | V codes 16 KB
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = base;                                                    // K 32 KB | V 32 KB
   uint8_t* qbuf = base + 65536;                                            // Q 16 heads x 128 (4 KB)
   float* osum = reinterpret_cast<float*>(base + 65536 + 4096);             // [4 warps][16 heads][kOsumStride]
@@ -410,7 +416,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         tma_load_3d(qbuf, &tm_q, &full[0], 0, g * G + hs * 16, s);
         tma_load_3d(qbuf + 2048, &tm_q, &full[0], 64, g * G + hs * 16, s);
         if constexpr (FP8) {
-          tma_load_3d(stage8, &tm_k, &full[0], 0, g, krow);
+          tma_load_3d(ring + 16384, &tm_k, &full[0], 0, g, krow);
         } else {
           tma_load_3d(ring, &tm_k, &full[0], 0, g, krow);
           tma_load_3d(ring + 16384, &tm_k, &full[0], 64, g, krow);
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         }
         if constexpr (FP8) {
           mbar_arrive_expect_tx(&full[1], 16384);
-          tma_load_3d(stage8 + 16384, &tm_v, &full[1], 0, g, krow);
+          tma_load_3d(ring + 49152, &tm_v, &full[1], 0, g, krow);
         } else {
           mbar_arrive_expect_tx(&full[1], 32768);
           tma_load_3d(ring + 32768, &tm_v, &full[1], 0, g, krow);
@@ -473,8 +479,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
     const float sk = vinfo->sk, sv = vinfo->sv;
     if (sel < 0) break;
     if constexpr (FP8) {
-      // the previous item's K buffer is free (every compute warp arrived on empty[0] before these codes landed)
-      widen_e4m3_row(stage8, ring, threadIdx.x);
+      widen_e4m3_row(ring, threadIdx.x);
       if (!meet(3, n)) break;
     }
     const float scale_log2 = p.scale_log2 * sk;
@@ -505,6 +510,8 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       }
     }
     // this warp is done with Q, K and the item hand-over: the producer may load the next item's
+    // (fp8: into the K buffer this CTA's threads wrote, hence the proxy fence)
+    if constexpr (FP8) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[0]);
     // masked, scaled logits; per-head max and sum over this warp's keys
@@ -547,7 +554,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       break;
     }
     if constexpr (FP8) {
-      widen_e4m3_row(stage8 + 16384, ring + 32768, threadIdx.x);
+      widen_e4m3_row(ring + 32768, threadIdx.x);
       if (!meet(4, n)) break;
     }
     // O_w = P V over the warp's 32 keys: 2 k-steps of 16 keys, 16 n-tiles of 8 dims
@@ -577,6 +584,7 @@ __global__ void __launch_bounds__(kDecThreads + 32)
       }
     }
     // this warp is done with V
+    if constexpr (FP8) fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[1]);
     ++n;
@@ -666,10 +674,9 @@ cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const DecodeAttnParams& p, bool fp8, cudaStream_t stream) {
   const long long items = static_cast<long long>(p.num_seqs) * p.hkv * p.topk * (p.group >= 16 ? p.group / 16 : 1);
   if (items == 0) return cudaSuccess;
-  // persistent: two CTAs per SM (one with the fp8 staging area)
-  const long long per_sm = fp8 ? 1 : 2;
-  const long long grid = items < per_sm * p.sms ? items : per_sm * p.sms;
-  const size_t smem = kDecSmemBytes + (fp8 ? kDec8Staging : 0);
+  // persistent: two CTAs per SM
+  const long long grid = items < 2LL * p.sms ? items : 2LL * p.sms;
+  const size_t smem = kDecSmemBytes;
   auto* fn = fp8 ? decode_attn_kernel<true> : decode_attn_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
