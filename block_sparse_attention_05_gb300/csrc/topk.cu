@@ -18,7 +18,8 @@
 //
 // Long rows in small batches (decode: a few rows of thousands of blocks) take
 // topk_threshold_kernel: 1024 threads per row, each reducing its strided share
-// of the row to one maximum; a bitonic sort of those maxima gives the want-th
+// of the row to one maximum; a bitonic sort of those maxima (in registers:
+// shuffles within a warp, shared memory across warps) gives the want-th
 // largest, T.  At least want keys reach T (the want threads whose maxima do)
 // and at most want x (keys per thread) do, so the keys >= T are a small
 // candidate set holding the answer; each candidate's rank among them is
@@ -208,9 +209,11 @@ __global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p)
 constexpr int kThrThreads = 1024;
 constexpr int kThrMaxPerThread = 32;  // rows of up to 32 x 1024 blocks
 constexpr int kThrCandMax = 63 * kThrMaxPerThread;
+constexpr int kThrReg = 8;
 
 __global__ void __launch_bounds__(kThrThreads) topk_threshold_kernel(TopkParams p) {
-  __shared__ uint64_t tmax[kThrThreads];
+  __shared__ uint64_t xch[2][kThrThreads];  // bitonic exchanges between warps (double-buffered)
+  __shared__ uint64_t kth;
   __shared__ uint64_t cand[kThrCandMax];
   __shared__ int chosen[64];
   __shared__ int n_cand;
@@ -229,38 +232,62 @@ __global__ void __launch_bounds__(kThrThreads) topk_threshold_kernel(TopkParams 
   const float* pr = p.pooled + static_cast<int64_t>(row) * p.pooled_stride;
   int32_t* out = p.idx + static_cast<int64_t>(row) * p.topk;
   if (want > 0) {
+    // the first kThrReg keys of the thread's share stay in registers (all loads in flight at once); rows
+    // longer than kThrReg x 1024 blocks read the rest twice
+    float v[kThrReg];
+#pragma unroll
+    for (int r = 0; r < kThrReg; ++r) {
+      const int b = tid + r * kThrThreads;
+      v[r] = b < local ? pr[b] : 0.f;
+    }
     uint64_t mx = 0ull;
-    for (int b = tid; b < local; b += kThrThreads) {
+#pragma unroll
+    for (int r = 0; r < kThrReg; ++r) {
+      const int b = tid + r * kThrThreads;
+      const uint64_t key = b < local ? topk_key(v[r], b) : 0ull;
+      mx = key > mx ? key : mx;
+    }
+    for (int b = tid + kThrReg * kThrThreads; b < local; b += kThrThreads) {
       const uint64_t key = topk_key(pr[b], b);
       mx = key > mx ? key : mx;
     }
-    tmax[tid] = mx;
     if (tid == 0) n_cand = 0;
-    __syncthreads();
-    // bitonic sort of the maxima, descending
+    // bitonic sort of the maxima, descending, one key per thread in a register: partners closer than
+    // a warp exchange by shuffle, farther ones through shared memory
+    int xb = 0;
     for (int k = 2; k <= kThrThreads; k <<= 1) {
       for (int j = k >> 1; j > 0; j >>= 1) {
-        const int o = tid ^ j;
-        if (o > tid) {
-          const uint64_t a = tmax[tid], b = tmax[o];
-          if (((tid & k) == 0) ? (a < b) : (a > b)) {
-            tmax[tid] = b;
-            tmax[o] = a;
-          }
+        uint64_t y;
+        if (j < 32) {
+          y = __shfl_xor_sync(0xFFFFFFFFu, mx, j);
+        } else {
+          xch[xb][tid] = mx;
+          __syncthreads();
+          y = xch[xb][tid ^ j];
+          xb ^= 1;
         }
-        __syncthreads();
+        // the lower index of a pair keeps the larger key in a descending run ((tid & k) == 0)
+        const bool keep_max = ((tid & j) == 0) == ((tid & k) == 0);
+        mx = keep_max ? (y > mx ? y : mx) : (y < mx ? y : mx);
       }
     }
     // want <= min(local, 63) threads hold a key, so T > 0 is a real key
-    const uint64_t T = tmax[want - 1];
-    for (int b = tid; b < local; b += kThrThreads) {
-      const uint64_t key = topk_key(pr[b], b);
+    if (tid == want - 1) kth = mx;
+    __syncthreads();
+    const uint64_t T = kth;
+    // at most want x kThrMaxPerThread keys reach T; the guard only makes that explicit
+    auto keep = [&](uint64_t key) {
       if (key >= T) {
-        // at most want x kThrMaxPerThread keys reach T; the guard only makes that explicit
         const int c = atomicAdd(&n_cand, 1);
         if (c < kThrCandMax) cand[c] = key;
       }
+    };
+#pragma unroll
+    for (int r = 0; r < kThrReg; ++r) {
+      const int b = tid + r * kThrThreads;
+      if (b < local) keep(topk_key(v[r], b));
     }
+    for (int b = tid + kThrReg * kThrThreads; b < local; b += kThrThreads) keep(topk_key(pr[b], b));
     __syncthreads();
     const int nc = min(n_cand, kThrCandMax);
     // rank of each candidate among the candidates (keys are distinct); the want best are kept
