@@ -252,25 +252,19 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         for (int h = 0; h < 2; ++h) {  // block 2 bp + h: accumulator columns 128 h .. 128 h + 127
           const int b = 2 * bp + h;
           uint32_t r[4][32];
+          float cmax[4];  // the load's own maximum of each 32-column chunk
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c]);
-          tmem_ld_wait();
+          for (int c = 0; c < 4; ++c) tmem_ld_max_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c], cmax[c]);
+          tmem_ld_wait_max4(cmax);
           if (h == 1) {
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[ab]);
           }
           if (valid && b <= local) {
             const int lim = (b == local) ? (pos & 127) : 127;
-            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-            if (lim == 127) {
-#pragma unroll
-              for (int c = 0; c < 32; c += 2) {
-                m0 = fmax3(m0, __uint_as_float(r[0][c]), __uint_as_float(r[0][c + 1]));
-                m1 = fmax3(m1, __uint_as_float(r[1][c]), __uint_as_float(r[1][c + 1]));
-                m2 = fmax3(m2, __uint_as_float(r[2][c]), __uint_as_float(r[2][c + 1]));
-                m3 = fmax3(m3, __uint_as_float(r[3][c]), __uint_as_float(r[3][c + 1]));
-              }
-            } else {
+            float m0 = cmax[0], m1 = cmax[1], m2 = cmax[2], m3 = cmax[3];
+            if (lim < 127) {  // the query's own block: only keys up to its position
+              m0 = m1 = m2 = m3 = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
                 m0 = fmaxf(m0, c <= lim ? __uint_as_float(r[0][c]) : -INFINITY);
