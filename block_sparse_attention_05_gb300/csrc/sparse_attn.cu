@@ -512,15 +512,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           auto sval = [&](const uint32_t (&v)[32], int c, bool masked, int j) {
             return (!masked || c * 32 + j <= lim) ? __uint_as_float(v[j]) : -INFINITY;
           };
-          auto process = [&](const uint32_t (&v)[32], int c, bool masked) {
-            float t8[11];
+          // cmax: the load's own maximum of the step's 32 scores (used when no key is masked)
+          auto process = [&](const uint32_t (&v)[32], int c, bool masked, float cmax) {
+            float cm = cmax;
+            if (masked) {
+              float t8[11];
 #pragma unroll
-            for (int j = 0; j < 10; ++j)
-              t8[j] = fmax3(sval(v, c, masked, 3 * j), sval(v, c, masked, 3 * j + 1), sval(v, c, masked, 3 * j + 2));
-            t8[10] = fmaxf(sval(v, c, masked, 30), sval(v, c, masked, 31));
-            const float cm = fmaxf(fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]),
-                                         fmax3(t8[6], t8[7], t8[8])),
-                                   fmaxf(t8[9], t8[10]));
+              for (int j = 0; j < 10; ++j)
+                t8[j] = fmax3(sval(v, c, masked, 3 * j), sval(v, c, masked, 3 * j + 1), sval(v, c, masked, 3 * j + 2));
+              t8[10] = fmaxf(sval(v, c, masked, 30), sval(v, c, masked, 31));
+              cm = fmaxf(fmax3(fmax3(t8[0], t8[1], t8[2]), fmax3(t8[3], t8[4], t8[5]), fmax3(t8[6], t8[7], t8[8])),
+                         fmaxf(t8[9], t8[10]));
+            }
             if (c == 0) m_ref = (cm == -INFINITY) ? 0.f : cm * sc_log2;
             // The rescale uses warp-collective TMEM loads and stores, so the
             // whole warp enters it when any of its rows needs it; the other rows
@@ -550,30 +553,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               tmem_st_8cols(lane_addr + c * 16 + h * 8, pk);
             }
           };
-          tmem_ld_32cols(lane_addr, va);
-          tmem_ld_wait_regs(va);
+          float ma, mb;
+          tmem_ld_max_32cols(lane_addr, va, ma);
+          tmem_ld_wait_regs_max(va, ma);
           if (warp_full) {
-            tmem_ld_32cols(lane_addr + 32, vb);
-            process(va, 0, false);
-            tmem_ld_wait_regs(vb);
-            tmem_ld_32cols(lane_addr + 64, va);
-            process(vb, 1, false);
-            tmem_ld_wait_regs(va);
-            tmem_ld_32cols(lane_addr + 96, vb);
-            process(va, 2, false);
-            tmem_ld_wait_regs(vb);
-            process(vb, 3, false);
+            tmem_ld_max_32cols(lane_addr + 32, vb, mb);
+            process(va, 0, false, ma);
+            tmem_ld_wait_regs_max(vb, mb);
+            tmem_ld_max_32cols(lane_addr + 64, va, ma);
+            process(vb, 1, false, mb);
+            tmem_ld_wait_regs_max(va, ma);
+            tmem_ld_max_32cols(lane_addr + 96, vb, mb);
+            process(va, 2, false, ma);
+            tmem_ld_wait_regs_max(vb, mb);
+            process(vb, 3, false, mb);
           } else {
             tmem_ld_32cols(lane_addr + 32, vb);
-            process(va, 0, true);
+            process(va, 0, true, 0.f);
             tmem_ld_wait_regs(vb);
             tmem_ld_32cols(lane_addr + 64, va);
-            process(vb, 1, true);
+            process(vb, 1, true, 0.f);
             tmem_ld_wait_regs(va);
             tmem_ld_32cols(lane_addr + 96, vb);
-            process(va, 2, true);
+            process(va, 2, true, 0.f);
             tmem_ld_wait_regs(vb);
-            process(vb, 3, true);
+            process(vb, 3, true, 0.f);
           }
         }
         const float l = l2.x + l2.y;
