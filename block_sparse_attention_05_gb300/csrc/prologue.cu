@@ -11,9 +11,12 @@
 //
 // One GEMM, X [T, d_model] x W^T with W = the hkv query heads' rows followed
 // by the key head's (128 output columns each), on the tensor cores: work item
-// = 128 token rows x two heads (N = 256; a lone last head N = 128), K looped
-// in 64-column blocks, A and B tiles by TMA (128-byte swizzle) in a 4-stage
-// ring, tcgen05 MMAs into a double-buffered TMEM accumulator.  The epilogue
+// = 128 token rows x two heads (N = 256), or, for a lone last head, 256 token
+// rows x that head (two 128 x 128 MMAs sharing its weight tile, the second row
+// tile staged in the unused half of the weight stage), so every item does the
+// same 4.2 MFLOP per K step; K looped in 64-column blocks, A and B tiles by
+// TMA (128-byte swizzle) in a 4-stage ring, tcgen05 MMAs into a
+// double-buffered TMEM accumulator.  The epilogue
 // warps (one TMEM lane = one token row per thread) make two passes over each
 // head's 128 columns: the sum of squares, then normalisation, RoPE and the bf16
 // store.  The RoPE angle is reduced to a fraction of a turn before its sine
@@ -48,18 +51,32 @@ struct ProSmem {
 
 constexpr size_t kProSmemBytes = 1024 + kProStages * (kProATile + kProBTile) + sizeof(ProSmem);
 
-// Work item j of the persistent grid: row tile j / n_pairs, head pair j % n_pairs (heads 2p and 2p + 1;
-// head index hkv is the key head).
+// Work items, per 256 token rows (two row tiles): the head pairs (2p, 2p + 1) of row tile 0, then those of
+// row tile 1, then (n_heads odd) the lone last head over both row tiles.  Head index hkv is the key head.
+// Accumulator columns 0..127 and 128..255 hold slot 0 and slot 1: the pair's two heads, or the lone head's
+// two row tiles.
 struct ProItem {
-  int row0, h0, nh;  // first token row, first head, 1 or 2 heads
+  int row0, h0;
+  bool lone;  // one head over 256 rows (else two heads over 128 rows)
+  __device__ __forceinline__ int slot_row(int u) const { return lone ? row0 + 128 * u : row0; }
+  __device__ __forceinline__ int slot_head(int u) const { return lone ? h0 : h0 + u; }
 };
 
+__host__ __device__ __forceinline__ int pro_items_per_256(int hkv) {
+  const int n_heads = hkv + 1;
+  return 2 * (n_heads / 2) + (n_heads & 1);
+}
+__host__ __device__ __forceinline__ int pro_items(int total_q, int hkv) {
+  return ((total_q + 255) / 256) * pro_items_per_256(hkv);
+}
+
 __device__ __forceinline__ ProItem pro_item(const PrologueParams& p, int j) {
-  const int n_heads = p.hkv + 1, n_pairs = (n_heads + 1) / 2;
+  const int n_heads = p.hkv + 1, n_pairs = n_heads / 2, per = pro_items_per_256(p.hkv);
+  const int sub = j % per;
   ProItem it;
-  it.row0 = (j / n_pairs) * 128;
-  it.h0 = (j % n_pairs) * 2;
-  it.nh = min(2, n_heads - it.h0);
+  it.lone = sub >= 2 * n_pairs;
+  it.row0 = (j / per) * 256 + (it.lone ? 0 : (sub / n_pairs) * 128);
+  it.h0 = it.lone ? n_heads - 1 : (sub % n_pairs) * 2;
   return it;
 }
 
@@ -76,7 +93,7 @@ __global__ void __launch_bounds__(kProThreads, 1)
   uint8_t* b_buf = base + kProStages * kProATile;          // kProStages x 32 KB
   ProSmem& sm = *reinterpret_cast<ProSmem*>(base + kProStages * (kProATile + kProBTile));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = p.n_row_tiles * ((p.hkv + 2) / 2);
+  const int n_items = pro_items(p.total_q, p.hkv);
   const int kblocks = p.d_model / 64;
 
   if (threadIdx.x == 0) {
@@ -123,9 +140,12 @@ __global__ void __launch_bounds__(kProThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&sm.full[st], kProATile + w.nh * (kProBTile / 2));
+          // 48 KB either way: X 128 rows + two heads' weights, or X 2 x 128 rows (the second in the weight
+          // stage's upper half) + one head's weights (rows past the end read as zeros and count their bytes)
+          mbar_arrive_expect_tx(&sm.full[st], kProATile + kProBTile);
           tma_load_2d(a_buf + st * kProATile, &tm_x, &sm.full[st], kb * 64, w.row0);
-          for (int hh = 0; hh < w.nh; ++hh) {
+          if (w.lone) tma_load_2d(b_buf + st * kProBTile + kProBTile / 2, &tm_x, &sm.full[st], kb * 64, w.row0 + 128);
+          for (int hh = 0; hh < (w.lone ? 1 : 2); ++hh) {
             const int h = w.h0 + hh;
             uint8_t* dst = b_buf + st * kProBTile + hh * (kProBTile / 2);
             if (h < p.hkv) tma_load_2d(dst, &tm_wq, &sm.full[st], kb * 64, h * 128);
@@ -147,7 +167,7 @@ __global__ void __launch_bounds__(kProThreads, 1)
       bool ok = true;
       for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x, ++a_iter) {
         const ProItem w = pro_item(p, j);
-        const uint32_t idesc = idesc_bf16(128, 128 * w.nh, false);
+        const uint32_t idesc = idesc_bf16(128, w.lone ? 128 : 256, false);
         const int ab = a_iter & 1;
         if (a_iter >= 2 && !mbar_wait(&sm.acc_empty[ab], ((a_iter >> 1) - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 711);
@@ -163,10 +183,15 @@ __global__ void __launch_bounds__(kProThreads, 1)
           }
           tc_fence_after();
           const uint32_t aa = smem_u32(a_buf + st * kProATile), ba = smem_u32(b_buf + st * kProBTile);
+          const uint32_t acc = (kb > 0) ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < 4; ++kk) {
             umma_bf16(tmem + ab * 256, sdesc_sw128(aa + kk * 32, 16, 1024), sdesc_sw128(ba + kk * 32, 16, 1024),
-                      idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                      idesc, (acc || kk > 0) ? 1u : 0u);
+            if (w.lone)  // row tile 1 (its X in the weight stage's upper half) into columns 128..255
+              umma_bf16(tmem + ab * 256 + 128, sdesc_sw128(ba + kProBTile / 2 + kk * 32, 16, 1024),
+                        sdesc_sw128(ba + kk * 32, 16, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
+          }
           umma_commit(&sm.empty[st]);
         }
         if (!ok) break;
@@ -188,92 +213,94 @@ __global__ void __launch_bounds__(kProThreads, 1)
         break;
       }
       tc_fence_after();
-      const int i = w.row0 + r;
-      const bool valid = i < p.total_q;
-      int pos = 0;
-      long long krow = 0;
-      if (valid) {
-        const int s = find_seq(p.cu_q, p.num_seqs, i);
-        const SeqInfo si = p.seq[s];
-        pos = si.kv_len - si.q_len + (i - si.q_start);
-        krow = static_cast<long long>(si.k_start) + pos;
-      }
-      for (int hh = 0; hh < w.nh; ++hh) {
-        const int h = w.h0 + hh;
-        const uint32_t col = lane_addr + ab * 256 + hh * 128;
-        const float* gamma = sm.gamma[h < p.hkv ? 0 : 1];
-        // pass 1: sum of squares of the head's 128 projections
-        float ss = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32cols(col + c * 32, v);
-          tmem_ld_wait_regs(v);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(v[e]), __uint_as_float(v[e]), ss);
+      for (int hh = 0; hh < 2; ++hh) {  // accumulator slot: its rows and head
+        const int i = w.slot_row(hh) + r;
+        const bool valid = i < p.total_q;
+        int pos = 0;
+        long long krow = 0;
+        if (valid) {
+          const int s = find_seq(p.cu_q, p.num_seqs, i);
+          const SeqInfo si = p.seq[s];
+          pos = si.kv_len - si.q_len + (i - si.q_start);
+          krow = static_cast<long long>(si.k_start) + pos;
         }
-        const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + kRmsEps);
-        __nv_bfloat16* out = (h < p.hkv) ? p.q_idx + (static_cast<int64_t>(i) * p.hkv + h) * 128
-                                         : p.k_idx + krow * 128;
-        // pass 2: dims 0..63 (the RoPE pairs j, j + 32), then dims 64..127
         {
-          uint32_t a[32], b[32];
-          tmem_ld_32cols(col, a);
-          tmem_ld_32cols(col + 32, b);
-          tmem_ld_wait_regs(a);
-          tmem_ld_wait_regs(b);
-          uint32_t lo[16], hi[16];
-#pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            float2 za, zb;
-            float cs[2], sn[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              // fraction of a turn of pos * theta_j / (2 pi), with theta_j / (2 pi) = hi + lo (two floats):
-              // pos * hi = t + e exactly (fma), t - rint(t) is exact, and pos * lo is below 0.01 turns
-              const float fp = static_cast<float>(pos);
-              const float hi = p.rope_turns_hi[jj + u], lo = p.rope_turns_lo[jj + u];
-              const float t = fp * hi;
-              const float e = fmaf(fp, hi, -t);
-              const float f = (t - rintf(t)) + fmaf(fp, lo, e);
-              sincospif(2.0f * f, &sn[u], &cs[u]);
+          const int h = w.slot_head(hh);
+          const uint32_t col = lane_addr + ab * 256 + hh * 128;
+          const float* gamma = sm.gamma[h < p.hkv ? 0 : 1];
+          // pass 1: sum of squares of the head's 128 projections
+          float ss = 0.f;
+  #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld_32cols(col + c * 32, v);
+            tmem_ld_wait_regs(v);
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) ss = fmaf(__uint_as_float(v[e]), __uint_as_float(v[e]), ss);
+          }
+          const float inv = 1.0f / sqrtf(ss * (1.0f / 128.0f) + kRmsEps);
+          __nv_bfloat16* out = (h < p.hkv) ? p.q_idx + (static_cast<int64_t>(i) * p.hkv + h) * 128
+                                           : p.k_idx + krow * 128;
+          // pass 2: dims 0..63 (the RoPE pairs j, j + 32), then dims 64..127
+          {
+            uint32_t a[32], b[32];
+            tmem_ld_32cols(col, a);
+            tmem_ld_32cols(col + 32, b);
+            tmem_ld_wait_regs(a);
+            tmem_ld_wait_regs(b);
+            uint32_t lo[16], hi[16];
+  #pragma unroll
+            for (int jj = 0; jj < 32; jj += 2) {
+              float2 za, zb;
+              float cs[2], sn[2];
+  #pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                // fraction of a turn of pos * theta_j / (2 pi), with theta_j / (2 pi) = hi + lo (two floats):
+                // pos * hi = t + e exactly (fma), t - rint(t) is exact, and pos * lo is below 0.01 turns
+                const float fp = static_cast<float>(pos);
+                const float hi = p.rope_turns_hi[jj + u], lo = p.rope_turns_lo[jj + u];
+                const float t = fp * hi;
+                const float e = fmaf(fp, hi, -t);
+                const float f = (t - rintf(t)) + fmaf(fp, lo, e);
+                sincospif(2.0f * f, &sn[u], &cs[u]);
+              }
+              const float a0 = __uint_as_float(a[jj]) * inv * gamma[jj];
+              const float a1 = __uint_as_float(a[jj + 1]) * inv * gamma[jj + 1];
+              const float b0 = __uint_as_float(b[jj]) * inv * gamma[jj + 32];
+              const float b1 = __uint_as_float(b[jj + 1]) * inv * gamma[jj + 33];
+              za = make_float2(a0 * cs[0] - b0 * sn[0], a1 * cs[1] - b1 * sn[1]);
+              zb = make_float2(b0 * cs[0] + a0 * sn[0], b1 * cs[1] + a1 * sn[1]);
+              const __nv_bfloat162 pa = __floats2bfloat162_rn(za.x, za.y);
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(zb.x, zb.y);
+              lo[jj >> 1] = *reinterpret_cast<const uint32_t*>(&pa);
+              hi[jj >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
             }
-            const float a0 = __uint_as_float(a[jj]) * inv * gamma[jj];
-            const float a1 = __uint_as_float(a[jj + 1]) * inv * gamma[jj + 1];
-            const float b0 = __uint_as_float(b[jj]) * inv * gamma[jj + 32];
-            const float b1 = __uint_as_float(b[jj + 1]) * inv * gamma[jj + 33];
-            za = make_float2(a0 * cs[0] - b0 * sn[0], a1 * cs[1] - b1 * sn[1]);
-            zb = make_float2(b0 * cs[0] + a0 * sn[0], b1 * cs[1] + a1 * sn[1]);
-            const __nv_bfloat162 pa = __floats2bfloat162_rn(za.x, za.y);
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(zb.x, zb.y);
-            lo[jj >> 1] = *reinterpret_cast<const uint32_t*>(&pa);
-            hi[jj >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-          }
-          if (valid) {
-            uint4* o4 = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              o4[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
-              o4[4 + q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+            if (valid) {
+              uint4* o4 = reinterpret_cast<uint4*>(out);
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                o4[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+                o4[4 + q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+              }
             }
           }
-        }
-#pragma unroll
-        for (int c = 2; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32cols(col + c * 32, v);
-          tmem_ld_wait_regs(v);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[e]) * inv * gamma[c * 32 + e],
-                                                           __uint_as_float(v[e + 1]) * inv * gamma[c * 32 + e + 1]);
-            pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&t);
-          }
-          if (valid) {
-            uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  #pragma unroll
+          for (int c = 2; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld_32cols(col + c * 32, v);
+            tmem_ld_wait_regs(v);
+            uint32_t pk[16];
+  #pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[e]) * inv * gamma[c * 32 + e],
+                                                             __uint_as_float(v[e + 1]) * inv * gamma[c * 32 + e + 1]);
+              pk[e >> 1] = *reinterpret_cast<const uint32_t*>(&t);
+            }
+            if (valid) {
+              uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) o4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
           }
         }
       }
@@ -294,7 +321,7 @@ size_t index_prologue_smem_bytes() { return kProSmemBytes; }
 
 cudaError_t launch_index_prologue(const CUtensorMap& tx, const CUtensorMap& twq, const CUtensorMap& twk,
                                   const PrologueParams& p, int sms, cudaStream_t stream) {
-  const long long items = static_cast<long long>(p.n_row_tiles) * ((p.hkv + 2) / 2);
+  const long long items = pro_items(p.total_q, p.hkv);
   if (items == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(index_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kProSmemBytes));
