@@ -639,12 +639,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // contiguous in the partial buffer.  A quarter of the row (32 values)
         // at a time goes through this warp's staging area (16-byte chunks
         // XOR-swizzled by row pair, so neither side has bank conflicts) and
-        // leaves as 16-byte stores that fill whole 64-byte runs of 8 rows.
+        // leaves as 32-byte stores, two lanes per row, that fill whole 64-byte
+        // runs of 16 rows (half the store instructions of 16-byte stores:
+        // 10.38 -> 10.05 ms at 128K).
         const unsigned long long orow = rs.orow;
-        unsigned long long rowp[4];
+        unsigned long long rowp[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) rowp[k] = __shfl_sync(0xFFFFFFFFu, orow, 8 * k + (lane >> 2));
-        const int ck = lane & 3;  // the 16-byte chunk this lane stores
+        for (int k = 0; k < 2; ++k) rowp[k] = __shfl_sync(0xFFFFFFFFu, orow, 16 * k + (lane >> 1));
+        const int ck = (lane & 1) * 2;  // the first of the two 16-byte chunks this lane stores
         auto emit = [&](const uint32_t (&o)[32], int quarter) {
           uint4 pk[4];
 #pragma unroll
@@ -663,10 +665,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           }
           __syncwarp();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int R = 8 * k + (lane >> 2);
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + R * 64 + ((ck ^ ((R >> 1) & 3)) << 4));
-            if (rowp[k]) *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(rowp[k]) + quarter * 32 + ck * 8) = v;
+          for (int k = 0; k < 2; ++k) {
+            const int R = 16 * k + (lane >> 1);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(stg + R * 64 + ((ck ^ ((R >> 1) & 3)) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(stg + R * 64 + (((ck + 1) ^ ((R >> 1) & 3)) << 4));
+            if (rowp[k]) {
+              uint16_t* dst = reinterpret_cast<uint16_t*>(rowp[k]) + quarter * 32 + ck * 8;
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" :: "l"(dst), "r"(v0.x), "r"(v0.y),
+                           "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w) : "memory");
+            }
           }
           __syncwarp();
         };
