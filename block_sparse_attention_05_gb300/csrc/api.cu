@@ -861,7 +861,6 @@ msa_status_t msa_index_prologue(const msa_problem_t* problem, const void* x, int
   pp.total_q = c.d.T;
   pp.hkv = c.d.hkv;
   pp.d_model = d_model;
-  pp.n_row_tiles = (c.d.T + 127) / 128;
   pp.cu_q = problem->cu_seqlens_q;
   pp.seq = c.seq;
   pp.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);

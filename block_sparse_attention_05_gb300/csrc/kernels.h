@@ -196,7 +196,7 @@ cudaError_t launch_decode_attn(const CUtensorMap& tq, const CUtensorMap& tk, con
 // ---------------------------------------------------------------- index prologue
 // Hidden states -> Q_idx and the new tokens' K_idx rows (projection, RMSNorm, RoPE on dims 0..63).
 struct PrologueParams {
-  int num_seqs, total_q, hkv, d_model, n_row_tiles;
+  int num_seqs, total_q, hkv, d_model;
   const int32_t* cu_q;
   const SeqInfo* seq;
   const __nv_bfloat16* gamma_q;  // [128]
