@@ -113,6 +113,10 @@ for _fn in (_lib.msa_sparse_attn_prefill_fp8, _lib.msa_sparse_attn_decode_fp8):
     _fn.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_forward_fp8.restype = ctypes.c_int
 _lib.msa_forward_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+# problem, q, k8, v8, k_scale, v_scale, q_idx, k_idx cache, block table, stride, pages, idx, o, lse, ws, bytes, stream
+_lib.msa_forward_decode_paged_fp8.restype = ctypes.c_int
+_lib.msa_forward_decode_paged_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, _i64, _vp,
+                                              _vp, _vp, _vp, _sz, _vp]
 _lib.msa_index_prologue.restype = ctypes.c_int
 _lib.msa_index_prologue.argtypes = [_P, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
@@ -127,7 +131,8 @@ EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_inde
             "msa_read_device_status", "msa_status_string", "msa_abi_version", "msa_set_stage_events",
             "msa_kernel_launch_count", "msa_last_error_detail", "msa_sparse_attn_decode_static",
             "msa_forward_decode_paged", "msa_quantize_kv_fp8", "msa_sparse_attn_prefill_fp8",
-            "msa_sparse_attn_decode_fp8", "msa_forward_fp8", "msa_index_prologue")
+            "msa_sparse_attn_decode_fp8", "msa_forward_fp8", "msa_index_prologue",
+            "msa_forward_decode_paged_fp8")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 
@@ -423,6 +428,38 @@ def msa_forward_fp8(problem: Problem, q, k8, v8, k_scale, v_scale, q_idx, k_idx,
     _check(_lib.msa_forward_fp8(ctypes.byref(problem.c()), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale), _ptr(v_scale),
                                 _ptr(q_idx), _ptr(k_idx), _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()),
            "msa_forward_fp8")
+    return idx, o, lse
+
+
+def msa_forward_decode_paged_fp8(problem: Problem, q, k8_cache, v8_cache, k_scale, v_scale, q_idx, k_idx_cache,
+                                 block_table, idx=None, o=None, lse=None, ws=None):
+    """Decode from paged fp8 caches: E4M3 codes [num_pages * 128, hkv, 128] with one scale row per page
+    (k_scale / v_scale [num_pages, hkv]); bf16 q, q_idx and index-key cache; block_table int32
+    [num_seqs, max_blocks].  Returns (idx, o, lse) as msa_forward."""
+    for t, n in ((q, "q"), (q_idx, "q_idx"), (k_idx_cache, "k_idx_cache")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((k8_cache, "k8_cache"), (v8_cache, "v8_cache")):
+        _need(t, torch.uint8, n)
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or k8_cache.shape[0] % 128:
+        raise ValueError("block_table must be [num_seqs, max_blocks] and the caches whole pages of 128 rows")
+    n_pages = k8_cache.shape[0] // 128
+    if k_scale.numel() < n_pages * problem.hkv or v_scale.numel() < n_pages * problem.hkv:
+        raise ValueError("k_scale and v_scale need one row of num_kv_heads scales per page")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.FORWARD_FP8, ws)
+    _check(_lib.msa_forward_decode_paged_fp8(ctypes.byref(problem.c()), _ptr(q), _ptr(k8_cache), _ptr(v8_cache),
+                                             _ptr(k_scale), _ptr(v_scale), _ptr(q_idx), _ptr(k_idx_cache),
+                                             _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx), _ptr(o),
+                                             _ptr(lse), _ptr(ws), nws, _stream()), "msa_forward_decode_paged_fp8")
     return idx, o, lse
 
 

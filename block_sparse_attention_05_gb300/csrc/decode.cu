@@ -408,7 +408,11 @@ __global__ void __launch_bounds__(kDecThreads + 32)
         info->sk = 1.f;
         info->sv = 1.f;
         if constexpr (FP8) {
-          const long long srow = (static_cast<long long>(p.blk_off[s]) + b) * p.hkv + g;
+          // the block's scales: per key block of the sequence (packed) or per page (paged; a page outside the
+          // cache, already flagged, reads page 0's)
+          const long long pg = krow >> 7;
+          const long long srow =
+              (p.block_table ? (pg < p.n_pages ? pg : 0) : static_cast<long long>(p.blk_off[s]) + b) * p.hkv + g;
           info->sk = p.k_scale[srow];
           info->sv = p.v_scale[srow];
         }

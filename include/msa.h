@@ -92,7 +92,7 @@ typedef enum msa_status {
 #define MSA_DEVICE_TIMEOUT 1u        /* a kernel wait exceeded its time limit */
 #define MSA_DEVICE_BAD_SEQLENS 2u    /* cu_seqlens disagree with the host sizes */
 #define MSA_DEVICE_BAD_INDEX 4u      /* a computed index failed its check (checked builds), or a block-table
-                                        entry of msa_forward_decode_paged named a page outside the cache */
+                                        entry of msa_forward_decode_paged(_fp8) named a page outside the cache */
 
 typedef struct msa_problem {
   int32_t num_seqs;              /* >= 1 */
@@ -292,8 +292,11 @@ msa_status_t msa_index_prologue(const msa_problem_t *problem, const void *x, int
  * fp8 Main Branch computes exactly the bf16 one over the dequantized values
  * (value = code * scale); results differ from bf16 K/V by the quantization.
  * Decode reads the codes directly (half the K/V bytes); prefill widens them
- * once per call into exact 16-bit copies in the workspace.  Paged caches are
- * bf16 only.
+ * once per call into exact 16-bit copies in the workspace.  A paged decode
+ * cache (msa_forward_decode_paged_fp8) has one scale row per page instead:
+ * k_scale / v_scale [num_pages, num_kv_heads]; msa_quantize_kv_fp8 produces
+ * exactly that layout when given the page pool as one sequence of
+ * num_pages * 128 keys (each page is then one key block).
  * ------------------------------------------------------------------------ */
 
 /* bf16 K and V -> E4M3 codes and scales as above (msa_workspace_size op
@@ -321,6 +324,19 @@ msa_status_t msa_forward_fp8(const msa_problem_t *problem, const void *q, const 
                              const float *k_scale, const float *v_scale, const void *q_idx, const void *k_idx,
                              int32_t *idx, void *o, float *lse, void *workspace, size_t workspace_bytes,
                              msa_stream_t stream);
+
+/* msa_forward_decode_paged with fp8 K and V caches (op MSA_OP_FORWARD_FP8):
+ * k8_cache, v8_cache [num_pages * 128, num_kv_heads, 128] E4M3 codes, and
+ * k_scale, v_scale [num_pages, num_kv_heads] fp32, one row per page (see
+ * above); the Index Branch reads the bf16 k_idx_cache as in
+ * msa_forward_decode_paged.  Arguments, block table, errors and the device
+ * flag for a page outside the cache as for msa_forward_decode_paged. */
+msa_status_t msa_forward_decode_paged_fp8(const msa_problem_t *problem, const void *q, const void *k8_cache,
+                                          const void *v8_cache, const float *k_scale, const float *v_scale,
+                                          const void *q_idx, const void *k_idx_cache, const int32_t *block_table,
+                                          int32_t max_blocks_per_seq, int64_t num_pages, int32_t *idx, void *o,
+                                          float *lse, void *workspace, size_t workspace_bytes,
+                                          msa_stream_t stream);
 
 /* Waits for `stream`, then returns in *flags the MSA_DEVICE_* bits that the
  * last call on this workspace raised (0 = none).  workspace = NULL reads the

@@ -124,6 +124,21 @@ def test_paged_decode_rejects_bad_arguments_on_the_host(msa):
     assert lib.msa_forward_decode_paged(ctypes.byref(pre), *args()[1:]) == -1
 
 
+def test_paged_fp8_decode_rejects_bad_arguments_on_the_host(msa):
+    lib = msa._lib
+    dec = base_problem(msa, num_seqs=4, total_q=4, max_seqlen_q=1)
+    p = ctypes.byref(dec)
+    args = lambda ks=FAKE, bt=FAKE, mb=16, npg=100: (p, FAKE, FAKE, FAKE, ks, FAKE, FAKE, FAKE, bt, mb, npg, FAKE,
+                                                      FAKE, FAKE, FAKE, 1 << 40, None)
+    assert lib.msa_forward_decode_paged_fp8(*args(ks=None)) == -1     # no K scales
+    assert lib.msa_forward_decode_paged_fp8(*args(ks=FAKE + 2)) == -3 # misaligned scales
+    assert lib.msa_forward_decode_paged_fp8(*args(bt=None)) == -1     # no block table
+    assert lib.msa_forward_decode_paged_fp8(*args(npg=0)) == -1       # no pages
+    assert lib.msa_forward_decode_paged_fp8(*args(mb=7)) == -1        # a row cannot hold the longest sequence
+    pre = base_problem(msa)                                           # a prefill batch
+    assert lib.msa_forward_decode_paged_fp8(ctypes.byref(pre), *args()[1:]) == -1
+
+
 def test_status_strings(msa):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert msa._lib.msa_status_string(code)

@@ -143,3 +143,59 @@ def test_forward_fp8_prefill_end_to_end(msa):
     o8, l8 = oracle.attention_fp8(x.cu_q, x.cu_k, x.q, k8, v8, ks[:nkb], vs[:nkb], ref["idx"], block=cfg.block)
     assert_attention_close(to_np(o), to_np(lse), {"o": o8, "lse": l8}, cfg.hq // cfg.hkv, exempt=tie,
                            what="forward fp8")
+
+
+# ------------------------------------------------------------------ paged fp8 decode caches
+@pytest.mark.parametrize("n,ctx,seed", [(6, 9000, 51), (3, 40000, 52), (2, 200, 53)])
+def test_forward_decode_paged_fp8(msa, n, ctx, seed):
+    """Paged fp8 caches (E4M3 codes in pages of 128 rows, one scale row per page) give the packed fp8 path's
+    results bit for bit, and quantizing the bf16 page pool as one sequence of num_pages * 128 keys yields
+    exactly those codes and per-page scales."""
+    cfg = workloads.configs.Workload("dec8p", None, seed=seed, decode_batch=n, decode_ctx=ctx, topk=16,
+                                     n_topics=16, hq=64, hkv=4)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    k8, v8, ks, vs, nkb = _quantized(msa, x, prob, cfg)
+    cu_k = x.cu_k.cpu().numpy()
+    nbs = [int(cu_k[s + 1] - cu_k[s] + 127) // 128 for s in range(n)]
+    n_pages = sum(nbs) + 3
+    perm = np.random.default_rng(seed).permutation(n_pages)
+    bt = np.full((n, max(nbs) + 2), -7, np.int32)
+    rows = (n_pages * 128,) + tuple(x.k.shape[1:])
+    k8c = torch.zeros(rows, dtype=torch.uint8, device="cuda")
+    v8c = torch.zeros_like(k8c)
+    k_c = torch.zeros(rows, dtype=torch.bfloat16, device="cuda")
+    v_c = torch.zeros_like(k_c)
+    ki_c = torch.zeros((n_pages * 128,) + tuple(x.k_idx.shape[1:]), dtype=x.k_idx.dtype, device="cuda")
+    ksc = torch.ones((n_pages, cfg.hkv), dtype=torch.float32, device="cuda")
+    vsc = torch.ones_like(ksc)
+    at = blk = 0
+    used = []
+    for s in range(n):
+        for b in range(nbs[s]):
+            pg = int(perm[at])
+            at += 1
+            bt[s, b] = pg
+            lo, hi = int(cu_k[s]) + 128 * b, min(int(cu_k[s]) + 128 * (b + 1), int(cu_k[s + 1]))
+            dst = slice(pg * 128, pg * 128 + hi - lo)
+            k8c[dst], v8c[dst], k_c[dst], v_c[dst], ki_c[dst] = k8[lo:hi], v8[lo:hi], x.k[lo:hi], x.v[lo:hi], \
+                x.k_idx[lo:hi]
+            ksc[pg], vsc[pg] = ks[blk], vs[blk]
+            used.append((pg, hi - lo))
+            blk += 1
+    bt = torch.from_numpy(bt).cuda()
+    ws = msa.workspace(prob, msa.Op.FORWARD_FP8)
+    idx, o, lse = msa.msa_forward_decode_paged_fp8(prob, x.q, k8c, v8c, ksc, vsc, x.q_idx, ki_c, bt, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
+    idx_r, o_r, lse_r = msa.msa_forward_fp8(prob, x.q, k8, v8, ks, vs, x.q_idx, x.k_idx)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_r) and torch.equal(o, o_r) and torch.equal(lse, lse_r)
+    # the recommended quantization of a page pool: one sequence of num_pages * 128 keys, a key block per page
+    pool = msa.problem_from_seqlens([1], [n_pages * 128], hq=cfg.hq, hkv=cfg.hkv, d_idx=cfg.d_idx, topk=cfg.topk)
+    k8q, v8q, ksq, vsq = msa.msa_quantize_kv_fp8(pool, k_c, v_c)
+    torch.cuda.synchronize()
+    for pg, nrow in used:
+        r = slice(pg * 128, pg * 128 + nrow)
+        assert torch.equal(k8q[r], k8c[r]) and torch.equal(v8q[r], v8c[r]), pg
+        assert torch.equal(ksq[pg], ksc[pg]) and torch.equal(vsq[pg], vsc[pg]), pg
