@@ -669,11 +669,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int R = 16 * k + (lane >> 1);
             const uint4 v0 = *reinterpret_cast<const uint4*>(stg + R * 64 + ((ck ^ ((R >> 1) & 3)) << 4));
             const uint4 v1 = *reinterpret_cast<const uint4*>(stg + R * 64 + (((ck + 1) ^ ((R >> 1) & 3)) << 4));
-            if (rowp[k]) {
-              uint16_t* dst = reinterpret_cast<uint16_t*>(rowp[k]) + quarter * 32 + ck * 8;
-              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" :: "l"(dst), "r"(v0.x), "r"(v0.y),
-                           "r"(v0.z), "r"(v0.w), "r"(v1.x), "r"(v1.y), "r"(v1.z), "r"(v1.w) : "memory");
-            }
+            if (rowp[k]) st_global_32b(reinterpret_cast<uint16_t*>(rowp[k]) + quarter * 32 + ck * 8, v0, v1);
           }
           __syncwarp();
         };
