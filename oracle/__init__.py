@@ -19,7 +19,10 @@ blocks", section "The mechanism, precisely", and its Figure 1):
   * ``quantize_fp8``, ``e4m3_value``, ``e4m3_code``, ``attention_fp8`` -- fp8
     (E4M3) K/V with one scale per (key block, KV head), and the Main Branch
     over such K/V (the atlas record of the report: the kernels "also support
-    fp8"; the format is a reading, see ``msa_oracle.c``).
+    fp8"; the format is a reading, see ``msa_oracle.c``);
+  * ``quantize_index_fp8``, ``pooled_fp8``, ``index_fp8`` -- the same codes for
+    the index inputs (K_idx: one scale per key block; Q_idx: one per query row
+    and group), and the Index Branch over them.
 """
 from __future__ import annotations
 
@@ -73,6 +76,12 @@ def _load(path: str | None = None):
             lib.msa_oracle_index.argtypes = [
                 ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 _u16p, _u16p, ctypes.c_int, _i32p, _i32p, _f64p]
+            lib.msa_oracle_pooled_fp8.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u8p, _f32p, _u8p, _f32p, ctypes.c_int, _i32p, ctypes.c_int, _f32p]
+            lib.msa_oracle_index_fp8.argtypes = [
+                ctypes.c_int, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _u8p, _f32p, _u8p, _f32p, ctypes.c_int, _i32p, _i32p, _f64p]
             lib.msa_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
             lib.msa_oracle_e4m3_value.restype = ctypes.c_double
             lib.msa_oracle_e4m3_code.argtypes = [ctypes.c_float]
@@ -90,7 +99,8 @@ def _load(path: str | None = None):
                 _f64p, _f64p]
             for fn in (lib.msa_oracle_pooled, lib.msa_oracle_select, lib.msa_oracle_attention,
                        lib.msa_oracle_forward, lib.msa_oracle_index, lib.msa_oracle_key_blocks,
-                       lib.msa_oracle_quantize_fp8, lib.msa_oracle_attention_fp8, lib.msa_oracle_index_prologue):
+                       lib.msa_oracle_quantize_fp8, lib.msa_oracle_attention_fp8, lib.msa_oracle_index_prologue,
+                       lib.msa_oracle_pooled_fp8, lib.msa_oracle_index_fp8):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -315,6 +325,54 @@ def attention_fp8(cu_q, cu_k, q, k8, v8, k_scale, v_scale, idx, block: int, scal
                                           _ptr(rows_a, _i32p), _ptr(o, _f64p), _ptr(lse, _f64p))
     _check(rc, "attention_fp8")
     return o, lse
+
+
+def quantize_index_fp8(cu_q, cu_k, q_idx, k_idx, block: int):
+    """fp8 copies of the index inputs: (q8 [total_q, Hkv, d_idx] uint8, q_scale [total_q, Hkv] fp32,
+    k8 [total_k, d_idx] uint8, k_scale [key blocks] fp32).  K_idx is quantized per key block of a sequence,
+    Q_idx per (query row, group): the same quantizer, the query rows taken as blocks of one row."""
+    qb, kb = _bits(q_idx), _bits(k_idx)
+    total_k, d_idx = kb.shape
+    k8, k_scale = quantize_fp8(cu_k, kb.reshape(total_k, 1, d_idx), block)
+    total_q = qb.shape[0]
+    q8, q_scale = quantize_fp8(np.arange(total_q + 1, dtype=np.int32), qb, 1)
+    return q8, q_scale, k8.reshape(total_k, d_idx), k_scale.reshape(-1)
+
+
+def pooled_fp8(cu_q, cu_k, q8, q_scale, k8, k_scale, block: int, rows=None, nb_stride: int | None = None):
+    """``pooled`` over E4M3 index inputs (codes and scales as ``quantize_index_fp8`` gives them)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    q8a, k8a, qs, ks = _u8(q8), _u8(k8), _f32(q_scale), _f32(k_scale)
+    total_q, hkv, d_idx = q8a.shape
+    assert k8a.shape == (int(cu_k[-1]), d_idx) and qs.shape == (total_q, hkv)
+    assert ks.size >= key_blocks(cu_k, block)
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    nb_stride = nb_stride or max_blocks(cu_k, block)
+    out = np.empty((n_rows, hkv, nb_stride), np.float32)
+    rc = _load().msa_oracle_pooled_fp8(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hkv, d_idx, block,
+                                       _ptr(q8a, _u8p), _ptr(qs, _f32p), _ptr(k8a, _u8p), _ptr(ks, _f32p), n_rows,
+                                       _ptr(rows_a, _i32p), nb_stride, _ptr(out, _f32p))
+    _check(rc, "pooled_fp8")
+    return out
+
+
+def index_fp8(cu_q, cu_k, q8, q_scale, k8, k_scale, block: int, topk: int, rows=None):
+    """``index`` over E4M3 index inputs.  Returns dict(idx [n,Hkv,k] i32, gap [n,Hkv] f64)."""
+    cu_q, cu_k = _i32(cu_q), _i32(cu_k)
+    q8a, k8a, qs, ks = _u8(q8), _u8(k8), _f32(q_scale), _f32(k_scale)
+    total_q, hkv, d_idx = q8a.shape
+    assert k8a.shape == (int(cu_k[-1]), d_idx) and qs.shape == (total_q, hkv)
+    assert ks.size >= key_blocks(cu_k, block)
+    rows_a = None if rows is None else _i32(rows)
+    n_rows = total_q if rows_a is None else rows_a.size
+    idx = np.empty((n_rows, hkv, topk), np.int32)
+    gap = np.empty((n_rows, hkv), np.float64)
+    rc = _load().msa_oracle_index_fp8(len(cu_q) - 1, _ptr(cu_q, _i32p), _ptr(cu_k, _i32p), hkv, d_idx, block, topk,
+                                      _ptr(q8a, _u8p), _ptr(qs, _f32p), _ptr(k8a, _u8p), _ptr(ks, _f32p), n_rows,
+                                      _ptr(rows_a, _i32p), _ptr(idx, _i32p), _ptr(gap, _f64p))
+    _check(rc, "index_fp8")
+    return {"idx": idx, "gap": gap}
 
 
 def query_positions(cu_q, cu_k) -> np.ndarray:

@@ -22,7 +22,9 @@
  *     local block is forced in and that selection is per query and per group.
  *     Ranking: pooled score descending, ties to the lower block index.
  *
- *     msa_oracle_index chains steps 1 and 2 (the Index Branch alone).
+ *     msa_oracle_index chains steps 1 and 2 (the Index Branch alone);
+ *     msa_oracle_pooled_fp8 and msa_oracle_index_fp8 do the same over E4M3
+ *     index inputs (see the fp8 notes near the end of the file).
  *
  *  3. msa_oracle_attention -- Main Branch: exact softmax attention of every
  *     query head over only the tokens of its group's selected blocks.  Same
@@ -109,24 +111,63 @@ static int seq_of_query(int num_seqs, const int32_t *cu_q, int i) {
 
 int msa_oracle_num_blocks(int pos, int block) { return pos / block + 1; }
 
+double msa_oracle_e4m3_value(uint8_t code);
+
+/* The inputs of step 1, in one of two forms: bf16 bits (q_idx, k_idx), or
+ * E4M3 codes with fp32 scales (q8, k8; the fp8 index notes below), each
+ * element then read as value(code) * scale.  The scores are the same
+ * definition on those values. */
+typedef struct {
+  const uint16_t *q_idx, *k_idx; /* bf16: [total_q][hkv][d_idx], [total_k][d_idx] */
+  const uint8_t *q8, *k8;        /* E4M3: same shapes */
+  const float *q_scale;          /* [total_q][hkv]: one per (query row, group) */
+  const float *k_scale;          /* [n_key_blocks]: one per key block of a sequence */
+} index_inputs;
+
+/* Index keys of sequence s widened to double, kd[j * d_idx + d] for its
+ * kv_len keys; blk0 = scale row of the sequence's first key block. */
+static void widen_keys(const index_inputs *in, const int32_t *cu_k, int s, int d_idx, int block, int blk0,
+                       double *kd) {
+  const int kv_len = cu_k[s + 1] - cu_k[s];
+  for (int j = 0; j < kv_len; ++j)
+    for (int d = 0; d < d_idx; ++d) {
+      const size_t e = (size_t)(cu_k[s] + j) * d_idx + d;
+      kd[(size_t)j * d_idx + d] = in->k8 ? msa_oracle_e4m3_value(in->k8[e]) * (double)in->k_scale[blk0 + j / block]
+                                         : bf16_bits_to_double(in->k_idx[e]);
+    }
+}
+
+/* Index query row i (all groups) widened to double, qd[g * d_idx + d]. */
+static void widen_query(const index_inputs *in, int i, int hkv, int d_idx, double *qd) {
+  for (int g = 0; g < hkv; ++g)
+    for (int d = 0; d < d_idx; ++d) {
+      const size_t e = ((size_t)i * hkv + g) * d_idx + d;
+      qd[g * d_idx + d] = in->q8 ? msa_oracle_e4m3_value(in->q8[e]) * (double)in->q_scale[(size_t)i * hkv + g]
+                                 : bf16_bits_to_double(in->q_idx[e]);
+    }
+}
+
 /*
  * Step 1.  pooled[r][g][b] for query row rows[r] (all rows when rows == NULL,
  * then n_rows must equal total_q) and group g:
  *     s_j      = fp32( sum_d q_idx[i][g][d] * k_idx[key j][d] )   (sum in double)
  *     pooled_b = max over keys j of block b with j <= pos of s_j  (fp32)
  * for b = 0 .. pos / block.  Entries b > pos / block are set to -INFINITY.
+ * The bf16 inputs and their products are exact in double; so are E4M3 values
+ * times fp32 scales, whose products carry up to 56 significant bits and are
+ * rounded to double (far below the final rounding to fp32).
  */
-int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
-                      int hkv, int d_idx, int block,
-                      const uint16_t *q_idx, const uint16_t *k_idx,
-                      int n_rows, const int32_t *rows,
-                      int nb_stride, float *pooled) {
+static int pooled_core(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                       int hkv, int d_idx, int block, const index_inputs *in,
+                       int n_rows, const int32_t *rows,
+                       int nb_stride, float *pooled) {
   if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
   if (hkv <= 0 || d_idx <= 0 || block <= 0 || n_rows < 0 || !pooled) return ORACLE_EINVAL;
+  if (in->q8 ? (!in->k8 || !in->q_scale || !in->k_scale) : (!in->q_idx || !in->k_idx)) return ORACLE_EINVAL;
   const int total_q = cu_q[num_seqs];
   if (!rows && n_rows != total_q) return ORACLE_EINVAL;
   /* The rows are processed one sequence at a time, with that sequence's index
-   * keys widened once to double (exact) while its rows are scored. */
+   * keys widened once to double while its rows are scored. */
   int bad = 0;
   int *row_seq = (int *)malloc(sizeof(int) * (size_t)(n_rows > 0 ? n_rows : 1));
   if (!row_seq) return ORACLE_ENOMEM;
@@ -135,7 +176,8 @@ int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
     row_seq[r] = (i >= 0 && i < total_q) ? seq_of_query(num_seqs, cu_q, i) : -1;
     if (row_seq[r] < 0) bad = 1;
   }
-  for (int s = 0; s < num_seqs && !bad; ++s) {
+  int blk0 = 0; /* scale row of sequence s's first key block */
+  for (int s = 0; s < num_seqs && !bad; blk0 += (cu_k[s + 1] - cu_k[s] + block - 1) / block, ++s) {
     int used = 0;
     for (int r = 0; r < n_rows && !used; ++r) used = (row_seq[r] == s);
     if (!used) continue;
@@ -143,8 +185,7 @@ int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
     const int kv_len = cu_k[s + 1] - cu_k[s];
     double *kd = (double *)malloc(sizeof(double) * (size_t)(kv_len > 0 ? kv_len : 1) * d_idx);
     if (!kd) { bad = 1; break; }
-    for (size_t e = 0; e < (size_t)kv_len * d_idx; ++e)
-      kd[e] = bf16_bits_to_double(k_idx[(size_t)cu_k[s] * d_idx + e]);
+    widen_keys(in, cu_k, s, d_idx, block, blk0, kd);
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
     for (int r = 0; r < n_rows; ++r) {
       if (row_seq[r] != s) continue;
@@ -154,7 +195,7 @@ int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
       if (nb > nb_stride) { bad = 1; continue; }
       double *qd = (double *)malloc(sizeof(double) * (size_t)hkv * d_idx);  /* qd[g * d_idx + d] */
       if (!qd) { bad = 1; continue; }
-      for (int e = 0; e < hkv * d_idx; ++e) qd[e] = bf16_bits_to_double(q_idx[(size_t)i * hkv * d_idx + e]);
+      widen_query(in, i, hkv, d_idx, qd);
       float *out = pooled + (size_t)r * hkv * nb_stride;  /* out[g * nb_stride + b] */
       for (int e = 0; e < hkv * nb_stride; ++e) out[e] = -INFINITY;
       for (int b = 0; b < nb; ++b) {
@@ -181,6 +222,15 @@ int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   }
   free(row_seq);
   return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+int msa_oracle_pooled(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                      int hkv, int d_idx, int block,
+                      const uint16_t *q_idx, const uint16_t *k_idx,
+                      int n_rows, const int32_t *rows,
+                      int nb_stride, float *pooled) {
+  const index_inputs in = {q_idx, k_idx, NULL, NULL, NULL, NULL};
+  return pooled_core(num_seqs, cu_q, cu_k, hkv, d_idx, block, &in, n_rows, rows, nb_stride, pooled);
 }
 
 /*
@@ -320,11 +370,10 @@ int msa_oracle_attention(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
  * (all when NULL): idx [n_rows][hkv][topk] (ascending, -1 padded) and gap
  * [n_rows][hkv] (see msa_oracle_select).
  */
-int msa_oracle_index(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
-                     int hkv, int d_idx, int block, int topk,
-                     const uint16_t *q_idx, const uint16_t *k_idx,
-                     int n_rows, const int32_t *rows,
-                     int32_t *idx, double *gap) {
+static int index_core(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                      int hkv, int d_idx, int block, int topk, const index_inputs *in,
+                      int n_rows, const int32_t *rows,
+                      int32_t *idx, double *gap) {
   if (check_seqlens(num_seqs, cu_q, cu_k)) return ORACLE_EINVAL;
   if (hkv <= 0 || block <= 0 || topk <= 0 || !idx || n_rows < 0) return ORACLE_EINVAL;
   int max_nb = 1;
@@ -337,8 +386,7 @@ int msa_oracle_index(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   }
   float *pooled = (float *)malloc(sizeof(float) * (size_t)(n_rows > 0 ? n_rows : 1) * hkv * max_nb);
   if (!pooled) return ORACLE_ENOMEM;
-  int rc = msa_oracle_pooled(num_seqs, cu_q, cu_k, hkv, d_idx, block, q_idx, k_idx,
-                             n_rows, rows, max_nb, pooled);
+  int rc = pooled_core(num_seqs, cu_q, cu_k, hkv, d_idx, block, in, n_rows, rows, max_nb, pooled);
   if (rc) { free(pooled); return rc; }
   int bad = 0;
 #pragma omp parallel for schedule(dynamic, 64) reduction(| : bad)
@@ -354,6 +402,15 @@ int msa_oracle_index(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
   }
   free(pooled);
   return bad ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+int msa_oracle_index(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                     int hkv, int d_idx, int block, int topk,
+                     const uint16_t *q_idx, const uint16_t *k_idx,
+                     int n_rows, const int32_t *rows,
+                     int32_t *idx, double *gap) {
+  const index_inputs in = {q_idx, k_idx, NULL, NULL, NULL, NULL};
+  return index_core(num_seqs, cu_q, cu_k, hkv, d_idx, block, topk, &in, n_rows, rows, idx, gap);
 }
 
 /*
@@ -462,6 +519,36 @@ int msa_oracle_quantize_fp8(int num_seqs, const int32_t *cu_k, int hkv, int head
     }
   }
   return ORACLE_OK;
+}
+
+/*
+ * fp8 index (the same provenance; the pages give no format, and the report
+ * warns that quantizing the index changes which blocks are selected, so this
+ * is an option beside the bf16 index, not a replacement): Q_idx and K_idx as
+ * E4M3 codes with the quantizer above, K_idx with one scale per key block of a
+ * sequence (msa_oracle_quantize_fp8 with hkv = 1, head_dim = d_idx) and Q_idx
+ * with one scale per (query row, group) (the same quantizer over the query
+ * rows with block = 1: scales [total_q][hkv]).  Steps 1 and 2 then run
+ * unchanged on the dequantized values.
+ */
+int msa_oracle_pooled_fp8(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                          int hkv, int d_idx, int block,
+                          const uint8_t *q8, const float *q_scale, const uint8_t *k8, const float *k_scale,
+                          int n_rows, const int32_t *rows,
+                          int nb_stride, float *pooled) {
+  const index_inputs in = {NULL, NULL, q8, k8, q_scale, k_scale};
+  if (!q8) return ORACLE_EINVAL;
+  return pooled_core(num_seqs, cu_q, cu_k, hkv, d_idx, block, &in, n_rows, rows, nb_stride, pooled);
+}
+
+int msa_oracle_index_fp8(int num_seqs, const int32_t *cu_q, const int32_t *cu_k,
+                         int hkv, int d_idx, int block, int topk,
+                         const uint8_t *q8, const float *q_scale, const uint8_t *k8, const float *k_scale,
+                         int n_rows, const int32_t *rows,
+                         int32_t *idx, double *gap) {
+  const index_inputs in = {NULL, NULL, q8, k8, q_scale, k_scale};
+  if (!q8) return ORACLE_EINVAL;
+  return index_core(num_seqs, cu_q, cu_k, hkv, d_idx, block, topk, &in, n_rows, rows, idx, gap);
 }
 
 /*

@@ -12,6 +12,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_fp8_index_pins as fp8_index_pins
 import test_oracle_fp8_pins as fp8_pins
 import test_oracle_pins as pins
 import test_oracle_prologue_pins as prologue_pins
@@ -43,6 +44,13 @@ MUTANTS = {
                                        "k_scale[(size_t)(key[t] / block) * hkv + g]"),
     "fp8_value_scale_dropped": ("oh[d] += p * (msa_oracle_e4m3_value(vj[d]) * sv);",
                                 "oh[d] += p * msa_oracle_e4m3_value(vj[d]);"),
+    # fp8 index
+    "fp8_index_key_scale_row_ignores_sequence": ("(double)in->k_scale[blk0 + j / block]",
+                                                 "(double)in->k_scale[j / block]"),
+    "fp8_index_query_scale_of_group_0": ("(double)in->q_scale[(size_t)i * hkv + g]",
+                                         "(double)in->q_scale[(size_t)i * hkv]"),
+    "fp8_index_key_scale_dropped": ("msa_oracle_e4m3_value(in->k8[e]) * (double)in->k_scale[blk0 + j / block]",
+                                    "msa_oracle_e4m3_value(in->k8[e])"),
     # index prologue
     "rope_rotation_sign": ("out[j] = y[j] * c - y[j + half] * sn;", "out[j] = y[j] * c + y[j + half] * sn;"),
     "rope_frequency_exponent": ("pow(rope_base, -2.0 * j / rope_dim)", "pow(rope_base, -1.0 * j / rope_dim)"),
@@ -64,6 +72,10 @@ PIN_TESTS = [
     lambda: fp8_pins.test_e4m3_codes_match_torch_rounding(),
     lambda: fp8_pins.test_quantizer_scale_and_error_bound(),
     lambda: fp8_pins.test_attention_fp8_equals_bf16_attention_on_the_fp8_grid(),
+    lambda: fp8_index_pins.test_pooled_fp8_equals_bf16_pooled_on_the_fp8_grid(),
+    lambda: fp8_index_pins.test_pooled_fp8_matches_brute_force_with_quantizer_scales(),
+    lambda: fp8_index_pins.test_index_fp8_is_the_selection_over_pooled_fp8(),
+    lambda: fp8_index_pins.test_quantize_index_fp8_scales_and_extremes(),
     lambda: prologue_pins.test_identity_projection_matches_torch_rms_norm(),
     lambda: prologue_pins.test_rms_norm_is_scale_invariant_and_normalises_constants(),
     lambda: prologue_pins.test_rope_is_a_complex_rotation_of_each_pair(4, 100.0),
