@@ -605,9 +605,81 @@ def measure_fp8(msa, cfg, steps, warmup, dev):
         else:
             rec["attn_tflops"] = work["attn_flops"] / (stage["attn"] * 1e-3) / 1e12
             rec["attn_frac_of_tc_peak"] = rec["attn_tflops"] / peaks["bf16_tflops"]
+    if cfg.d_idx == 128:
+        rec["fp8_index"] = measure_fp8_index(msa, x, prob, k8, v8, ks, vs, idx, ws, flush, steps, warmup, peaks)
     del x, ws, idx, o, lse, flush, k8, v8, ks, vs, qws
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+    return rec
+
+
+def measure_fp8_index(msa, x, prob, k8, v8, ks, vs, idx_bf16_index, ws, flush, steps, warmup, peaks):
+    """The all-fp8 step (msa_forward_fp8_index: E4M3 Q_idx / K_idx as well as K / V) after one
+    msa_quantize_index_fp8 of the workload's index inputs (timed separately), with the same flush protocol as
+    the other steps.  Also how far its selection departs from the bf16 index's (informational: a quantized
+    index selects other blocks; its parity is against the oracle over the same codes, in the tests)."""
+    cfg = x.cfg
+    qws = msa.workspace(prob, msa.Op.QUANTIZE_INDEX_FP8)
+    q8, qsc, kk8, ksc = msa.msa_quantize_index_fp8(prob, x.q_idx, x.k_idx, ws=qws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    msa.msa_quantize_index_fp8(prob, x.q_idx, x.k_idx, q8, qsc, kk8, ksc, ws=qws)
+    b.record()
+    torch.cuda.synchronize()
+    quant_ms = a.elapsed_time(b)
+    idx = torch.empty_like(idx_bf16_index)  # ws: the fp8 K/V step's workspace (op MSA_OP_FORWARD_FP8)
+    o = torch.empty_like(x.q)
+    lse = torch.empty((x.total_q, cfg.hq), dtype=torch.float32, device=x.q.device)
+
+    def step():
+        msa.msa_forward_fp8_index(prob, x.q, k8, v8, ks, vs, q8, qsc, kk8, ksc, idx=idx, o=o, lse=lse, ws=ws)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s_, e_ in ev:
+        flush.zero_()
+        s_.record()
+        step()
+        e_.record()
+    torch.cuda.synchronize()
+    if msa.msa_read_device_status(ws):
+        raise RuntimeError("device status flags raised by the all-fp8 forward")
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in ev) / steps
+    timer = msa.StageTimer()
+    stage = {}
+    n_st = min(steps, 20)
+    with timer:
+        for _ in range(n_st):
+            flush.zero_()
+            step()
+            torch.cuda.synchronize()
+            for k_, v_ in timer.elapsed_ms().items():
+                stage[k_] = stage.get(k_, 0.0) + v_ / n_st
+    work = algorithmic_work(x, idx)
+    unit = "tok/s" if cfg.is_decode else "query tok/s"
+    rec = {"workload": f"{cfg.name}, fp8 K/V and fp8 index", "value": x.total_q / (ms * 1e-3), "unit": unit,
+           "ms_per_step": ms, "steps": steps, "stages_ms": stage, "quantize_index_ms": quant_ms}
+    same = (idx == idx_bf16_index).all(dim=-1)
+    a_ = idx_bf16_index.long()
+    b_ = idx.long()
+    inter = ((a_[..., :, None] == b_[..., None, :]) & (a_[..., :, None] >= 0)).any(dim=-1).sum(dim=-1)
+    n_sel = (a_ >= 0).sum(dim=-1).clamp(min=1)
+    rec["selection_vs_bf16_index"] = {"rows_identical": float(same.float().mean().item()),
+                                      "mean_overlap": float((inter.float() / n_sel.float()).mean().item())}
+    if "index" in stage:
+        if cfg.is_decode:
+            kb = work["k_idx_bytes"] / 2 + 4.0 * x.total_k / 128  # one byte per code, one fp32 scale per block
+            rec["index_gbs"] = kb / (stage["index"] * 1e-3) / 1e9
+            rec["index_frac_of_hbm_peak"] = rec["index_gbs"] / peaks["hbm_gbs"]
+            rec["index_bytes"] = kb
+        else:
+            rec["index_tflops"] = work["index_flops"] / (stage["index"] * 1e-3) / 1e12
+            rec["index_frac_of_fp8_peak"] = rec["index_tflops"] / (2.0 * peaks["bf16_tflops"])
+            rec["fp8_peak_source"] = "2 x the measured bf16 burst (the nominal fp8 / bf16 ratio)"
+    del qws, q8, qsc, kk8, ksc, idx, o, lse
     return rec
 
 

@@ -11,6 +11,8 @@ Entry points (same names as the C functions):
   msa_sparse_attn_prefill, msa_sparse_attn_decode, msa_forward,
   msa_sparse_attn_decode_static, msa_forward_decode_paged,
   msa_quantize_kv_fp8, msa_sparse_attn_prefill_fp8, msa_sparse_attn_decode_fp8, msa_forward_fp8,
+  msa_forward_decode_paged_fp8,
+  msa_quantize_index_fp8, msa_index_pool_fp8, msa_index_topk_fp8, msa_forward_fp8_index,
   msa_index_prologue,
   msa_workspace_size, msa_read_device_status.
 """
@@ -54,6 +56,7 @@ class Op(enum.IntEnum):
     SPARSE_ATTN_PREFILL_FP8 = 8
     SPARSE_ATTN_DECODE_FP8 = 9
     FORWARD_FP8 = 10
+    QUANTIZE_INDEX_FP8 = 12
 
 
 DEVICE_TIMEOUT = 1
@@ -117,6 +120,17 @@ _lib.msa_forward_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp
 _lib.msa_forward_decode_paged_fp8.restype = ctypes.c_int
 _lib.msa_forward_decode_paged_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, _i64, _vp,
                                               _vp, _vp, _vp, _sz, _vp]
+# problem, q_idx, k_idx, q_idx8, q_idx_scale, k_idx8, k_idx_scale, ws, bytes, stream
+_lib.msa_quantize_index_fp8.restype = ctypes.c_int
+_lib.msa_quantize_index_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+# problem, q_idx8, q_idx_scale, k_idx8, k_idx_scale, pooled, stride, ws, bytes, stream
+_lib.msa_index_pool_fp8.restype = ctypes.c_int
+_lib.msa_index_pool_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _sz, _vp]
+_lib.msa_index_topk_fp8.restype = ctypes.c_int
+_lib.msa_index_topk_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+# problem, q, k8, v8, k_scale, v_scale, q_idx8, q_idx_scale, k_idx8, k_idx_scale, idx, o, lse, ws, bytes, stream
+_lib.msa_forward_fp8_index.restype = ctypes.c_int
+_lib.msa_forward_fp8_index.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_index_prologue.restype = ctypes.c_int
 _lib.msa_index_prologue.argtypes = [_P, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
@@ -132,7 +146,8 @@ EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_inde
             "msa_kernel_launch_count", "msa_last_error_detail", "msa_sparse_attn_decode_static",
             "msa_forward_decode_paged", "msa_quantize_kv_fp8", "msa_sparse_attn_prefill_fp8",
             "msa_sparse_attn_decode_fp8", "msa_forward_fp8", "msa_index_prologue",
-            "msa_forward_decode_paged_fp8")
+            "msa_forward_decode_paged_fp8", "msa_quantize_index_fp8", "msa_index_pool_fp8", "msa_index_topk_fp8",
+            "msa_forward_fp8_index")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 
@@ -460,6 +475,95 @@ def msa_forward_decode_paged_fp8(problem: Problem, q, k8_cache, v8_cache, k_scal
                                              _ptr(k_scale), _ptr(v_scale), _ptr(q_idx), _ptr(k_idx_cache),
                                              _ptr(block_table), block_table.shape[1], n_pages, _ptr(idx), _ptr(o),
                                              _ptr(lse), _ptr(ws), nws, _stream()), "msa_forward_decode_paged_fp8")
+    return idx, o, lse
+
+
+def msa_quantize_index_fp8(problem: Problem, q_idx=None, k_idx=None, q_idx8=None, q_idx_scale=None, k_idx8=None,
+                           k_idx_scale=None, ws=None):
+    """bf16 Q_idx [total_q, Hkv, 128] and/or K_idx [total_k, 128] -> E4M3 codes (uint8, same shapes) with fp32
+    scales: q_idx_scale [total_q, Hkv] (one per query row and group), k_idx_scale [key blocks] (one per key block
+    of a sequence).  Either input may be None (that side is skipped and its outputs returned as None unless given).
+    Returns (q_idx8, q_idx_scale, k_idx8, k_idx_scale)."""
+    if q_idx is None and k_idx is None:
+        raise ValueError("nothing to quantize: q_idx and k_idx are both None")
+    if q_idx is not None:
+        _need(q_idx, torch.bfloat16, "q_idx")
+        dev = q_idx.device
+        if q_idx8 is None:
+            q_idx8 = torch.empty(q_idx.shape, dtype=torch.uint8, device=dev)
+        if q_idx_scale is None:
+            q_idx_scale = torch.empty(q_idx.shape[:2], dtype=torch.float32, device=dev)
+    if k_idx is not None:
+        _need(k_idx, torch.bfloat16, "k_idx")
+        dev = k_idx.device
+        if k_idx8 is None:
+            k_idx8 = torch.empty(k_idx.shape, dtype=torch.uint8, device=dev)
+        if k_idx_scale is None:
+            k_idx_scale = torch.zeros(fp8_scale_rows(problem), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.QUANTIZE_INDEX_FP8, ws)
+    _check(_lib.msa_quantize_index_fp8(ctypes.byref(problem.c()), _ptr(q_idx), _ptr(k_idx),
+                                       _ptr(q_idx8 if q_idx is not None else None),
+                                       _ptr(q_idx_scale if q_idx is not None else None),
+                                       _ptr(k_idx8 if k_idx is not None else None),
+                                       _ptr(k_idx_scale if k_idx is not None else None), _ptr(ws), nws, _stream()),
+           "msa_quantize_index_fp8")
+    return q_idx8, q_idx_scale, k_idx8, k_idx_scale
+
+
+def _need_fp8_index(q_idx8, q_idx_scale, k_idx8, k_idx_scale):
+    _need(q_idx8, torch.uint8, "q_idx8")
+    _need(k_idx8, torch.uint8, "k_idx8")
+    _need(q_idx_scale, torch.float32, "q_idx_scale")
+    _need(k_idx_scale, torch.float32, "k_idx_scale")
+
+
+def msa_index_pool_fp8(problem: Problem, q_idx8, q_idx_scale, k_idx8, k_idx_scale, pooled=None, ws=None):
+    """msa_index_pool over fp8 index inputs: pooled fp32 [total_q * hkv, ceil(max_k / 128)] (entries past a row's
+    causal end are left as they were, NaN when ``pooled`` is allocated here)."""
+    _need_fp8_index(q_idx8, q_idx_scale, k_idx8, k_idx_scale)
+    if pooled is None:
+        pooled = torch.full((problem.total_q * problem.hkv, max_blocks(problem)), float("nan"), dtype=torch.float32,
+                            device=q_idx8.device)
+    ws, nws = _ws(problem, Op.INDEX_POOL, ws)
+    _check(_lib.msa_index_pool_fp8(ctypes.byref(problem.c()), _ptr(q_idx8), _ptr(q_idx_scale), _ptr(k_idx8),
+                                   _ptr(k_idx_scale), _ptr(pooled), pooled.stride(0), _ptr(ws), nws, _stream()),
+           "msa_index_pool_fp8")
+    return pooled
+
+
+def msa_index_topk_fp8(problem: Problem, q_idx8, q_idx_scale, k_idx8, k_idx_scale, idx=None, ws=None):
+    """msa_index_topk over fp8 index inputs.  Returns idx [total_q, Hkv, topk] int32."""
+    _need_fp8_index(q_idx8, q_idx_scale, k_idx8, k_idx_scale)
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=q_idx8.device)
+    _need(idx, torch.int32, "idx")
+    ws, nws = _ws(problem, Op.INDEX_TOPK, ws)
+    _check(_lib.msa_index_topk_fp8(ctypes.byref(problem.c()), _ptr(q_idx8), _ptr(q_idx_scale), _ptr(k_idx8),
+                                   _ptr(k_idx_scale), _ptr(idx), _ptr(ws), nws, _stream()), "msa_index_topk_fp8")
+    return idx
+
+
+def msa_forward_fp8_index(problem: Problem, q, k8, v8, k_scale, v_scale, q_idx8, q_idx_scale, k_idx8, k_idx_scale,
+                          idx=None, o=None, lse=None, ws=None):
+    """msa_forward_fp8 with the Index Branch on fp8 inputs too.  Returns (idx, o, lse)."""
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((k8, "k8"), (v8, "v8")):
+        _need(t, torch.uint8, n)
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need_fp8_index(q_idx8, q_idx_scale, k_idx8, k_idx_scale)
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.FORWARD_FP8, ws)
+    _check(_lib.msa_forward_fp8_index(ctypes.byref(problem.c()), _ptr(q), _ptr(k8), _ptr(v8), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(q_idx8), _ptr(q_idx_scale), _ptr(k_idx8), _ptr(k_idx_scale),
+                                      _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()),
+           "msa_forward_fp8_index")
     return idx, o, lse
 
 

@@ -246,6 +246,14 @@ bool map_3d(CUtensorMap& m, const void* ptr, long long n, int heads, int box_hea
   return make_map(m, ptr, 3, dims, strides, box, dtype);
 }
 
+// E4M3 codes [rows, cols] (one byte each), box = 128 codes x box_rows rows
+bool map_2d_u8(CUtensorMap& m, const void* ptr, long long rows, int cols, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  return make_map(m, ptr, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
 // E4M3 codes [n, heads, 128] (one byte each), box = 128 codes x 1 head x 128 rows
 bool map_3d_u8(CUtensorMap& m, const void* ptr, long long n, int heads) {
   cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(n > 0 ? n : 1)};
@@ -283,6 +291,10 @@ struct Ctx {
   bool fp8 = false;
   const float* k_scale = nullptr;
   const float* v_scale = nullptr;
+  // fp8 index: q_idx and k_idx are E4M3 codes with these scales ([total_q * hkv] and [n_key_blocks])
+  bool fp8_index = false;
+  const float* q_idx_scale = nullptr;
+  const float* k_idx_scale = nullptr;
   long long cache_rows() const { return block_table ? n_pages * 128 : d.N; }
 };
 
@@ -342,10 +354,15 @@ msa_status_t run_index_prefill(const msa_problem_t* p, Ctx& c, const void* q_idx
                                float* pooled, int64_t pooled_stride, int32_t* idx) {
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tq, tk;
-  if (!map_2d(tq, q_idx, static_cast<long long>(c.d.T) * c.d.hkv, c.d.d_idx, 128) ||
-      !map_2d(tk, k_idx, c.d.N, c.d.d_idx, 256))  // index scoring loads two key blocks per box
+  const long long q_rows = static_cast<long long>(c.d.T) * c.d.hkv;
+  // index scoring loads two key blocks per box
+  if (c.fp8_index ? (!map_2d_u8(tq, q_idx, q_rows, c.d.d_idx, 128) || !map_2d_u8(tk, k_idx, c.d.N, c.d.d_idx, 256))
+                  : (!map_2d(tq, q_idx, q_rows, c.d.d_idx, 128) || !map_2d(tk, k_idx, c.d.N, c.d.d_idx, 256)))
     return MSA_ERR_CUDA;
   IndexParams ip{};
+  ip.q_scale = c.q_idx_scale;
+  ip.k_scale = c.k_idx_scale;
+  ip.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   ip.seq = c.seq;
   ip.tiles = at<int2>(c.ws, c.L.tiles);
   ip.hdr = c.hdr;
@@ -360,7 +377,7 @@ msa_status_t run_index_prefill(const msa_problem_t* p, Ctx& c, const void* q_idx
   if (grid > c.dev.sms) grid = c.dev.sms;
   if (grid < 1) grid = 1;
   StageScope scope(MSA_STAGE_INDEX, c.stream);
-  return cuda_status(launch_index_score(tq, tk, ip, fused, static_cast<int>(grid), c.stream));
+  return cuda_status(launch_index_score(tq, tk, ip, fused, c.fp8_index, static_cast<int>(grid), c.stream));
   (void)p;
 }
 
@@ -384,14 +401,23 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
 msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx, const void* k_idx, int32_t* idx) {
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tk;
-  if (!map_2d(tk, k_idx, c.cache_rows(), c.d.d_idx, 128)) return MSA_ERR_CUDA;
+  if (c.fp8_index ? !map_2d_u8(tk, k_idx, c.cache_rows(), c.d.d_idx, 128)
+                  : !map_2d(tk, k_idx, c.cache_rows(), c.d.d_idx, 128))
+    return MSA_ERR_CUDA;
   float* pooled = at<float>(c.ws, c.L.pooled);
   DecodeScanParams sp{};
   sp.num_seqs = c.d.S;
   sp.hkv = c.d.hkv;
   sp.d_idx = c.d.d_idx;
   sp.seq = c.seq;
-  sp.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  if (c.fp8_index) {
+    sp.q_idx8 = static_cast<const uint8_t*>(q_idx);
+    sp.q_scale = c.q_idx_scale;
+    sp.k_scale = c.k_idx_scale;
+  } else {
+    sp.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  }
+  sp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   sp.pooled = pooled;
   sp.pooled_stride = c.d.max_nb;
   // about 4 work units per SM in total, at least 16 blocks each
@@ -414,7 +440,7 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   msa_status_t st;
   {
     StageScope scope(MSA_STAGE_INDEX, c.stream);
-    st = cuda_status(launch_decode_scan(tk, sp, grid, c.stream));
+    st = cuda_status(launch_decode_scan(tk, sp, c.fp8_index, grid, c.stream));
   }
   if (st != MSA_OK) return st;
   return run_topk_pooled(p, c, pooled, c.d.max_nb, idx);
@@ -673,7 +699,7 @@ const char* msa_status_string(msa_status_t s) {
 
 msa_status_t msa_workspace_size(const msa_problem_t* problem, msa_op_t op, size_t* bytes) {
   if (!bytes) return MSA_ERR_INVALID_ARG;
-  if (op < MSA_OP_INDEX_POOL || op > MSA_OP_INDEX_PROLOGUE) return MSA_ERR_INVALID_ARG;
+  if (op < MSA_OP_INDEX_POOL || op > MSA_OP_QUANTIZE_INDEX_FP8) return MSA_ERR_INVALID_ARG;
   Derived d;
   msa_status_t st = derive(problem, d);
   if (st != MSA_OK) return st;
@@ -1005,6 +1031,120 @@ msa_status_t msa_forward_decode_paged_fp8(const msa_problem_t* problem, const vo
   if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
   if ((st = run_index_decode(problem, c, q_idx, k_idx_cache, idx)) != MSA_OK) return st;
   return run_attn_decode(problem, c, q, k8_cache, v8_cache, idx, o, lse);
+}
+
+// ---------------------------------------------------------------- fp8 index
+static msa_status_t check_fp8_index_args(const Derived& d, const void* q8, const float* q_scale, const void* k8,
+                                         const float* k_scale) {
+  if (!q8 || !q_scale || !k8 || !k_scale) return MSA_ERR_INVALID_ARG;
+  if (d.d_idx != 128) return MSA_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || (reinterpret_cast<uintptr_t>(q_scale) & 3u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u))
+    return MSA_ERR_ALIGNMENT;
+  return MSA_OK;
+}
+
+static void use_fp8_index(Ctx& c, const float* q_scale, const float* k_scale) {
+  c.fp8_index = true;
+  c.q_idx_scale = q_scale;
+  c.k_idx_scale = k_scale;
+}
+
+msa_status_t msa_quantize_index_fp8(const msa_problem_t* problem, const void* q_idx, const void* k_idx,
+                                    void* q_idx8, float* q_idx_scale, void* k_idx8, float* k_idx_scale,
+                                    void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!q_idx && !k_idx) return MSA_ERR_INVALID_ARG;
+  if ((q_idx && (!q_idx8 || !q_idx_scale)) || (k_idx && (!k_idx8 || !k_idx_scale))) return MSA_ERR_INVALID_ARG;
+  if (d.d_idx != 128) return MSA_ERR_UNSUPPORTED;
+  if ((q_idx && (!aligned16(q_idx) || !aligned16(q_idx8) || (reinterpret_cast<uintptr_t>(q_idx_scale) & 3u))) ||
+      (k_idx && (!aligned16(k_idx) || !aligned16(k_idx8) || (reinterpret_cast<uintptr_t>(k_idx_scale) & 3u))))
+    return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_QUANTIZE_INDEX_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK)
+    return st;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  IndexQuantParams qp{};
+  qp.num_seqs = c.d.S;
+  qp.hkv = c.d.hkv;
+  qp.total_q = c.d.T;
+  qp.seq = c.seq;
+  qp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
+  qp.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  qp.k_idx = static_cast<const __nv_bfloat16*>(k_idx);
+  qp.q8 = static_cast<uint8_t*>(q_idx8);
+  qp.q_scale = q_idx_scale;
+  qp.k8 = static_cast<uint8_t*>(k_idx8);
+  qp.k_scale = k_idx_scale;
+  qp.key_ctas = (k_idx && c.d.N > 0) ? c.d.total_blocks : 0;
+  qp.hdr = c.hdr;
+  return cuda_status(launch_quantize_index_fp8(qp, c.stream));
+}
+
+msa_status_t msa_index_pool_fp8(const msa_problem_t* problem, const void* q_idx8, const float* q_idx_scale,
+                                const void* k_idx8, const float* k_idx_scale, float* pooled, int64_t pooled_stride,
+                                void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_fp8_index_args(d, q_idx8, q_idx_scale, k_idx8, k_idx_scale)) != MSA_OK) return st;
+  if (!pooled) return MSA_ERR_INVALID_ARG;
+  if (pooled_stride < d.max_nb) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(pooled)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_INDEX_POOL, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  use_fp8_index(c, q_idx_scale, k_idx_scale);
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  return run_index_prefill(problem, c, q_idx8, k_idx8, false, pooled, pooled_stride, nullptr);
+}
+
+msa_status_t msa_index_topk_fp8(const msa_problem_t* problem, const void* q_idx8, const float* q_idx_scale,
+                                const void* k_idx8, const float* k_idx_scale, int32_t* idx, void* workspace,
+                                size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_fp8_index_args(d, q_idx8, q_idx_scale, k_idx8, k_idx_scale)) != MSA_OK) return st;
+  if (!idx) return MSA_ERR_INVALID_ARG;
+  if (!aligned16(idx)) return MSA_ERR_ALIGNMENT;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_INDEX_TOPK, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  use_fp8_index(c, q_idx_scale, k_idx_scale);
+  if (c.d.decode) {
+    if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+    return run_index_decode(problem, c, q_idx8, k_idx8, idx);
+  }
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  return run_index_select_prefill(problem, c, q_idx8, k_idx8, idx);
+}
+
+msa_status_t msa_forward_fp8_index(const msa_problem_t* problem, const void* q, const void* k8, const void* v8,
+                                   const float* k_scale, const float* v_scale, const void* q_idx8,
+                                   const float* q_idx_scale, const void* k_idx8, const float* k_idx_scale,
+                                   int32_t* idx, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                   msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if ((st = check_attn_args(q, k8, v8, idx, o, lse)) != MSA_OK) return st;
+  if ((st = check_fp8_args(k8, v8, k_scale, v_scale)) != MSA_OK) return st;
+  if ((st = check_fp8_index_args(d, q_idx8, q_idx_scale, k_idx8, k_idx_scale)) != MSA_OK) return st;
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_FORWARD_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  c.fp8 = true;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  use_fp8_index(c, q_idx_scale, k_idx_scale);
+  if (c.d.decode) {
+    if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+    if ((st = run_index_decode(problem, c, q_idx8, k_idx8, idx)) != MSA_OK) return st;
+    return run_attn_decode(problem, c, q, k8, v8, idx, o, lse);
+  }
+  if ((st = run_plan(problem, c, c.d.qt)) != MSA_OK) return st;
+  if ((st = run_index_select_prefill(problem, c, q_idx8, k_idx8, idx)) != MSA_OK) return st;
+  return run_attn_prefill(problem, c, q, k8, v8, idx, o, lse);
 }
 
 msa_status_t msa_read_device_status(const void* workspace, uint32_t* flags, msa_stream_t stream) {

@@ -27,15 +27,23 @@ namespace msa {
 
 namespace {
 
-// One consumer warp per ring stage: block j of a CTA's stream goes to stage
-// j % kScanStages and is consumed by warp j % kScanStages, so every stage has a
-// single consumer that takes its fills in order (a parity wait is only sound
-// when the waiter already consumed the stage's previous fill).
-constexpr int kScanStages = 6;
-constexpr int kScanConsumers = kScanStages;
-constexpr int kScanThreads = 32 * (kScanConsumers + 1);
-constexpr int kScanTile = 128 * 128 * 2;  // 128 keys x up to 128 dims, bf16
-constexpr size_t kScanSmemBytes = 1024 + kScanStages * kScanTile + 256;
+// Six consumer warps: block j of a CTA's stream goes to stage j % stages and
+// is consumed by warp j % 6; the stage count is a multiple of 6, so every stage
+// has a single consumer that takes its fills in order (a parity wait is only
+// sound when the waiter already consumed the stage's previous fill).  A stage
+// holds one key block: 128 keys x up to 128 dims, bf16 (32 KB), or x 128 E4M3
+// codes (16 KB) for an fp8 index; the fp8 ring has twice the stages (two per
+// consumer), so the same bytes are in flight per SM.
+template <bool FP8>
+struct ScanCfg {
+  static constexpr int kStages = FP8 ? 12 : 6;
+  static constexpr int kConsumers = 6;
+  static constexpr int kThreads = 32 * (kConsumers + 1);
+  static constexpr int kTile = FP8 ? 128 * 128 : 128 * 128 * 2;
+  static constexpr size_t kSmem = 1024 + kStages * kTile + 256;
+  static_assert(kStages % kConsumers == 0, "each stage needs a single consumer warp");
+};
+constexpr int kScanMaxStages = 12;
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                             uint32_t& r3) {
@@ -57,6 +65,17 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// D = A(16x32, row) * B(32x8, col) + D, E4M3 inputs, fp32 accumulate.  The
+// fragments hold four codes per register where the bf16 shape holds two
+// values: a 16-byte row chunk is k 0..15 here, so the same ldmatrix loads
+// feed it.
+__device__ __forceinline__ void mma_16832_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 // Byte offset of (row, 8-element chunk) in a TMA 128-byte-swizzled tile whose
 // 64-column halves are 16 KB apart.
@@ -65,7 +84,7 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
 }
 
 struct ScanSmem {
-  uint64_t full[kScanStages], empty[kScanStages];
+  uint64_t full[kScanMaxStages], empty[kScanMaxStages];
   int abort_flag;
 };
 
@@ -91,8 +110,14 @@ __device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor&
 
 }  // namespace
 
-__global__ void __launch_bounds__(kScanThreads, 1)
+// FP8: K_idx holds E4M3 codes (d_idx 128, one 128-byte row per key) with one
+// scale per key block, Q_idx codes with one scale per (sequence, group); the
+// pooled score is the block's maximum code dot product times both scales.
+template <bool FP8>
+__global__ void __launch_bounds__(ScanCfg<FP8>::kThreads, 1)
     decode_scan_kernel(const __grid_constant__ CUtensorMap tm_k, DecodeScanParams p) {
+  using Cfg = ScanCfg<FP8>;
+  constexpr int kScanStages = Cfg::kStages, kScanConsumers = Cfg::kConsumers, kScanTile = Cfg::kTile;
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   griddep_wait();  // sequence facts and the header come from the plan kernel
@@ -100,8 +125,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   ScanSmem& sm = *reinterpret_cast<ScanSmem*>(base + kScanStages * kScanTile);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kchunks = p.d_idx >> 6;
-  const uint32_t tile_tx = 128u * p.d_idx * 2u;
+  const int kchunks = FP8 ? 1 : p.d_idx >> 6;
+  const uint32_t tile_tx = 128u * p.d_idx * (FP8 ? 1u : 2u);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kScanStages; ++i) {
       mbar_init(&sm.full[i], 1);
@@ -147,6 +172,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int cur_s = -1;
     uint32_t qf[8][2];
     int pos = 0;
+    float qs0 = 1.f, qs1 = 1.f;               // fp8: Q_idx scales of groups 2 lane, 2 lane + 1 (lanes 0..3)
     const int gq = lane >> 2;                 // B-fragment column = group
     while (scan_next(p, c)) {
       const int st = it % kScanStages;
@@ -159,16 +185,34 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         cur_s = c.s;
         const SeqInfo si = p.seq[cur_s];
         pos = si.kv_len - 1;
-        const __nv_bfloat16* qrow = p.q_idx + (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx;
-        const bool q_ok = gq >= p.hkv || index_ok(hdr, (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx +
-                                                             p.d_idx - 1, static_cast<long long>(p.num_seqs) * p.hkv * p.d_idx, 403);
+        const int64_t qbase = (static_cast<int64_t>(cur_s) * p.hkv + gq) * p.d_idx;
+        const bool q_ok = gq >= p.hkv || index_ok(hdr, qbase + p.d_idx - 1,
+                                                  static_cast<long long>(p.num_seqs) * p.hkv * p.d_idx, 403);
+        if constexpr (FP8) {
+          // m16n8k32 B fragment: codes k = 4 (lane % 4) .. + 3 and 16 + 4 (lane % 4) .. + 3 of each 32
+          const uint8_t* qrow = p.q_idx8 + qbase;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          qf[ks][0] = qf[ks][1] = 0u;
-          if (q_ok && gq < p.hkv && ks * 16 < p.d_idx) {
-            const int d0 = ks * 16 + (lane & 3) * 2;
-            qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + d0);
-            qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + d0 + 8);
+          for (int ks = 0; ks < 8; ++ks) {
+            qf[ks][0] = qf[ks][1] = 0u;
+            if (q_ok && gq < p.hkv && ks < 4) {
+              const int d0 = ks * 32 + (lane & 3) * 4;
+              qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + d0);
+              qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + d0 + 16);
+            }
+          }
+          const int g0 = 2 * lane;
+          qs0 = (lane < 4 && g0 < p.hkv) ? p.q_scale[static_cast<int64_t>(cur_s) * p.hkv + g0] : 1.f;
+          qs1 = (lane < 4 && g0 + 1 < p.hkv) ? p.q_scale[static_cast<int64_t>(cur_s) * p.hkv + g0 + 1] : 1.f;
+        } else {
+          const __nv_bfloat16* qrow = p.q_idx + qbase;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            qf[ks][0] = qf[ks][1] = 0u;
+            if (q_ok && gq < p.hkv && ks * 16 < p.d_idx) {
+              const int d0 = ks * 16 + (lane & 3) * 2;
+              qf[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + d0);
+              qf[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + d0 + 8);
+            }
           }
         }
       }
@@ -186,10 +230,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         const int arow = sub * 16 + (mtx & 1) * 8 + mr;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          if (ks * 16 < p.d_idx) {
+          if (FP8 ? ks < 4 : ks * 16 < p.d_idx) {
             uint32_t a[4];
             ldmatrix_x4(tile + sw128_off(arow, ks * 2 + (mtx >> 1)), a[0], a[1], a[2], a[3]);
-            mma_16816(acc, a, qf[ks][0], qf[ks][1]);
+            if constexpr (FP8)
+              mma_16832_e4m3(acc, a, qf[ks][0], qf[ks][1]);
+            else
+              mma_16816(acc, a, qf[ks][0], qf[ks][1]);
           }
         }
         const int k0 = key_base + sub * 16 + (lane >> 2);
@@ -209,6 +256,21 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
       }
+      if (FP8 && lane < 4) {
+        // the block's K_idx scale: per key block of the sequence (packed) or per page (paged; a page outside
+        // the cache, already flagged by the producer, reads page 0's); scales are positive, so scaling the
+        // maximum is the maximum of the scaled scores
+        long long srow;
+        if (p.block_table) {
+          const long long pg = p.block_table[static_cast<long long>(cur_s) * p.bt_stride + b];
+          srow = (pg >= 0 && pg < p.n_pages) ? pg : 0;
+        } else {
+          srow = static_cast<long long>(p.blk_off[cur_s]) + b;
+        }
+        const float ks = p.k_scale[srow];
+        mx0 *= qs0 * ks;
+        mx1 *= qs1 * ks;
+      }
       if (lane < 4) {
         const int g0 = lane * 2;
         const long long rows = static_cast<long long>(p.num_seqs) * p.hkv;
@@ -224,15 +286,22 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   __syncthreads();
 }
 
-size_t decode_scan_smem_bytes() { return kScanSmemBytes; }
+size_t decode_scan_smem_bytes() { return ScanCfg<false>::kSmem; }
 
-cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kScanSmemBytes));
+template <bool FP8>
+static cudaError_t launch_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream) {
+  using Cfg = ScanCfg<FP8>;
+  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::kSmem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(decode_scan_kernel, dim3(grid), dim3(kScanThreads), kScanSmemBytes, stream, tk, p);
+  e = launch_pdl(decode_scan_kernel<FP8>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmem, stream, tk, p);
   note_launches(1);
   return e;
+}
+
+cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, bool fp8, int grid,
+                               cudaStream_t stream) {
+  return fp8 ? launch_scan<true>(tk, p, grid, stream) : launch_scan<false>(tk, p, grid, stream);
 }
 
 // ----------------------------------------------------------------------------

@@ -99,6 +99,45 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kv_fp8_kernel(QuantPar
   quantize_block(p.v + at, p.v8 + at, p.hkv, rows, sv);
 }
 
+// Index inputs (d_idx 128): CTAs 0 .. key_ctas - 1 take one key block of K_idx
+// each (the K/V block routines above with one head), the others eight Q_idx
+// rows each, one warp per (query row, group) with four values per lane.  Same
+// rounding as K/V: scale = amax / 448 (1 when 0), code = RNE(x / scale),
+// saturated.
+__global__ void __launch_bounds__(kQuantThreads) quantize_index_fp8_kernel(IndexQuantParams p) {
+  __shared__ uint32_t red[kQuantThreads / 32];
+  if (p.hdr->status & kFlagBadSeqlens) return;
+  if (blockIdx.x < p.key_ctas) {
+    const int gb = blockIdx.x;
+    if (!p.k_idx || gb >= p.blk_off[p.num_seqs]) return;  // CTA-uniform, before block_absmax's barriers
+    const int s = find_seq(p.blk_off, p.num_seqs, gb);
+    const int b = gb - p.blk_off[s];
+    const SeqInfo si = p.seq[s];
+    const int rows = min(kBlock, si.kv_len - b * kBlock);
+    const int64_t at = (static_cast<int64_t>(si.k_start) + b * kBlock) * kHeadDim;
+    const float a = block_absmax(p.k_idx + at, 1, rows, red);
+    const float sc = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
+    if (threadIdx.x == 0) p.k_scale[gb] = sc;
+    quantize_block(p.k_idx + at, p.k8 + at, 1, rows, sc);
+    return;
+  }
+  if (!p.q_idx) return;
+  const long long r =
+      (static_cast<long long>(blockIdx.x) - p.key_ctas) * (kQuantThreads / 32) + (threadIdx.x >> 5);
+  if (r >= static_cast<long long>(p.total_q) * p.hkv) return;
+  const int lane = threadIdx.x & 31;
+  const uint2 v = *reinterpret_cast<const uint2*>(p.q_idx + r * kHeadDim + lane * 4);
+  uint32_t m = max(max(bf16_abs_bits(v.x), bf16_abs_bits(v.x >> 16)), max(bf16_abs_bits(v.y), bf16_abs_bits(v.y >> 16)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  const float a = __uint_as_float(m << 16);
+  const float sc = a > 0.f ? __fdiv_rn(a, 448.0f) : 1.0f;
+  const float f0 = __fdiv_rn(__uint_as_float(v.x << 16), sc), f1 = __fdiv_rn(__uint_as_float(v.x & 0xFFFF0000u), sc);
+  const float f2 = __fdiv_rn(__uint_as_float(v.y << 16), sc), f3 = __fdiv_rn(__uint_as_float(v.y & 0xFFFF0000u), sc);
+  *reinterpret_cast<uint32_t*>(p.q8 + r * kHeadDim + lane * 4) = e4m3x4(f0, f1, f2, f3);
+  if (lane == 0) p.q_scale[r] = sc;
+}
+
 __global__ void __launch_bounds__(256) kv8_widen_kernel(const uint4* __restrict__ k8, const uint4* __restrict__ v8,
                                                         uint4* __restrict__ k16, uint4* __restrict__ v16,
                                                         long long n16, const WsHeader* hdr) {
@@ -132,6 +171,16 @@ cudaError_t launch_quantize_kv_fp8(const QuantParams& p, long long max_blocks, c
   const long long grid = max_blocks * p.hkv;
   if (grid <= 0) return cudaSuccess;
   quantize_kv_fp8_kernel<<<static_cast<unsigned>(grid), kQuantThreads, 0, stream>>>(p);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_index_fp8(const IndexQuantParams& p, cudaStream_t stream) {
+  const long long q_ctas =
+      p.q_idx ? (static_cast<long long>(p.total_q) * p.hkv + kQuantThreads / 32 - 1) / (kQuantThreads / 32) : 0;
+  const long long grid = p.key_ctas + q_ctas;
+  if (grid <= 0) return cudaSuccess;
+  quantize_index_fp8_kernel<<<static_cast<unsigned>(grid), kQuantThreads, 0, stream>>>(p);
   note_launches(1);
   return cudaGetLastError();
 }

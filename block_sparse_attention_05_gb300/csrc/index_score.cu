@@ -29,14 +29,21 @@ namespace msa {
 
 namespace {
 
-constexpr int kIdxStagesK = 3;             // K_idx ring depth (block pairs)
-constexpr int kQTile = 128 * 128 * 2;      // 128 rows x 128 bf16 columns
-constexpr int kKPair = 2 * kQTile;         // 256 keys x 128 bf16 columns
+// Tiles: 128 rows x 128 bf16 columns (two 64-column halves of 128-byte rows),
+// or x 128 E4M3 codes (one 128-byte row) for an fp8 index; the K_idx ring holds
+// pairs of key blocks, as many as fit the same 192 KB.
+template <bool FP8>
+struct IdxCfg {
+  static constexpr int kStagesK = FP8 ? 6 : 3;
+  static constexpr int kQTile = FP8 ? 128 * 128 : 128 * 128 * 2;
+  static constexpr int kKPair = 2 * kQTile;
+};
+constexpr int kIdxMaxStagesK = 6;
 constexpr int kIdxThreads = 256;
 
 struct IdxSmem {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kIdxStagesK], k_empty[kIdxStagesK];
+  uint64_t k_full[kIdxMaxStagesK], k_empty[kIdxMaxStagesK];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t work_full[2], work_empty[2];
   uint64_t mma_done;
@@ -45,7 +52,10 @@ struct IdxSmem {
   int abort_flag;
 };
 
-constexpr size_t kIdxSmemBytes = 1024 /*align slack*/ + kQTile + kIdxStagesK * kKPair + sizeof(IdxSmem);
+template <bool FP8>
+constexpr size_t idx_smem_bytes() {
+  return 1024 /*align slack*/ + IdxCfg<FP8>::kQTile + IdxCfg<FP8>::kStagesK * IdxCfg<FP8>::kKPair + sizeof(IdxSmem);
+}
 
 __device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt, int& nq, int& lmax) {
   nq = min(qt, si.q_len - t0);
@@ -55,10 +65,15 @@ __device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt,
 
 }  // namespace
 
-template <int CAP, bool FUSED>
+// FP8: Q_idx and K_idx are E4M3 codes (kind::f8f6f4 MMAs, K = 32 codes per
+// instruction) with one scale per Q_idx row and one per key block; a block's
+// pooled score is its maximum code dot product times the two scales (positive,
+// so scaling the maximum is the maximum of the scaled scores).
+template <int CAP, bool FUSED, bool FP8>
 __global__ void __launch_bounds__(kIdxThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        IndexParams p) {
+  constexpr int kIdxStagesK = IdxCfg<FP8>::kStagesK, kQTile = IdxCfg<FP8>::kQTile, kKPair = IdxCfg<FP8>::kKPair;
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   if (hdr->status & kFlagBadSeqlens) return;
@@ -71,9 +86,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tiles = static_cast<int>(hdr->n_qtiles);
-  const int kchunks = p.d_idx >> 6;                // 64-column chunks per row
-  const int ksteps = p.d_idx >> 4;                 // UMMA K = 16 steps
-  const uint32_t row_tx = p.d_idx * 2u;            // bytes of one row
+  const int kchunks = FP8 ? 1 : p.d_idx >> 6;      // 128-byte chunks per row
+  const int ksteps = p.d_idx >> (FP8 ? 5 : 4);     // UMMA K = 32 bytes per step
+  const uint32_t row_tx = p.d_idx * (FP8 ? 1u : 2u);  // bytes of one row
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, 256, false);
+      const uint32_t idesc = FP8 ? idesc_e4m3(128, 256) : idesc_bf16(128, 256, false);
       uint32_t q_iter = 0, k_iter = 0, a_iter = 0;
       for (uint32_t w = 0;; ++w) {
         const int slot = w & 1;
@@ -196,8 +211,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           for (int kk = 0; kk < ksteps; ++kk) {
             const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32;
             const uint32_t koff = (kk >> 2) * 32768 + (kk & 3) * 32;
-            umma_bf16(tmem + ab * 256, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), idesc,
-                      kk > 0 ? 1u : 0u);
+            if constexpr (FP8)
+              umma_e4m3(tmem + ab * 256, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), idesc,
+                        kk > 0 ? 1u : 0u);
+            else
+              umma_bf16(tmem + ab * 256, sdesc_sw128(qa + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024), idesc,
+                        kk > 0 ? 1u : 0u);
           }
           umma_commit(&sm.k_empty[ks]);
           umma_commit(&sm.acc_full[ab]);
@@ -237,11 +256,22 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int pos = si.kv_len - si.q_len + t;
       const int local = pos >> 7;
       const int64_t grow = static_cast<int64_t>(si.q_start + tile.y) * p.hkv + row;  // global Q_idx row
+      float q_sc = 1.f;
+      int blk0 = 0;
+      if constexpr (FP8) {
+        q_sc = valid ? p.q_scale[grow] : 1.f;
+        blk0 = p.blk_off[tile.x];
+      }
       TopkList<CAP> list;
       list.clear();
       bool ok = true;
       for (int bp = 0; 2 * bp <= lmax; ++bp) {
         const int ab = a_iter & 1;
+        float sc[2] = {1.f, 1.f};  // fp8: the two blocks' combined scales (blocks past the tile's last: unused)
+        if constexpr (FP8) {
+          sc[0] = q_sc * p.k_scale[blk0 + 2 * bp];
+          if (2 * bp + 1 <= lmax) sc[1] = q_sc * p.k_scale[blk0 + 2 * bp + 1];
+        }
         if (!mbar_wait_warp(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 122);
           ok = false;
@@ -273,7 +303,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
                 m3 = fmaxf(m3, c + 96 <= lim ? __uint_as_float(r[3][c]) : -INFINITY);
               }
             }
-            const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+            if constexpr (FP8) m *= sc[h];
             if constexpr (FUSED) {
               if (b < local) list.insert(topk_key(m, b));
             } else {
@@ -304,26 +335,33 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   }
 }
 
-size_t index_score_smem_bytes() { return kIdxSmemBytes; }
+size_t index_score_smem_bytes(bool fp8) { return fp8 ? idx_smem_bytes<true>() : idx_smem_bytes<false>(); }
 
-template <int CAP, bool FUSED>
+template <int CAP, bool FUSED, bool FP8>
 static cudaError_t launch_index(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p, int grid,
                                 cudaStream_t stream) {
-  auto* fn = index_score_kernel<CAP, FUSED>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kIdxSmemBytes));
+  auto* fn = index_score_kernel<CAP, FUSED, FP8>;
+  constexpr size_t smem = idx_smem_bytes<FP8>();
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<grid, kIdxThreads, kIdxSmemBytes, stream>>>(tq, tk, p);
+  fn<<<grid, kIdxThreads, smem, stream>>>(tq, tk, p);
   note_launches(1);
   return cudaGetLastError();
 }
 
+template <bool FP8>
+static cudaError_t launch_index_dtype(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p,
+                                     bool fused, int grid, cudaStream_t stream) {
+  if (!fused) return launch_index<1, false, FP8>(tq, tk, p, grid, stream);
+  if (p.topk <= 4) return launch_index<3, true, FP8>(tq, tk, p, grid, stream);
+  if (p.topk <= 8) return launch_index<7, true, FP8>(tq, tk, p, grid, stream);
+  return launch_index<15, true, FP8>(tq, tk, p, grid, stream);
+}
+
 cudaError_t launch_index_score(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p, bool fused,
-                               int grid, cudaStream_t stream) {
-  if (!fused) return launch_index<1, false>(tq, tk, p, grid, stream);
-  if (p.topk <= 4) return launch_index<3, true>(tq, tk, p, grid, stream);
-  if (p.topk <= 8) return launch_index<7, true>(tq, tk, p, grid, stream);
-  return launch_index<15, true>(tq, tk, p, grid, stream);
+                               bool fp8, int grid, cudaStream_t stream) {
+  return fp8 ? launch_index_dtype<true>(tq, tk, p, fused, grid, stream)
+             : launch_index_dtype<false>(tq, tk, p, fused, grid, stream);
 }
 
 }  // namespace msa

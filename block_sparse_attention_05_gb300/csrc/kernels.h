@@ -70,10 +70,15 @@ struct IndexParams {
   float* pooled;
   int64_t pooled_stride;
   int32_t* idx;
+  // fp8 index (launch with fp8 = true; tq / tk then map E4M3 codes, d_idx 128): Q_idx scales [total_q * hkv],
+  // K_idx scales [n_key_blocks], first key block of each sequence
+  const float* q_scale;
+  const float* k_scale;
+  const int32_t* blk_off;
 };
-size_t index_score_smem_bytes();
+size_t index_score_smem_bytes(bool fp8);
 cudaError_t launch_index_score(const CUtensorMap& tq, const CUtensorMap& tk, const IndexParams& p, bool fused,
-                               int grid, cudaStream_t stream);
+                               bool fp8, int grid, cudaStream_t stream);
 
 // Top-k over pooled rows r = i * hkv + g (rows of queries, or of decode
 // sequences when every q_len is 1).
@@ -93,6 +98,12 @@ struct DecodeScanParams {
   int num_seqs, hkv, d_idx;
   const SeqInfo* seq;
   const __nv_bfloat16* q_idx;   // [num_seqs, hkv, d_idx]
+  // fp8 index (launch with fp8 = true; tk then maps E4M3 codes, d_idx 128): Q_idx codes and scales
+  // [num_seqs * hkv], K_idx scales per key block (packed: first block of each sequence in blk_off) or per page
+  const uint8_t* q_idx8;
+  const float* q_scale;
+  const float* k_scale;
+  const int32_t* blk_off;
   float* pooled;                // [num_seqs * hkv, pooled_stride]
   int64_t pooled_stride;
   int units_per_seq;            // work units per sequence
@@ -106,7 +117,8 @@ struct DecodeScanParams {
   long long n_pages;
 };
 size_t decode_scan_smem_bytes();
-cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_decode_scan(const CUtensorMap& tk, const DecodeScanParams& p, bool fp8, int grid,
+                               cudaStream_t stream);
 
 // ---------------------------------------------------------------- main branch
 // Partial results of one (query, group, slot): G rows of 128 16-bit values + G
@@ -226,6 +238,22 @@ struct QuantParams {
   WsHeader* hdr;
 };
 cudaError_t launch_quantize_kv_fp8(const QuantParams& p, long long max_blocks, cudaStream_t stream);
+// Quantization of the index inputs to E4M3 codes: K_idx with one scale per key block of a sequence, Q_idx with
+// one per (query row, group); either side may be skipped (null input).  d_idx 128.
+struct IndexQuantParams {
+  int num_seqs, hkv, total_q;
+  const SeqInfo* seq;
+  const int32_t* blk_off;
+  const __nv_bfloat16* q_idx;   // [total_q, hkv, 128] or null
+  const __nv_bfloat16* k_idx;   // [total_k, 128] or null
+  uint8_t* q8;
+  float* q_scale;               // [total_q * hkv]
+  uint8_t* k8;
+  float* k_scale;               // [n_key_blocks]
+  long long key_ctas;           // CTAs of the grid that take key blocks (the rest take query rows)
+  WsHeader* hdr;
+};
+cudaError_t launch_quantize_index_fp8(const IndexQuantParams& p, cudaStream_t stream);
 // 16-bit copies of fp8 K (bf16) and V (fp16) for the prefill Main Branch; exact.
 cudaError_t launch_kv8_widen(const uint8_t* k8, const uint8_t* v8, __nv_bfloat16* k16, __half* v16,
                              long long n_elems, const WsHeader* hdr, int sms, cudaStream_t stream);

@@ -122,7 +122,8 @@ typedef enum msa_op {
   MSA_OP_SPARSE_ATTN_PREFILL_FP8 = 8, /* msa_sparse_attn_prefill_fp8 */
   MSA_OP_SPARSE_ATTN_DECODE_FP8 = 9,  /* msa_sparse_attn_decode_fp8 */
   MSA_OP_FORWARD_FP8 = 10,       /* msa_forward_fp8 */
-  MSA_OP_INDEX_PROLOGUE = 11     /* msa_index_prologue */
+  MSA_OP_INDEX_PROLOGUE = 11,    /* msa_index_prologue */
+  MSA_OP_QUANTIZE_INDEX_FP8 = 12 /* msa_quantize_index_fp8 */
 } msa_op_t;
 
 /* Workspace bytes that `op` needs for `problem` (host-only; no CUDA call).
@@ -288,8 +289,9 @@ msa_status_t msa_index_prologue(const msa_problem_t *problem, const void *x, int
  *                     n_key_blocks = sum over sequences of ceil(kv_len / 128)
  *                     (at most total_k / 128 + num_seqs); key block b of
  *                     sequence s is row (key blocks of sequences 0..s-1) + b.
- * The Index Branch stays bf16 (a quantized index selects other blocks).  The
- * fp8 Main Branch computes exactly the bf16 one over the dequantized values
+ * The Index Branch reads bf16 Q_idx / K_idx here (a quantized index selects
+ * other blocks; the fp8 index below is a separate option).  The fp8 Main
+ * Branch computes exactly the bf16 one over the dequantized values
  * (value = code * scale); results differ from bf16 K/V by the quantization.
  * Decode reads the codes directly (half the K/V bytes); prefill widens them
  * once per call into exact 16-bit copies in the workspace.  A paged decode
@@ -337,6 +339,57 @@ msa_status_t msa_forward_decode_paged_fp8(const msa_problem_t *problem, const vo
                                           int32_t max_blocks_per_seq, int64_t num_pages, int32_t *idx, void *o,
                                           float *lse, void *workspace, size_t workspace_bytes,
                                           msa_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * fp8 index (the same provenance as fp8 K/V above; the report also warns that
+ * quantizing the index changes which blocks are selected, so this is an
+ * option beside the bf16 Index Branch, and its selections are those of the
+ * method applied to the dequantized index inputs, not to the bf16 ones).
+ * Q_idx and K_idx as E4M3 codes (index_dim 128 only) with the rounding of
+ * msa_quantize_kv_fp8 (scale = max |x| / 448, 1 when 0; code = RNE(x / scale)
+ * in fp32, saturated):
+ *   q_idx8       [total_q, num_kv_heads, 128] uint8, 16-byte aligned
+ *   q_idx_scale  [total_q, num_kv_heads] fp32: one scale per (query row, group)
+ *   k_idx8       [total_k, 128] uint8, 16-byte aligned
+ *   k_idx_scale  [n_key_blocks] fp32: one scale per key block of 128 tokens of
+ *                a sequence, block b of sequence s at row (key blocks of
+ *                sequences 0..s-1) + b, as for k_scale above.
+ * A token score is the fp32 dot product of the two code rows (the tensor
+ * cores multiply E4M3 codes exactly and sum in fp32) and a block's pooled
+ * score is the block's maximum times q_idx_scale * k_idx_scale: scales must be
+ * positive and finite (msa_quantize_index_fp8 gives such), so the maximum of
+ * the scaled scores is the scaled maximum.  Half the index bytes of bf16: the
+ * decode index scan, which streams every cached key, reads half as much.
+ * ------------------------------------------------------------------------ */
+
+/* bf16 Q_idx and/or K_idx -> E4M3 codes and scales as above (workspace op
+ * MSA_OP_QUANTIZE_INDEX_FP8).  Either input may be NULL to skip that side (for
+ * example a decode step that quantizes only its new queries); the outputs of
+ * a given side are then not touched.  Only the rows of the sequences' key
+ * blocks are written. */
+msa_status_t msa_quantize_index_fp8(const msa_problem_t *problem, const void *q_idx, const void *k_idx,
+                                    void *q_idx8, float *q_idx_scale, void *k_idx8, float *k_idx_scale,
+                                    void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_index_pool over fp8 index inputs (workspace op MSA_OP_INDEX_POOL). */
+msa_status_t msa_index_pool_fp8(const msa_problem_t *problem, const void *q_idx8, const float *q_idx_scale,
+                                const void *k_idx8, const float *k_idx_scale, float *pooled,
+                                int64_t pooled_stride, void *workspace, size_t workspace_bytes,
+                                msa_stream_t stream);
+
+/* msa_index_topk over fp8 index inputs (workspace op MSA_OP_INDEX_TOPK):
+ * prefill and decode batches, the same selection rule. */
+msa_status_t msa_index_topk_fp8(const msa_problem_t *problem, const void *q_idx8, const float *q_idx_scale,
+                                const void *k_idx8, const float *k_idx_scale, int32_t *idx, void *workspace,
+                                size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_forward_fp8 with the Index Branch on fp8 inputs as well (workspace op
+ * MSA_OP_FORWARD_FP8): every K, V, Q_idx and K_idx read is an E4M3 code. */
+msa_status_t msa_forward_fp8_index(const msa_problem_t *problem, const void *q, const void *k8, const void *v8,
+                                   const float *k_scale, const float *v_scale, const void *q_idx8,
+                                   const float *q_idx_scale, const void *k_idx8, const float *k_idx_scale,
+                                   int32_t *idx, void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                   msa_stream_t stream);
 
 /* Waits for `stream`, then returns in *flags the MSA_DEVICE_* bits that the
  * last call on this workspace raised (0 = none).  workspace = NULL reads the

@@ -74,5 +74,42 @@ def assert_attention_close(o_gpu, lse_gpu, ref, group, exempt=None, what=""):
     return emax, emean, lmax
 
 
+def _e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of fp32 values within +-448 by torch's float8_e4m3fn conversion (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(
+        torch.uint8).numpy()
+
+
+def quantize_index_cpu(x, block: int = 128, chunk: int = 1 << 20):
+    """fp8 index inputs of workload x, computed on the CPU with torch's float8_e4m3fn conversion as the rounding
+    step, for sizes the oracle's code-by-code quantizer is too slow for: (q8, q_scale, k8, k_scale) in the
+    layout of oracle.quantize_index_fp8, which test_oracle_fp8_index_pins checks it against bit for bit.
+    Scale = max |x| / 448 in fp32 (1 when 0) per Q_idx row and group and per key block of a sequence;
+    code = RNE(x / scale) with the division in fp32 (the quotient never exceeds 448)."""
+    qf = x.q_idx.float().cpu().numpy()
+    amax = np.abs(qf).max(axis=2)
+    q_scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q8 = _e4m3_codes(qf / q_scale[:, :, None])
+    cu_k = x.cu_k.cpu().numpy().astype(np.int64)
+    n_keys = int(cu_k[-1])
+    blk_of_key = np.empty(n_keys, np.int64)
+    r0 = 0
+    for s in range(len(cu_k) - 1):
+        n = int(cu_k[s + 1] - cu_k[s])
+        blk_of_key[cu_k[s]:cu_k[s + 1]] = r0 + np.arange(n) // block
+        r0 += -(-n // block)
+    k_amax = np.zeros(r0, np.float32)
+    k_idx = x.k_idx.cpu()
+    for a in range(0, n_keys, chunk):
+        kf = k_idx[a:a + chunk].float().numpy()
+        np.maximum.at(k_amax, blk_of_key[a:a + chunk], np.abs(kf).max(axis=1))
+    k_scale = np.where(k_amax > 0, k_amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    k8 = np.empty((n_keys, k_idx.shape[1]), np.uint8)
+    for a in range(0, n_keys, chunk):
+        kf = k_idx[a:a + chunk].float().numpy()
+        k8[a:a + chunk] = _e4m3_codes(kf / k_scale[blk_of_key[a:a + chunk]][:, None])
+    return q8, q_scale, k8, k_scale
+
+
 def to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().numpy()

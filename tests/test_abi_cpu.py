@@ -139,6 +139,30 @@ def test_paged_fp8_decode_rejects_bad_arguments_on_the_host(msa):
     assert lib.msa_forward_decode_paged_fp8(ctypes.byref(pre), *args()[1:]) == -1
 
 
+def test_fp8_index_calls_reject_bad_arguments_on_the_host(msa):
+    lib = msa._lib
+    pre = base_problem(msa)
+    p = ctypes.byref(pre)
+    p64 = ctypes.byref(base_problem(msa, index_dim=64))
+    quant = lambda prob=p, qi=FAKE, ki=FAKE, q8=FAKE, qs=FAKE, k8=FAKE, ks=FAKE: (prob, qi, ki, q8, qs, k8, ks, FAKE,
+                                                                                   1 << 40, None)
+    assert lib.msa_quantize_index_fp8(*quant(qi=None, ki=None)) == -1   # nothing to quantize
+    assert lib.msa_quantize_index_fp8(*quant(qs=None)) == -1            # a side without its scales
+    assert lib.msa_quantize_index_fp8(*quant(k8=FAKE + 8)) == -3        # misaligned codes
+    assert lib.msa_quantize_index_fp8(*quant(ks=FAKE + 2)) == -3        # misaligned scales
+    assert lib.msa_quantize_index_fp8(*quant(prob=p64)) == -2           # index_dim 64: bf16 index only
+    topk = lambda prob=p, qs=FAKE, k8=FAKE: (prob, FAKE, qs, k8, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert lib.msa_index_topk_fp8(*topk(qs=None)) == -1
+    assert lib.msa_index_topk_fp8(*topk(k8=FAKE + 4)) == -3
+    assert lib.msa_index_topk_fp8(*topk(prob=p64)) == -2
+    assert lib.msa_index_pool_fp8(p, FAKE, FAKE, FAKE, FAKE, FAKE, 7, FAKE, 1 << 40, None) == -1  # stride < 8 blocks
+    fwd = lambda ks=FAKE: (p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ks, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert lib.msa_forward_fp8_index(*fwd(ks=None)) == -1
+    assert lib.msa_forward_fp8_index(*fwd(ks=FAKE + 1)) == -3
+    st, n = ws_size(msa, pre, msa.Op.QUANTIZE_INDEX_FP8)
+    assert st == 0 and n > 0
+
+
 def test_status_strings(msa):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert msa._lib.msa_status_string(code)

@@ -20,6 +20,7 @@ import torch
 
 import oracle
 import workloads
+from parity import quantize_index_cpu
 from workloads.configs import small
 
 BLOCK = 32  # small blocks: many key blocks, so many scale rows per sequence
@@ -122,3 +123,13 @@ def test_quantize_index_fp8_scales_and_extremes():
         assert k8[rows == r][j] in (0x7E, 0xFE)
     i, g = np.unravel_index(amax_q.argmax(), amax_q.shape)
     assert q8[i, g, np.abs(qf[i, g]).argmax()] in (0x7E, 0xFE)
+
+
+def test_cpu_quantizer_of_the_tests_matches_the_oracle():
+    """The torch-based quantizer that feeds the full-size GPU tests (the oracle's code-by-code search is too
+    slow there) gives the oracle quantizer's codes and scales bit for bit."""
+    cfg, x = _case(seed=6, seqs=((70, 300), (1, 1), (128, 128), (200, 513)), hkv=4, d_idx=128)
+    ref = oracle.quantize_index_fp8(x.cu_q, x.cu_k, x.q_idx, x.k_idx, 128)
+    got = quantize_index_cpu(x, block=128, chunk=100)
+    for a, b in zip(got, ref):
+        assert a.shape == b.shape and np.array_equal(a, b)
