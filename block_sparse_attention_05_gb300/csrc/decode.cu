@@ -85,13 +85,16 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
 
 struct ScanSmem {
   uint64_t full[kScanMaxStages], empty[kScanMaxStages];
+  int srow[kScanMaxStages];  // fp8: the K_idx scale row of the block in each stage (written with its fill)
   int abort_flag;
 };
 
 // The work of one CTA: units u = blockIdx.x + j * gridDim.x; unit u covers
-// blocks [c * bpu, min((c + 1) * bpu, nb)) of sequence u / ups.
+// blocks [c * bpu, min((c + 1) * bpu, nb)) of sequence u / ups, whose first
+// key row is k0 (kept here so that the TMA thread loads it once per unit, not
+// once per block).
 struct ScanCursor {
-  int u, b, b_end, s;
+  int u, b, b_end, s, k0;
 };
 
 __device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor& c) {
@@ -105,6 +108,7 @@ __device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor&
     const int nb = (si.kv_len + kBlock - 1) / kBlock;
     c.b = unit * p.blocks_per_unit;
     c.b_end = min(nb, c.b + p.blocks_per_unit);
+    c.k0 = si.k_start;
   }
 }
 
@@ -142,17 +146,33 @@ __global__ void __launch_bounds__(ScanCfg<FP8>::kThreads, 1)
   if (warp == kScanConsumers) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0};
+      ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0, 0};
       uint32_t it = 0;
+      int blk0_s = -1, blk0 = 0;  // fp8, packed: first key block of sequence blk0_s
       while (scan_next(p, c)) {
         const int st = it % kScanStages;
         if (it >= kScanStages && !mbar_wait(&sm.empty[st], ((it / kScanStages) - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 301);
           break;
         }
-        const int row = key_block_row(p.block_table, p.bt_stride, p.n_pages, p.seq[c.s].k_start, c.s, c.b, hdr);
+        const int row = key_block_row(p.block_table, p.bt_stride, p.n_pages, c.k0, c.s, c.b, hdr);
         index_ok(hdr, c.s, p.num_seqs, 401);
         index_ok(hdr, row, p.total_k, 402);
+        if constexpr (FP8) {
+          // the block's K_idx scale row, handed to the consumer with the fill (the consumer then loads the
+          // scale under its MMAs): per key block of the sequence (packed) or the page (paged; a page outside
+          // the cache, already flagged, reads page 0's)
+          if (p.block_table) {
+            const int pg = row >> 7;
+            sm.srow[st] = pg < p.n_pages ? pg : 0;
+          } else {
+            if (c.s != blk0_s) {
+              blk0_s = c.s;
+              blk0 = p.blk_off[c.s];
+            }
+            sm.srow[st] = blk0 + c.b;
+          }
+        }
         mbar_arrive_expect_tx(&sm.full[st], tile_tx);
         for (int ch = 0; ch < kchunks; ++ch)
           tma_load_2d(base + st * kScanTile + ch * 16384, &tm_k, &sm.full[st], ch * 64, row);
@@ -167,7 +187,7 @@ __global__ void __launch_bounds__(ScanCfg<FP8>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ consumers
-    ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0};
+    ScanCursor c{static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x), 0, 0, 0, 0};
     uint32_t it = 0;
     int cur_s = -1;
     uint32_t qf[8][2];
@@ -220,6 +240,10 @@ __global__ void __launch_bounds__(ScanCfg<FP8>::kThreads, 1)
         report_timeout(abort_flag, hdr, 311);
         break;
       }
+      float k_sc = 1.f;  // fp8: the block's K_idx scale, loaded before the MMAs that hide its latency
+      if constexpr (FP8) {
+        if (lane < 4) k_sc = p.k_scale[sm.srow[st]];
+      }
       const uint32_t tile = smem_u32(base + st * kScanTile);
       float mx0 = -INFINITY, mx1 = -INFINITY;
       const int key_base = b * kBlock;
@@ -256,20 +280,9 @@ __global__ void __launch_bounds__(ScanCfg<FP8>::kThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
       }
-      if (FP8 && lane < 4) {
-        // the block's K_idx scale: per key block of the sequence (packed) or per page (paged; a page outside
-        // the cache, already flagged by the producer, reads page 0's); scales are positive, so scaling the
-        // maximum is the maximum of the scaled scores
-        long long srow;
-        if (p.block_table) {
-          const long long pg = p.block_table[static_cast<long long>(cur_s) * p.bt_stride + b];
-          srow = (pg >= 0 && pg < p.n_pages) ? pg : 0;
-        } else {
-          srow = static_cast<long long>(p.blk_off[cur_s]) + b;
-        }
-        const float ks = p.k_scale[srow];
-        mx0 *= qs0 * ks;
-        mx1 *= qs1 * ks;
+      if (FP8 && lane < 4) {  // scales are positive: scaling the maximum is the maximum of the scaled scores
+        mx0 *= qs0 * k_sc;
+        mx1 *= qs1 * k_sc;
       }
       if (lane < 4) {
         const int g0 = lane * 2;

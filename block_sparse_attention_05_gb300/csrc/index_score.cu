@@ -31,15 +31,25 @@ namespace {
 
 // Tiles: 128 rows x 128 bf16 columns (two 64-column halves of 128-byte rows),
 // or x 128 E4M3 codes (one 128-byte row) for an fp8 index; the K_idx ring holds
-// pairs of key blocks, as many as fit the same 192 KB.
+// pairs of key blocks, as many as fit the same 192 KB.  The fp8 MMAs take half
+// the time of the bf16 ones, so the fp8 kernel has two epilogue warpgroups,
+// one per block of a pair, each keeping its own top-k list per row; at the end
+// of a work item the second hands its lists to the first through shared
+// memory (kMergeBytes) to be merged.
 template <bool FP8>
 struct IdxCfg {
   static constexpr int kStagesK = FP8 ? 6 : 3;
   static constexpr int kQTile = FP8 ? 128 * 128 : 128 * 128 * 2;
   static constexpr int kKPair = 2 * kQTile;
+  static constexpr int kEpiGroups = FP8 ? 2 : 1;
+  static constexpr int kThreads = 128 + 128 * kEpiGroups;
+  static constexpr int kMergeBytes = FP8 ? 128 * 15 * 8 : 0;  // 128 rows x up to 15 keys
+  // fp8: registers per thread after the reallocation (warps 0-3: TMA, MMA and TMEM allocation; the two
+  // epilogue warpgroups load a whole block's 128 accumulator columns at once)
+  static constexpr int kCtlRegs = 96, kEpiRegs = 200;
+  static constexpr int kRegsNeeded = 128 * kCtlRegs + 128 * kEpiGroups * kEpiRegs;
 };
 constexpr int kIdxMaxStagesK = 6;
-constexpr int kIdxThreads = 256;
 
 struct IdxSmem {
   uint64_t q_full, q_empty;
@@ -47,6 +57,7 @@ struct IdxSmem {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t work_full[2], work_empty[2];
   uint64_t mma_done;
+  uint64_t merge_full, merge_empty;  // fp8: the second epilogue group's lists written / read
   int work[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -54,8 +65,10 @@ struct IdxSmem {
 
 template <bool FP8>
 constexpr size_t idx_smem_bytes() {
-  return 1024 /*align slack*/ + IdxCfg<FP8>::kQTile + IdxCfg<FP8>::kStagesK * IdxCfg<FP8>::kKPair + sizeof(IdxSmem);
+  return 1024 /*align slack*/ + IdxCfg<FP8>::kQTile + IdxCfg<FP8>::kStagesK * IdxCfg<FP8>::kKPair +
+         sizeof(IdxSmem) + IdxCfg<FP8>::kMergeBytes;
 }
+static_assert(idx_smem_bytes<true>() <= 232448 && idx_smem_bytes<false>() <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt, int& nq, int& lmax) {
   nq = min(qt, si.q_len - t0);
@@ -70,10 +83,11 @@ __device__ __forceinline__ void tile_geometry(const SeqInfo& si, int t0, int qt,
 // pooled score is its maximum code dot product times the two scales (positive,
 // so scaling the maximum is the maximum of the scaled scores).
 template <int CAP, bool FUSED, bool FP8>
-__global__ void __launch_bounds__(kIdxThreads, 1)
+__global__ void __launch_bounds__(IdxCfg<FP8>::kThreads, 1)
     index_score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        IndexParams p) {
   constexpr int kIdxStagesK = IdxCfg<FP8>::kStagesK, kQTile = IdxCfg<FP8>::kQTile, kKPair = IdxCfg<FP8>::kKPair;
+  constexpr int kEpi = IdxCfg<FP8>::kEpiGroups;
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
   if (hdr->status & kFlagBadSeqlens) return;
@@ -82,6 +96,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   uint8_t* q_buf = base;                      // one 128-row tile
   uint8_t* k_buf = base + kQTile;             // kIdxStagesK pairs of key blocks
   IdxSmem& sm = *reinterpret_cast<IdxSmem*>(base + kQTile + kIdxStagesK * kKPair);
+  // fp8: merge buffer, key j of row r at [j * 128 + r]
+  uint64_t* merge_keys = reinterpret_cast<uint64_t*>(base + kQTile + kIdxStagesK * kKPair + sizeof(IdxSmem));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -95,10 +111,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     mbar_init(&sm.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.acc_full[i], 1);
-      mbar_init(&sm.acc_empty[i], 128);
+      mbar_init(&sm.acc_empty[i], 128 * kEpi);
       mbar_init(&sm.work_full[i], 1);
-      mbar_init(&sm.work_empty[i], 5);
+      mbar_init(&sm.work_empty[i], 1 + 4 * kEpi);  // the MMA warp and every epilogue warp
     }
+    mbar_init(&sm.merge_full, 128);
+    mbar_init(&sm.merge_empty, 128);
     for (int i = 0; i < kIdxStagesK; ++i) {
       mbar_init(&sm.k_full[i], 1);
       mbar_init(&sm.k_empty[i], 1);
@@ -119,6 +137,10 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
+  // fp8: the control warpgroup gives registers to the two epilogue warpgroups (each warpgroup reallocates at
+  // the top of its own branch; the launcher checked that the launch allocation covers the counts)
+  if (warp < 4) {
+  if constexpr (FP8) regs_release<IdxCfg<FP8>::kCtlRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -231,11 +253,14 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       umma_commit(&sm.mma_done);
       mbar_wait(&sm.mma_done, 0, nullptr);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int row = (warp - 4) * 32 + lane;  // TMEM lane == tile row
+    if constexpr (FP8) regs_claim<IdxCfg<FP8>::kEpiRegs>();
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane == tile row
+    const int eg = (warp - 4) >> 2;           // epilogue group: block eg of each pair (fp8), both blocks (bf16)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    uint32_t a_iter = 0;
+    uint32_t a_iter = 0, n_items = 0;
     for (uint32_t w = 0;; ++w) {
       const int slot = w & 1;
       if (!mbar_wait_warp(&sm.work_full[slot], (w >> 1) & 1, abort_flag)) {
@@ -267,10 +292,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       bool ok = true;
       for (int bp = 0; 2 * bp <= lmax; ++bp) {
         const int ab = a_iter & 1;
-        float sc[2] = {1.f, 1.f};  // fp8: the two blocks' combined scales (blocks past the tile's last: unused)
+        float sc = 1.f;  // fp8: the combined scale of this group's block (a block past the tile's last: unused)
         if constexpr (FP8) {
-          sc[0] = q_sc * p.k_scale[blk0 + 2 * bp];
-          if (2 * bp + 1 <= lmax) sc[1] = q_sc * p.k_scale[blk0 + 2 * bp + 1];
+          if (2 * bp + eg <= lmax) sc = q_sc * p.k_scale[blk0 + 2 * bp + eg];
         }
         if (!mbar_wait_warp(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 122);
@@ -279,21 +303,52 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // block 2 bp + h: accumulator columns 128 h .. 128 h + 127
+        for (int hh = 0; hh < 2 / kEpi; ++hh) {  // block 2 bp + h: accumulator columns 128 h .. 128 h + 127
+          const int h = kEpi == 2 ? eg : hh;
           const int b = 2 * bp + h;
-          uint32_t r[4][32];
-          float cmax[4];  // the load's own maximum of each 32-column chunk
+          if constexpr (kEpi == 1) {
+            uint32_t r[4][32];
+            float cmax[4];  // the load's own maximum of each 32-column chunk
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld_max_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c], cmax[c]);
-          tmem_ld_wait_max4(cmax);
-          if (h == 1) {
+            for (int c = 0; c < 4; ++c) tmem_ld_max_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c], cmax[c]);
+            tmem_ld_wait_max4(cmax);
+            if (hh == 1) {
+              tc_fence_before();
+              mbar_arrive(&sm.acc_empty[ab]);
+            }
+            if (valid && b <= local) {
+              const int lim = (b == local) ? (pos & 127) : 127;
+              float m0 = cmax[0], m1 = cmax[1], m2 = cmax[2], m3 = cmax[3];
+              if (lim < 127) {  // the query's own block: only keys up to its position
+                m0 = m1 = m2 = m3 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  m0 = fmaxf(m0, c <= lim ? __uint_as_float(r[0][c]) : -INFINITY);
+                  m1 = fmaxf(m1, c + 32 <= lim ? __uint_as_float(r[1][c]) : -INFINITY);
+                  m2 = fmaxf(m2, c + 64 <= lim ? __uint_as_float(r[2][c]) : -INFINITY);
+                  m3 = fmaxf(m3, c + 96 <= lim ? __uint_as_float(r[3][c]) : -INFINITY);
+                }
+              }
+              const float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+              if constexpr (FUSED) {
+                if (b < local) list.insert(topk_key(m, b));
+              } else {
+                p.pooled[grow * p.pooled_stride + b] = m;
+              }
+            }
+          } else {
+            // this group's block, all 128 columns in flight at once
+            const bool take = valid && b <= local;
+            uint32_t r[4][32];
+            float cmax[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_max_32cols(lane_addr + ab * 256 + h * 128 + c * 32, r[c], cmax[c]);
+            tmem_ld_wait_max4(cmax);
             tc_fence_before();
             mbar_arrive(&sm.acc_empty[ab]);
-          }
-          if (valid && b <= local) {
-            const int lim = (b == local) ? (pos & 127) : 127;
             float m0 = cmax[0], m1 = cmax[1], m2 = cmax[2], m3 = cmax[3];
-            if (lim < 127) {  // the query's own block: only keys up to its position
+            const int lim = (b == local) ? (pos & 127) : 127;
+            if (take && lim < 127) {  // the query's own block: only keys up to its position
               m0 = m1 = m2 = m3 = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
@@ -304,11 +359,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
               }
             }
             float m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-            if constexpr (FP8) m *= sc[h];
-            if constexpr (FUSED) {
-              if (b < local) list.insert(topk_key(m, b));
-            } else {
-              p.pooled[grow * p.pooled_stride + b] = m;
+            if (take) {
+              m *= sc;
+              if constexpr (FUSED) {
+                if (b < local) list.insert(topk_key(m, b));
+              } else {
+                p.pooled[grow * p.pooled_stride + b] = m;
+              }
             }
           }
         }
@@ -316,7 +373,28 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       if (!ok) break;
       if constexpr (FUSED) {
-        if (valid) {
+        if constexpr (kEpi == 2) {
+          // the second group's lists go to the first through shared memory (bounded waits on both sides)
+          static_assert(CAP <= 15, "merge buffer holds 15 keys per row");
+          if (eg == 1) {
+            if (n_items > 0 && !mbar_wait_warp(&sm.merge_empty, (n_items - 1) & 1, abort_flag)) {
+              report_timeout(abort_flag, hdr, 123);
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < CAP; ++j) merge_keys[j * 128 + row] = list.k[j];
+            mbar_arrive(&sm.merge_full);
+          } else {
+            if (!mbar_wait_warp(&sm.merge_full, n_items & 1, abort_flag)) {
+              report_timeout(abort_flag, hdr, 124);
+              break;
+            }
+#pragma unroll
+            for (int j = 0; j < CAP; ++j) list.insert(merge_keys[j * 128 + row]);
+            mbar_arrive(&sm.merge_empty);
+          }
+        }
+        if (valid && eg == 0) {
           int chosen[CAP];
 #pragma unroll
           for (int j = 0; j < CAP; ++j)
@@ -324,6 +402,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
           write_selection<CAP>(p.idx + grow * p.topk, p.topk, chosen, local);
         }
       }
+      ++n_items;
     }
   }
 
@@ -344,7 +423,15 @@ static cudaError_t launch_index(const CUtensorMap& tq, const CUtensorMap& tk, co
   constexpr size_t smem = idx_smem_bytes<FP8>();
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  fn<<<grid, kIdxThreads, smem, stream>>>(tq, tk, p);
+  if constexpr (FP8) {
+    // the register reallocation's increases must fit in the launch allocation, or they would never complete
+    cudaFuncAttributes fa{};
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < IdxCfg<FP8>::kCtlRegs || fa.numRegs * IdxCfg<FP8>::kThreads < IdxCfg<FP8>::kRegsNeeded)
+      return cudaErrorInvalidConfiguration;
+  }
+  fn<<<grid, IdxCfg<FP8>::kThreads, smem, stream>>>(tq, tk, p);
   note_launches(1);
   return cudaGetLastError();
 }
