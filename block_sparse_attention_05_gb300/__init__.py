@@ -13,6 +13,7 @@ Entry points (same names as the C functions):
   msa_quantize_kv_fp8, msa_sparse_attn_prefill_fp8, msa_sparse_attn_decode_fp8, msa_forward_fp8,
   msa_forward_decode_paged_fp8,
   msa_quantize_index_fp8, msa_index_pool_fp8, msa_index_topk_fp8, msa_forward_fp8_index,
+  msa_forward_decode_paged_fp8_index,
   msa_index_prologue,
   msa_workspace_size, msa_read_device_status.
 """
@@ -131,6 +132,11 @@ _lib.msa_index_topk_fp8.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 # problem, q, k8, v8, k_scale, v_scale, q_idx8, q_idx_scale, k_idx8, k_idx_scale, idx, o, lse, ws, bytes, stream
 _lib.msa_forward_fp8_index.restype = ctypes.c_int
 _lib.msa_forward_fp8_index.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+# problem, q, k8, v8, k_scale, v_scale, q_idx8, q_idx_scale, k_idx8 cache, k_idx_scale, block table, stride, pages,
+# idx, o, lse, ws, bytes, stream
+_lib.msa_forward_decode_paged_fp8_index.restype = ctypes.c_int
+_lib.msa_forward_decode_paged_fp8_index.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                                    ctypes.c_int32, _i64, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_index_prologue.restype = ctypes.c_int
 _lib.msa_index_prologue.argtypes = [_P, _vp, ctypes.c_int32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
 _lib.msa_read_device_status.restype = ctypes.c_int
@@ -147,7 +153,7 @@ EXPORTED = ("msa_workspace_size", "msa_index_pool", "msa_topk_pooled", "msa_inde
             "msa_forward_decode_paged", "msa_quantize_kv_fp8", "msa_sparse_attn_prefill_fp8",
             "msa_sparse_attn_decode_fp8", "msa_forward_fp8", "msa_index_prologue",
             "msa_forward_decode_paged_fp8", "msa_quantize_index_fp8", "msa_index_pool_fp8", "msa_index_topk_fp8",
-            "msa_forward_fp8_index")
+            "msa_forward_fp8_index", "msa_forward_decode_paged_fp8_index")
 
 STAGES = ("plan", "index", "topk", "schedule", "attn", "combine")
 
@@ -564,6 +570,40 @@ def msa_forward_fp8_index(problem: Problem, q, k8, v8, k_scale, v_scale, q_idx8,
                                       _ptr(v_scale), _ptr(q_idx8), _ptr(q_idx_scale), _ptr(k_idx8), _ptr(k_idx_scale),
                                       _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()),
            "msa_forward_fp8_index")
+    return idx, o, lse
+
+
+def msa_forward_decode_paged_fp8_index(problem: Problem, q, k8_cache, v8_cache, k_scale, v_scale, q_idx8,
+                                       q_idx_scale, k_idx8_cache, k_idx_scale, block_table, idx=None, o=None,
+                                       lse=None, ws=None):
+    """Decode from paged fp8 caches with the index keys in fp8 too: K/V codes [num_pages * 128, hkv, 128] with
+    scales [num_pages, hkv]; index-key codes [num_pages * 128, 128] with scales [num_pages]; q_idx8 / q_idx_scale
+    for the queries; block_table int32 [num_seqs, max_blocks].  Returns (idx, o, lse) as msa_forward."""
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((k8_cache, "k8_cache"), (v8_cache, "v8_cache")):
+        _need(t, torch.uint8, n)
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need_fp8_index(q_idx8, q_idx_scale, k_idx8_cache, k_idx_scale)
+    _need(block_table, torch.int32, "block_table")
+    if block_table.dim() != 2 or k8_cache.shape[0] % 128 or k_idx8_cache.shape[0] != k8_cache.shape[0]:
+        raise ValueError("block_table must be [num_seqs, max_blocks] and the caches whole pages of 128 rows")
+    n_pages = k8_cache.shape[0] // 128
+    if k_scale.numel() < n_pages * problem.hkv or v_scale.numel() < n_pages * problem.hkv or \
+            k_idx_scale.numel() < n_pages:
+        raise ValueError("the scale arrays need one row per page")
+    dev = q.device
+    if idx is None:
+        idx = torch.empty((problem.total_q, problem.hkv, problem.topk), dtype=torch.int32, device=dev)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((problem.total_q, problem.hq), dtype=torch.float32, device=dev)
+    ws, nws = _ws(problem, Op.FORWARD_FP8, ws)
+    _check(_lib.msa_forward_decode_paged_fp8_index(
+        ctypes.byref(problem.c()), _ptr(q), _ptr(k8_cache), _ptr(v8_cache), _ptr(k_scale), _ptr(v_scale), _ptr(q_idx8),
+        _ptr(q_idx_scale), _ptr(k_idx8_cache), _ptr(k_idx_scale), _ptr(block_table), block_table.shape[1], n_pages,
+        _ptr(idx), _ptr(o), _ptr(lse), _ptr(ws), nws, _stream()), "msa_forward_decode_paged_fp8_index")
     return idx, o, lse
 
 

@@ -1147,6 +1147,38 @@ msa_status_t msa_forward_fp8_index(const msa_problem_t* problem, const void* q, 
   return run_attn_prefill(problem, c, q, k8, v8, idx, o, lse);
 }
 
+msa_status_t msa_forward_decode_paged_fp8_index(const msa_problem_t* problem, const void* q, const void* k8_cache,
+                                                const void* v8_cache, const float* k_scale, const float* v_scale,
+                                                const void* q_idx8, const float* q_idx_scale,
+                                                const void* k_idx8_cache, const float* k_idx_scale,
+                                                const int32_t* block_table, int32_t max_blocks_per_seq,
+                                                int64_t num_pages, int32_t* idx, void* o, float* lse, void* workspace,
+                                                size_t workspace_bytes, msa_stream_t stream) {
+  Derived d;
+  msa_status_t st = derive(problem, d);
+  if (st != MSA_OK) return st;
+  if (!d.decode) return MSA_ERR_INVALID_ARG;  // one query per sequence
+  if ((st = check_attn_args(q, k8_cache, v8_cache, idx, o, lse)) != MSA_OK) return st;
+  if ((st = check_fp8_args(k8_cache, v8_cache, k_scale, v_scale)) != MSA_OK) return st;
+  if ((st = check_fp8_index_args(d, q_idx8, q_idx_scale, k_idx8_cache, k_idx_scale)) != MSA_OK) return st;
+  if (!block_table) return MSA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(block_table) & 3u) return MSA_ERR_ALIGNMENT;
+  if (num_pages < 1 || num_pages * 128 >= (1LL << 31)) return MSA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq < d.max_nb) return MSA_ERR_INVALID_ARG;  // a row must hold every block of the longest sequence
+  Ctx c;
+  if ((st = begin(problem, MSA_OP_FORWARD_FP8, workspace, workspace_bytes, stream, c)) != MSA_OK) return st;
+  c.fp8 = true;
+  c.k_scale = k_scale;
+  c.v_scale = v_scale;
+  use_fp8_index(c, q_idx_scale, k_idx_scale);
+  c.block_table = block_table;
+  c.bt_stride = max_blocks_per_seq;
+  c.n_pages = num_pages;
+  if ((st = run_plan(problem, c, 0)) != MSA_OK) return st;
+  if ((st = run_index_decode(problem, c, q_idx8, k_idx8_cache, idx)) != MSA_OK) return st;
+  return run_attn_decode(problem, c, q, k8_cache, v8_cache, idx, o, lse);
+}
+
 msa_status_t msa_read_device_status(const void* workspace, uint32_t* flags, msa_stream_t stream) {
   if (!flags) return MSA_ERR_INVALID_ARG;
   t_error_detail[0] = 0;

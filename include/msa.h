@@ -92,7 +92,8 @@ typedef enum msa_status {
 #define MSA_DEVICE_TIMEOUT 1u        /* a kernel wait exceeded its time limit */
 #define MSA_DEVICE_BAD_SEQLENS 2u    /* cu_seqlens disagree with the host sizes */
 #define MSA_DEVICE_BAD_INDEX 4u      /* a computed index failed its check (checked builds), or a block-table
-                                        entry of msa_forward_decode_paged(_fp8) named a page outside the cache */
+                                        entry of msa_forward_decode_paged(_fp8)(_index) named a page outside
+                                        the cache */
 
 typedef struct msa_problem {
   int32_t num_seqs;              /* >= 1 */
@@ -390,6 +391,21 @@ msa_status_t msa_forward_fp8_index(const msa_problem_t *problem, const void *q, 
                                    const float *q_idx_scale, const void *k_idx8, const float *k_idx_scale,
                                    int32_t *idx, void *o, float *lse, void *workspace, size_t workspace_bytes,
                                    msa_stream_t stream);
+
+/* msa_forward_decode_paged_fp8 with the index-key cache in fp8 as well
+ * (workspace op MSA_OP_FORWARD_FP8): k_idx8_cache [num_pages * 128, 128] E4M3
+ * codes with k_idx_scale [num_pages], one scale per page (msa_quantize_index_fp8
+ * gives that layout for the page pool taken as one sequence of num_pages * 128
+ * keys), and q_idx8 / q_idx_scale for the batch's queries.  Block table,
+ * errors and the device flag for a page outside the cache as for
+ * msa_forward_decode_paged. */
+msa_status_t msa_forward_decode_paged_fp8_index(const msa_problem_t *problem, const void *q, const void *k8_cache,
+                                                const void *v8_cache, const float *k_scale, const float *v_scale,
+                                                const void *q_idx8, const float *q_idx_scale,
+                                                const void *k_idx8_cache, const float *k_idx_scale,
+                                                const int32_t *block_table, int32_t max_blocks_per_seq,
+                                                int64_t num_pages, int32_t *idx, void *o, float *lse,
+                                                void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Waits for `stream`, then returns in *flags the MSA_DEVICE_* bits that the
  * last call on this workspace raised (0 = none).  workspace = NULL reads the

@@ -161,6 +161,14 @@ def test_fp8_index_calls_reject_bad_arguments_on_the_host(msa):
     assert lib.msa_forward_fp8_index(*fwd(ks=FAKE + 1)) == -3
     st, n = ws_size(msa, pre, msa.Op.QUANTIZE_INDEX_FP8)
     assert st == 0 and n > 0
+    dec = base_problem(msa, num_seqs=4, total_q=4, max_seqlen_q=1)
+    paged = lambda prob=ctypes.byref(dec), kis=FAKE, bt=FAKE, mb=16, npg=100: (
+        prob, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, kis, bt, mb, npg, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert lib.msa_forward_decode_paged_fp8_index(*paged(kis=None)) == -1     # no index-key scales
+    assert lib.msa_forward_decode_paged_fp8_index(*paged(bt=FAKE + 2)) == -3  # misaligned block table
+    assert lib.msa_forward_decode_paged_fp8_index(*paged(npg=0)) == -1        # no pages
+    assert lib.msa_forward_decode_paged_fp8_index(*paged(mb=7)) == -1         # a row cannot hold a sequence
+    assert lib.msa_forward_decode_paged_fp8_index(*paged(prob=p)) == -1       # a prefill batch
 
 
 def test_status_strings(msa):

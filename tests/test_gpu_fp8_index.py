@@ -191,3 +191,57 @@ def test_full_size_fp8_index_selection(msa, name, parity_report):
                          f"{int(tie.sum())} near-ties, {excused} of them selected differently")
     assert mism == 0, f"{mism} rows select differently from the oracle"
     assert excused / tie.size < 1e-3
+
+
+@pytest.mark.parametrize("n,ctx,seed", [(6, 9000, 71), (3, 40000, 72), (2, 200, 73)])
+def test_forward_decode_paged_fp8_index(msa, n, ctx, seed):
+    """Paged fp8 caches with the index keys in fp8 too (one scale per page) give the packed all-fp8 path's
+    results bit for bit, and quantizing the bf16 index-key page pool as one sequence of num_pages * 128 keys
+    yields exactly those codes and per-page scales."""
+    cfg = workloads.configs.Workload("dec8pi", None, seed=seed, decode_batch=n, decode_ctx=ctx, topk=16,
+                                     n_topics=16, hq=64, hkv=4, d_idx=128)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    k8, v8, ks, vs = msa.msa_quantize_kv_fp8(prob, x.k, x.v)
+    q8, qs, ki8, kis = msa.msa_quantize_index_fp8(prob, x.q_idx, x.k_idx)
+    cu_k = x.cu_k.cpu().numpy()
+    nbs = [int(cu_k[s + 1] - cu_k[s] + 127) // 128 for s in range(n)]
+    n_pages = sum(nbs) + 3
+    perm = np.random.default_rng(seed).permutation(n_pages)
+    bt = np.full((n, max(nbs) + 2), -7, np.int32)
+    rows = (n_pages * 128,) + tuple(x.k.shape[1:])
+    k8c = torch.zeros(rows, dtype=torch.uint8, device="cuda")
+    v8c = torch.zeros_like(k8c)
+    ki8c = torch.zeros((n_pages * 128, cfg.d_idx), dtype=torch.uint8, device="cuda")
+    ki_c = torch.zeros((n_pages * 128, cfg.d_idx), dtype=torch.bfloat16, device="cuda")
+    ksc = torch.ones((n_pages, cfg.hkv), dtype=torch.float32, device="cuda")
+    vsc = torch.ones_like(ksc)
+    kisc = torch.ones(n_pages, dtype=torch.float32, device="cuda")
+    at = blk = 0
+    used = []
+    for s in range(n):
+        for b in range(nbs[s]):
+            pg = int(perm[at])
+            at += 1
+            bt[s, b] = pg
+            lo, hi = int(cu_k[s]) + 128 * b, min(int(cu_k[s]) + 128 * (b + 1), int(cu_k[s + 1]))
+            dst = slice(pg * 128, pg * 128 + hi - lo)
+            k8c[dst], v8c[dst], ki8c[dst], ki_c[dst] = k8[lo:hi], v8[lo:hi], ki8[lo:hi], x.k_idx[lo:hi]
+            ksc[pg], vsc[pg], kisc[pg] = ks[blk], vs[blk], kis[blk]
+            used.append((pg, hi - lo))
+            blk += 1
+    bt = torch.from_numpy(bt).cuda()
+    ws = msa.workspace(prob, msa.Op.FORWARD_FP8)
+    idx, o, lse = msa.msa_forward_decode_paged_fp8_index(prob, x.q, k8c, v8c, ksc, vsc, q8, qs, ki8c, kisc, bt,
+                                                         ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
+    idx_r, o_r, lse_r = msa.msa_forward_fp8_index(prob, x.q, k8, v8, ks, vs, q8, qs, ki8, kis)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx_r) and torch.equal(o, o_r) and torch.equal(lse, lse_r)
+    pool = msa.problem_from_seqlens([1], [n_pages * 128], hq=cfg.hq, hkv=cfg.hkv, d_idx=cfg.d_idx, topk=cfg.topk)
+    _, _, ki8q, kisq = msa.msa_quantize_index_fp8(pool, k_idx=ki_c)
+    torch.cuda.synchronize()
+    for pg, nrow in used:
+        r = slice(pg * 128, pg * 128 + nrow)
+        assert torch.equal(ki8q[r], ki8c[r]) and torch.equal(kisq[pg], kisc[pg]), pg
