@@ -14,6 +14,10 @@
 // quantize_kv_fp8_kernel: one CTA per (key block, KV head): max |x| of the
 // block's K (and V) rows of that head, then the codes.  HBM-bound: 2 bytes read
 // and 1 written per element.
+// quantize_index_fp8_kernel: the same codes for the index inputs (an option
+// beside the bf16 index, since a quantized index selects other blocks): K_idx
+// with one scale per key block of a sequence (the index-key head is shared),
+// Q_idx with one scale per (query row, group).
 // kv8_widen_kernel: the prefill Main Branch multiplies on the tensor cores in
 // bf16 (QK^T) and fp16 (PV), so it reads 16-bit copies of the fp8 codes (K as
 // bf16, V as fp16); both conversions are exact (an E4M3 value has 4
