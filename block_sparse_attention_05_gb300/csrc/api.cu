@@ -321,6 +321,10 @@ msa_status_t begin(const msa_problem_t* p, msa_op_t op, void* ws, size_t ws_byte
   return MSA_OK;
 }
 
+// total_q == num_seqs with every q_len <= 1 means exactly one query per sequence, so query i belongs to
+// sequence i (cu_seqlens that say otherwise fail the plan kernel's check, and every later kernel skips).
+bool one_query_per_seq(const Derived& d) { return d.T == d.S && d.max_q <= 1; }
+
 msa_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return MSA_OK;
   std::snprintf(t_error_detail, sizeof t_error_detail, "stage %s: %s (%d)",
@@ -388,6 +392,7 @@ msa_status_t run_topk_pooled(const msa_problem_t* p, Ctx& c, const float* pooled
   tp.hkv = c.d.hkv;
   tp.topk = c.d.topk;
   tp.max_nb = static_cast<int>(stride < c.d.max_nb ? stride : c.d.max_nb);
+  tp.one_query_per_seq = one_query_per_seq(c.d);
   tp.cu_q = p->cu_seqlens_q;
   tp.seq = c.seq;
   tp.pooled = pooled;
@@ -475,6 +480,7 @@ msa_status_t run_combine(const msa_problem_t* p, Ctx& c, const int32_t* idx, voi
   cp.group = c.d.G;
   cp.topk = c.d.topk;
   cp.num_seqs = c.d.S;
+  cp.one_query_per_seq = one_query_per_seq(c.d);
   cp.sms = c.dev.sms;
   cp.cu_q = p->cu_seqlens_q;
   cp.seq = c.seq;

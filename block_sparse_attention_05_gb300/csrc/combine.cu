@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(32 * kCombineWarps, 2) combine_kernel(CombineP
       raw[sl] = (sl < p.topk) ? __ldcs(reinterpret_cast<const uint4*>(base + sl * slot_stride))
                               : make_uint4(0, 0, 0, 0);
 
-    const int s = find_seq(p.cu_q, p.num_seqs, i);
+    const int s = p.one_query_per_seq ? i : find_seq(p.cu_q, p.num_seqs, i);
     const SeqInfo si = p.seq[s];
     const int local = (si.kv_len - si.q_len + (i - si.q_start)) >> 7;
     bool valid[NG];

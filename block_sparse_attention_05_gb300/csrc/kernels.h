@@ -84,6 +84,7 @@ cudaError_t launch_index_score(const CUtensorMap& tq, const CUtensorMap& tk, con
 // sequences when every q_len is 1).
 struct TopkParams {
   int num_seqs, total_q, hkv, topk, max_nb;
+  bool one_query_per_seq;  // every sequence has exactly one query (a decode batch): query i is sequence i
   const int32_t* cu_q;
   const SeqInfo* seq;
   const float* pooled;
@@ -260,6 +261,7 @@ cudaError_t launch_kv8_widen(const uint8_t* k8, const uint8_t* v8, __nv_bfloat16
 
 struct CombineParams {
   int total_q, hq, hkv, group, topk, num_seqs;
+  bool one_query_per_seq;  // as in TopkParams
   int sms;  // grid: two CTAs per SM, grid-stride over the (query, head pair) items
   const int32_t* cu_q;
   const SeqInfo* seq;

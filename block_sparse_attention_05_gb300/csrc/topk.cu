@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(32 * kTopkMaxWarps) topk_pooled_kernel(TopkPar
   if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 502)) return;
   const int nwarps = blockDim.x >> 5;
   const int i = row / p.hkv;
-  const int s = find_seq(p.cu_q, p.num_seqs, i);
+  const int s = p.one_query_per_seq ? i : find_seq(p.cu_q, p.num_seqs, i);
   const SeqInfo si = p.seq[s];
   const int pos = si.kv_len - si.q_len + (i - si.q_start);
   const int nb = (pos >> 7) + 1;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kRadixThreads) topk_radix_kernel(TopkParams p)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 511)) return;
   const int i = row / p.hkv;
-  const int s = find_seq(p.cu_q, p.num_seqs, i);
+  const int s = p.one_query_per_seq ? i : find_seq(p.cu_q, p.num_seqs, i);
   const SeqInfo si = p.seq[s];
   const int pos = si.kv_len - si.q_len + (i - si.q_start);
   const int local = pos >> 7;  // also the number of non-local causal blocks
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThrThreads) topk_threshold_kernel(TopkParams 
   const int tid = threadIdx.x;
   if (!index_ok(p.hdr, row, static_cast<long long>(p.total_q) * p.hkv, 521)) return;
   const int i = row / p.hkv;
-  const int s = find_seq(p.cu_q, p.num_seqs, i);
+  const int s = p.one_query_per_seq ? i : find_seq(p.cu_q, p.num_seqs, i);
   const SeqInfo si = p.seq[s];
   const int pos = si.kv_len - si.q_len + (i - si.q_start);
   const int local = pos >> 7;  // also the number of non-local causal blocks

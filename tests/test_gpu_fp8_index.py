@@ -35,9 +35,12 @@ PREFILL = {
     # k > 16: pooled scores in the workspace, then the separate top-k
     "k32": dict(seqs=((900, 2600),), hq=64, hkv=4, topk=32, n_topics=8),
     "g128_hkv1": dict(seqs=((400, 400), (130, 700)), hq=128, hkv=1, topk=4, n_topics=4),
+    "k64": dict(seqs=((700, 3000), (64, 64)), hq=64, hkv=4, topk=64, n_topics=8),
+    "k1": dict(seqs=((300, 1000),), hq=64, hkv=4, topk=1, n_topics=8),
 }
 # decode batches: (sequences, context, topk, hq, hkv)
-DECODE = [(12, 9000, 16, 64, 4), (3, 40000, 16, 64, 8), (5, 700, 64, 64, 4), (2, 200, 16, 32, 1)]
+DECODE = [(12, 9000, 16, 64, 4), (3, 40000, 16, 64, 8), (5, 700, 64, 64, 4), (2, 200, 16, 32, 1),
+          (4, 20000, 32, 32, 4)]
 
 
 @pytest.fixture(scope="module")
