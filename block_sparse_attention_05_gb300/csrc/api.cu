@@ -886,7 +886,7 @@ msa_status_t msa_index_prologue(const msa_problem_t* problem, const void* x, int
   if (c.d.T == 0) return MSA_OK;
   CUtensorMap tx, twq, twk;
   if (!map_2d(tx, x, c.d.T, d_model, 128) || !map_2d(twq, w_q, static_cast<long long>(c.d.hkv) * 128, d_model, 128) ||
-      !map_2d(twk, w_k, 128, d_model, 128))
+      !map_2d(twk, w_k, 128, d_model, 64))  // the key head is loaded in 64-row halves (one per CTA of a pair)
     return MSA_ERR_CUDA;
   PrologueParams pp{};
   pp.num_seqs = c.d.S;

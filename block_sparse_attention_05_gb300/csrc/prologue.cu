@@ -10,13 +10,17 @@
 // RoPE on the first 64 dims, pairs (j, j + 32), angle pos * 10000^(-j/32).
 //
 // One GEMM, X [T, d_model] x W^T with W = the hkv query heads' rows followed
-// by the key head's (128 output columns each), on the tensor cores: work item
-// = 128 token rows x two heads (N = 256), or, for a lone last head, 256 token
-// rows x that head (two 128 x 128 MMAs sharing its weight tile, the second row
-// tile staged in the unused half of the weight stage), so every item does the
-// same 4.2 MFLOP per K step; K looped in 64-column blocks, A and B tiles by
-// TMA (128-byte swizzle) in a 4-stage ring, tcgen05 MMAs into a
-// double-buffered TMEM accumulator.  The epilogue
+// by the key head's (128 output columns each), on the tensor cores, by pairs
+// of CTAs (2-CTA clusters): a work item is 256 token rows x two heads (or the
+// lone last head), CTA rank r taking rows 128 r .. 128 r + 127 (N = 256, or
+// 128 for the lone head).  The weight rows are the same for both row tiles, so
+// each CTA loads its own X rows and one half of the item's weight rows,
+// multicast to both CTAs: 32 KB per K step per CTA from L2 instead of 48 (the
+// single-CTA kernel was paced by that operand feed).  K is looped in 64-column
+// blocks, tiles by TMA (128-byte swizzle) in a 4-stage ring whose slots a CTA
+// refills only when both CTAs' MMAs have read them (each MMA warp's commit
+// arrives on both CTAs' empty barriers), tcgen05 MMAs into a double-buffered
+// TMEM accumulator.  The epilogue
 // warps (one TMEM lane = one token row per thread) make two passes over each
 // head's 128 columns: the sum of squares, then normalisation, RoPE and the bf16
 // store.  The RoPE angle is reduced to a fraction of a turn before its sine
@@ -36,8 +40,10 @@ namespace {
 
 constexpr int kProStages = 4;
 constexpr int kProATile = 128 * 64 * 2;   // 128 rows x 64 bf16 = 16 KB
-constexpr int kProBTile = 256 * 64 * 2;   // 256 rows x 64 bf16 = 32 KB
+constexpr int kProBTile = 256 * 64 * 2;   // up to 256 weight rows x 64 bf16 = 32 KB
+constexpr int kProHead = 128 * 64 * 2;    // one head's weight rows of a K step: 16 KB
 constexpr int kProThreads = 256;
+constexpr uint16_t kProBoth = 0x3;        // both CTAs of the cluster
 constexpr float kRmsEps = 1e-6f;
 
 struct ProSmem {
@@ -51,55 +57,67 @@ struct ProSmem {
 
 constexpr size_t kProSmemBytes = 1024 + kProStages * (kProATile + kProBTile) + sizeof(ProSmem);
 
-// Work items, per 256 token rows (two row tiles): the head pairs (2p, 2p + 1) of row tile 0, then those of
-// row tile 1, then (n_heads odd) the lone last head over both row tiles.  Head index hkv is the key head.
-// Accumulator columns 0..127 and 128..255 hold slot 0 and slot 1: the pair's two heads, or the lone head's
-// two row tiles.
+// Work items of a CTA pair, per 256 token rows: the head pairs (2p, 2p + 1), then (n_heads odd) the lone last
+// head.  Head index hkv is the key head.  This CTA's rows are row0 .. row0 + 127; accumulator columns
+// 128 u .. 128 u + 127 hold head h0 + u.
 struct ProItem {
-  int row0, h0;
-  bool lone;  // one head over 256 rows (else two heads over 128 rows)
-  __device__ __forceinline__ int slot_row(int u) const { return lone ? row0 + 128 * u : row0; }
-  __device__ __forceinline__ int slot_head(int u) const { return lone ? h0 : h0 + u; }
+  int row0, h0, n_heads;
 };
 
 __host__ __device__ __forceinline__ int pro_items_per_256(int hkv) {
   const int n_heads = hkv + 1;
-  return 2 * (n_heads / 2) + (n_heads & 1);
+  return n_heads / 2 + (n_heads & 1);
 }
 __host__ __device__ __forceinline__ int pro_items(int total_q, int hkv) {
   return ((total_q + 255) / 256) * pro_items_per_256(hkv);
 }
 
-__device__ __forceinline__ ProItem pro_item(const PrologueParams& p, int j) {
+__device__ __forceinline__ ProItem pro_item(const PrologueParams& p, int j, int rank) {
   const int n_heads = p.hkv + 1, n_pairs = n_heads / 2, per = pro_items_per_256(p.hkv);
   const int sub = j % per;
   ProItem it;
-  it.lone = sub >= 2 * n_pairs;
-  it.row0 = (j / per) * 256 + (it.lone ? 0 : (sub / n_pairs) * 128);
-  it.h0 = it.lone ? n_heads - 1 : (sub % n_pairs) * 2;
+  const bool lone = sub >= n_pairs;
+  it.row0 = (j / per) * 256 + 128 * rank;
+  it.h0 = lone ? n_heads - 1 : 2 * sub;
+  it.n_heads = lone ? 1 : 2;
   return it;
+}
+
+// Loads weight rows [r0, r0 + n) (n = 64 or 128) of head h for K block kb into dst, multicast to both CTAs.
+// The key head's map has 64-row boxes, the query heads' 128-row boxes (each K step of a query head is one box).
+__device__ __forceinline__ void load_weights(const PrologueParams& p, const CUtensorMap* tm_wq,
+                                             const CUtensorMap* tm_wk, uint8_t* dst, uint64_t* bar, int h, int kb,
+                                             int r0, int n) {
+  if (h < p.hkv) {  // n == 128: only the key head is ever split (the lone head of an even hkv)
+    tma_load_2d_multicast(dst, tm_wq, bar, kb * 64, h * 128 + r0, kProBoth);
+  } else {
+    for (int q = 0; q < n; q += 64) tma_load_2d_multicast(dst + q * 128, tm_wk, bar, kb * 64, r0 + q, kProBoth);
+  }
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(kProThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProThreads, 1)
     index_prologue_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_wq,
                           const __grid_constant__ CUtensorMap tm_wk, PrologueParams p) {
   extern __shared__ uint8_t smem_raw[];
   WsHeader* hdr = p.hdr;
-  if (hdr->status & kFlagBadSeqlens) return;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* a_buf = base;                                   // kProStages x 16 KB
   uint8_t* b_buf = base + kProStages * kProATile;          // kProStages x 32 KB
   ProSmem& sm = *reinterpret_cast<ProSmem*>(base + kProStages * (kProATile + kProBTile));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_rank());
+  const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int n_items = pro_items(p.total_q, p.hkv);
   const int kblocks = p.d_model / 64;
+  // both CTAs of a pair see the same flag (the planning kernel before set it), so both skip or both run
+  const bool run = !(hdr->status & kFlagBadSeqlens);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kProStages; ++i) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.empty[i], 1);
+      mbar_init(&sm.empty[i], 2);  // both CTAs' MMA warps release a stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.acc_full[i], 1);
@@ -121,39 +139,39 @@ __global__ void __launch_bounds__(kProThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything is multicast to them
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
 
-  if (warp == 0) {
+  if (!run) {
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x) {
-        const ProItem w = pro_item(p, j);
+      for (int j = cluster; j < n_items && ok; j += n_clusters) {
+        const ProItem w = pro_item(p, j, rank);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int st = it % kProStages;
+          // the slot is free once both CTAs' MMAs have read its previous fill
           if (it >= kProStages && !mbar_wait(&sm.empty[st], ((it / kProStages) - 1) & 1, abort_flag)) {
             report_timeout(abort_flag, hdr, 701);
             ok = false;
             break;
           }
-          // 48 KB either way: X 128 rows + two heads' weights, or X 2 x 128 rows (the second in the weight
-          // stage's upper half) + one head's weights (rows past the end read as zeros and count their bytes)
-          mbar_arrive_expect_tx(&sm.full[st], kProATile + kProBTile);
+          // this CTA's X rows (rows past the end read as zeros and count their bytes), and the item's weight
+          // rows of this K step, half from each CTA
+          mbar_arrive_expect_tx(&sm.full[st], kProATile + w.n_heads * kProHead);
           tma_load_2d(a_buf + st * kProATile, &tm_x, &sm.full[st], kb * 64, w.row0);
-          if (w.lone) tma_load_2d(b_buf + st * kProBTile + kProBTile / 2, &tm_x, &sm.full[st], kb * 64, w.row0 + 128);
-          for (int hh = 0; hh < (w.lone ? 1 : 2); ++hh) {
-            const int h = w.h0 + hh;
-            uint8_t* dst = b_buf + st * kProBTile + hh * (kProBTile / 2);
-            if (h < p.hkv) tma_load_2d(dst, &tm_wq, &sm.full[st], kb * 64, h * 128);
-            else tma_load_2d(dst, &tm_wk, &sm.full[st], kb * 64, 0);
-          }
+          uint8_t* b = b_buf + st * kProBTile;
+          if (w.n_heads == 2)
+            load_weights(p, &tm_wq, &tm_wk, b + rank * kProHead, &sm.full[st], w.h0 + rank, kb, 0, 128);
+          else
+            load_weights(p, &tm_wq, &tm_wk, b + rank * (kProHead / 2), &sm.full[st], w.h0, kb, 64 * rank, 64);
         }
       }
-      // let every issued copy land before the CTA can exit
+      // let every copy into this CTA land before it can exit
       for (int s = 0; s < kProStages; ++s)
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t last = ((it - 1 - s) / kProStages) * kProStages + s;
@@ -165,9 +183,9 @@ __global__ void __launch_bounds__(kProThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, a_iter = 0;
       bool ok = true;
-      for (int j = blockIdx.x; j < n_items && ok; j += gridDim.x, ++a_iter) {
-        const ProItem w = pro_item(p, j);
-        const uint32_t idesc = idesc_bf16(128, w.lone ? 128 : 256, false);
+      for (int j = cluster; j < n_items && ok; j += n_clusters, ++a_iter) {
+        const ProItem w = pro_item(p, j, rank);
+        const uint32_t idesc = idesc_bf16(128, 128 * w.n_heads, false);
         const int ab = a_iter & 1;
         if (a_iter >= 2 && !mbar_wait(&sm.acc_empty[ab], ((a_iter >> 1) - 1) & 1, abort_flag)) {
           report_timeout(abort_flag, hdr, 711);
@@ -185,14 +203,10 @@ __global__ void __launch_bounds__(kProThreads, 1)
           const uint32_t aa = smem_u32(a_buf + st * kProATile), ba = smem_u32(b_buf + st * kProBTile);
           const uint32_t acc = (kb > 0) ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
+          for (int kk = 0; kk < 4; ++kk)
             umma_bf16(tmem + ab * 256, sdesc_sw128(aa + kk * 32, 16, 1024), sdesc_sw128(ba + kk * 32, 16, 1024),
                       idesc, (acc || kk > 0) ? 1u : 0u);
-            if (w.lone)  // row tile 1 (its X in the weight stage's upper half) into columns 128..255
-              umma_bf16(tmem + ab * 256 + 128, sdesc_sw128(ba + kProBTile / 2 + kk * 32, 16, 1024),
-                        sdesc_sw128(ba + kk * 32, 16, 1024), idesc, (acc || kk > 0) ? 1u : 0u);
-          }
-          umma_commit(&sm.empty[st]);
+          umma_commit_multicast(&sm.empty[st], kProBoth);
         }
         if (!ok) break;
         umma_commit(&sm.acc_full[ab]);
@@ -205,16 +219,16 @@ __global__ void __launch_bounds__(kProThreads, 1)
     const int r = (warp & 3) * 32 + lane;  // TMEM lane == token row of the tile
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     uint32_t a_iter = 0;
-    for (int j = blockIdx.x; j < n_items; j += gridDim.x, ++a_iter) {
-      const ProItem w = pro_item(p, j);
+    for (int j = cluster; j < n_items; j += n_clusters, ++a_iter) {
+      const ProItem w = pro_item(p, j, rank);
       const int ab = a_iter & 1;
       if (!mbar_wait_warp(&sm.acc_full[ab], (a_iter >> 1) & 1, abort_flag)) {
         report_timeout(abort_flag, hdr, 721);
         break;
       }
       tc_fence_after();
-      for (int hh = 0; hh < 2; ++hh) {  // accumulator slot: its rows and head
-        const int i = w.slot_row(hh) + r;
+      for (int hh = 0; hh < w.n_heads; ++hh) {  // accumulator slot: head h0 + hh of this CTA's rows
+        const int i = w.row0 + r;
         const bool valid = i < p.total_q;
         int pos = 0;
         long long krow = 0;
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(kProThreads, 1)
           krow = static_cast<long long>(si.k_start) + pos;
         }
         {
-          const int h = w.slot_head(hh);
+          const int h = w.h0 + hh;
           const uint32_t col = lane_addr + ab * 256 + hh * 128;
           const float* gamma = sm.gamma[h < p.hkv ? 0 : 1];
           // pass 1: sum of squares of the head's 128 projections
@@ -310,7 +324,8 @@ __global__ void __launch_bounds__(kProThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // neither CTA leaves while the other may still multicast into it or arrive on its barriers
+  cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -326,10 +341,22 @@ cudaError_t launch_index_prologue(const CUtensorMap& tx, const CUtensorMap& twq,
   cudaError_t e = cudaFuncSetAttribute(index_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kProSmemBytes));
   if (e != cudaSuccess) return e;
-  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  index_prologue_kernel<<<grid, kProThreads, kProSmemBytes, stream>>>(tx, twq, twk, p);
+  // persistent CTA pairs: as many as can be resident at once (a GPC with an odd number of free SMs leaves one
+  // idle), at most one per item
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (sms / 2)));
+  cfg.blockDim = dim3(kProThreads);
+  cfg.dynamicSmemBytes = kProSmemBytes;
+  cfg.stream = stream;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, index_prologue_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const long long n = items < clusters ? items : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+  e = cudaLaunchKernelEx(&cfg, index_prologue_kernel, tx, twq, twk, p);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa
