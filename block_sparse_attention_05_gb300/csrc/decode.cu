@@ -7,10 +7,12 @@
 // selection runs in decode too and that decode then reads about 2,048 KV
 // tokens whatever the context length).  The scan streams K_idx once and is
 // bound by HBM bandwidth, so it is built for bytes in flight: a persistent
-// grid, a TMA producer keeping a 6-stage ring of 128-key tiles full, and one
-// consumer warp per stage.  The 4 group queries against 16 keys are one small
-// mma.sync (m16n8k16: keys x d_idx times d_idx x groups) -- it keeps the
-// instruction count per byte low so the issue slots never limit the stream.
+// grid, a TMA producer keeping a ring of 128-key tiles full (6 stages of bf16
+// keys, or 12 of E4M3 codes for an fp8 index: the same bytes), and six
+// consumer warps.  The 4 group queries against 16 keys are one small mma.sync
+// (m16n8k16, or m16n8k32 for E4M3: keys x d_idx times d_idx x groups) -- it
+// keeps the instruction count per byte low so the issue slots never limit the
+// stream.
 //
 // Attention: persistent CTAs (two per SM) over the (sequence, group, selected
 // block, 16-head slice) items: a producer thread streams each item's Q rows,

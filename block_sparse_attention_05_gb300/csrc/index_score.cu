@@ -22,6 +22,12 @@
 // MMA issuer, warp 2 = TMEM allocator, warp 3 idle, warps 4..7 = epilogue.
 // Work items are claimed dynamically (atomic counter) from a list sorted by
 // descending cost, so the persistent grid balances itself.
+//
+// fp8 index inputs (E4M3 codes, d_idx 128): kind::f8f6f4 MMAs over 16 KB Q_idx
+// tiles and 32 KB pair tiles (a 6-stage ring), and 384 threads: warps 4..7 and
+// 8..11 are two epilogue groups, one per block of a pair, with registers moved
+// to them from warps 0..3 (setmaxnreg); a block's pooled score is its maximum
+// code dot product times its K_idx scale and the row's Q_idx scale.
 #include "common.cuh"
 #include "kernels.h"
 

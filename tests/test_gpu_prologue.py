@@ -87,6 +87,11 @@ CASES = {
     "hkv2_d3072": (dict(seqs=((700, 2000),), hq=64, hkv=2, d_idx=128, topk=16, n_topics=4), 3072),
     "hkv1_d1024": (dict(seqs=((260, 260),), hq=16, hkv=1, d_idx=128, topk=4, n_topics=4), 1024),
     "hkv8_d256": (dict(seqs=((333, 5000),), hq=64, hkv=8, d_idx=128, topk=16, n_topics=4), 256),
+    # 17 heads: eight head pairs and the lone key head per 256 rows
+    "hkv16_d512": (dict(seqs=((300, 900),), hq=128, hkv=16, d_idx=128, topk=8, n_topics=4), 512),
+    # a decode step: three new tokens, so the second CTA of the pair has no rows at all
+    "decode_step_d1024": (dict(seqs=((1, 5000), (1, 300), (1, 77)), hq=64, hkv=4, d_idx=128, topk=16, n_topics=4),
+                          1024),
 }
 
 
