@@ -166,8 +166,9 @@ def test_forward_fp8_index_end_to_end(msa, kind, key):
 
 
 # Full size, in the launch configuration of the benchmark's fp8 record: every row of the decode batches,
-# 4096 position-stratified rows of the 32K prefill.
-FULL_ROWS = {"decode_1m": None, "decode_128k": None, "prefill_32k": 4096}
+# 4096 position-stratified rows of the prefills.
+FULL_ROWS = {"decode_1m": None, "decode_128k": None, "prefill_32k": 4096, "prefill_128k": 4096, "varlen": 4096,
+             "chunked_1m": 4096}
 
 
 @pytest.mark.parametrize("name", sorted(FULL_ROWS))
