@@ -279,9 +279,26 @@ DECODE_CASES = [(8, 3000, 16, 128, 64, 4), (5, 700, 16, 64, 64, 4), (3, 128, 4, 
                 (16, 20000, 16, 128, 64, 4), (40, 60000, 16, 128, 64, 4),
                 (6, 9000, 32, 128, 64, 4), (4, 20000, 64, 128, 64, 4), (3, 1000, 64, 64, 64, 4),
                 (7, 5000, 16, 128, 32, 4), (5, 7000, 16, 128, 128, 4), (4, 6000, 24, 128, 128, 2),
-                (3, 4000, 16, 64, 128, 1),
-                # long rows: the decode top-k splits each row over 2 (and 4) CTAs and merges their candidates
+                (3, 4000, 16, 64, 128, 1), (4, 5000, 1, 128, 64, 4),
+                # long rows (about 2,300 and 4,700 blocks): the one-CTA-per-row threshold top-k
                 (3, 300000, 16, 128, 64, 4), (2, 600000, 8, 128, 64, 4)]
+
+
+def test_forward_decode_mixed_lengths(msa):
+    """A decode batch whose caches hold 1, 2, 128, 129, 257 and 5,000 keys: a first token alone in its block,
+    exact block boundaries, and sequences with fewer blocks than k next to one with more."""
+    cfg = small("dec_mixed", ((1, 1), (1, 2), (1, 128), (1, 129), (1, 257), (1, 5000)), hq=64, hkv=4, d_idx=128,
+                topk=16, n_topics=8, seed=77)
+    x = workloads.generate(cfg, device="cuda")
+    prob = problem_for(msa, x)
+    ws = msa.workspace(prob, msa.Op.FORWARD)
+    idx, o, lse = msa.msa_forward(prob, x.q, x.k, x.v, x.q_idx, x.k_idx, ws=ws)
+    torch.cuda.synchronize()
+    assert msa.msa_read_device_status(ws) == 0
+    ref = oracle.forward(x.cu_q, x.cu_k, x.q, x.k, x.v, x.q_idx, x.k_idx, block=cfg.block, topk=cfg.topk)
+    tie, mism = compare_indices(to_np(idx), ref)
+    assert mism == 0
+    assert_attention_close(to_np(o), to_np(lse), ref, cfg.hq // cfg.hkv, exempt=tie, what="dec_mixed")
 
 
 @pytest.mark.parametrize("n,ctx,topk,d_idx,hq,hkv", DECODE_CASES)
