@@ -64,6 +64,14 @@
  * Errors that only the device can see (cu_seqlens that contradict the host
  * sizes, a kernel wait that timed out) make the kernels skip their work and
  * set flags that msa_read_device_status() returns.
+ *
+ * CUDA graphs: since a call neither allocates nor synchronises, it may be
+ * enqueued on a stream that is being captured.  The graph keeps the pointers
+ * and sizes of the captured call (its workspace and outputs included) and
+ * reads the inputs' contents at each replay; the decode chain's dependent
+ * launches become programmatic edges.  Make one call of each entry point
+ * before the first capture (one-time driver look-ups happen on that call).
+ * msa_read_device_status() synchronises and is not capturable.
  */
 #ifndef MSA_H_
 #define MSA_H_
