@@ -495,16 +495,22 @@ def measure(msa, cfg, steps, warmup, args, dev, world, rank):
         t0.record(s_comp)
         s_in.wait_event(t0)
         s_out.wait_event(t0)
+        done = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         for n in range(steps):
             e2e_step(n + 2 * nbuf)
+            done[n].record(s_comp)  # this step's compute has finished
         for ev in ev_out:
             s_comp.wait_event(ev)  # every step's outputs are back in host memory
         t1.record(s_comp)
         t1.synchronize()
         e2e_ms = t0.elapsed_time(t1) / steps
         e2e_ms = max_over_ranks(e2e_ms, dev)
+        # spacing of consecutive steps' compute completions: a host copy that stalls shows as one long step
+        gaps = np.array([t0.elapsed_time(done[0])] + [done[i - 1].elapsed_time(done[i]) for i in range(1, steps)])
         e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
                "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "step_spacing_ms": {"median": float(np.median(gaps)), "min": float(gaps.min()),
+                                   "max": float(gaps.max()), "over_2x_median": int((gaps > 2 * np.median(gaps)).sum())},
                "overlap": "two buffer sets: step n+1's inputs in and step n-1's outputs out during step n"}
         if cfg.is_decode:
             e2e["inputs"] = "q, q_idx and the new token's k, v, k_idx rows (appended on the device); KV cache resident"

@@ -425,13 +425,22 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   sp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   sp.pooled = pooled;
   sp.pooled_stride = c.d.max_nb;
-  // about 4 work units per SM in total, at least 16 blocks each
-  long long want_units = 4LL * c.dev.sms;
-  int ups = static_cast<int>((want_units + c.d.S - 1) / c.d.S);
-  if (ups < 1) ups = 1;
-  int bpu = (c.d.max_nb + ups - 1) / ups;
-  if (bpu < 16) bpu = 16;
-  ups = (c.d.max_nb + bpu - 1) / bpu;
+  // Work units of consecutive key blocks, dealt to the CTAs in turn.  bf16 keys: about 4 units per SM in
+  // total, at least 16 blocks each.  E4M3 codes: 4 blocks (64 KB) per unit, so that the CTAs read the stream
+  // close together; it measured 5 % faster per all-fp8 decode step (decode_1m 0.1815 against 0.1913 ms,
+  // decode_128k 0.238 against 0.251), while bf16 keys moved within 1 % either way.
+  int ups, bpu;
+  if (c.fp8_index) {
+    bpu = 4;
+    ups = (c.d.max_nb + bpu - 1) / bpu;
+  } else {
+    const long long want_units = 4LL * c.dev.sms;
+    ups = static_cast<int>((want_units + c.d.S - 1) / c.d.S);
+    if (ups < 1) ups = 1;
+    bpu = (c.d.max_nb + ups - 1) / ups;
+    if (bpu < 16) bpu = 16;
+    ups = (c.d.max_nb + bpu - 1) / bpu;
+  }
   sp.units_per_seq = ups;
   sp.blocks_per_unit = bpu;
   sp.total_k = c.cache_rows();

@@ -93,10 +93,11 @@ struct ScanSmem {
 
 // The work of one CTA: units u = blockIdx.x + j * gridDim.x; unit u covers
 // blocks [c * bpu, min((c + 1) * bpu, nb)) of sequence u / ups, whose first
-// key row is k0 (kept here so that the TMA thread loads it once per unit, not
-// once per block).
+// key row k0 and block count nb are cached here (loaded when the sequence
+// changes, not once per unit or block).
 struct ScanCursor {
   int u, b, b_end, s, k0;
+  int cs = -1, nb = 0;  // the sequence whose facts are cached
 };
 
 __device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor& c) {
@@ -106,11 +107,14 @@ __device__ __forceinline__ bool scan_next(const DecodeScanParams& p, ScanCursor&
     if (c.u >= p.num_seqs * p.units_per_seq) return false;
     c.s = c.u / p.units_per_seq;
     const int unit = c.u % p.units_per_seq;
-    const SeqInfo si = p.seq[c.s];
-    const int nb = (si.kv_len + kBlock - 1) / kBlock;
+    if (c.s != c.cs) {
+      const SeqInfo si = p.seq[c.s];
+      c.cs = c.s;
+      c.nb = (si.kv_len + kBlock - 1) / kBlock;
+      c.k0 = si.k_start;
+    }
     c.b = unit * p.blocks_per_unit;
-    c.b_end = min(nb, c.b + p.blocks_per_unit);
-    c.k0 = si.k_start;
+    c.b_end = min(c.nb, c.b + p.blocks_per_unit);
   }
 }
 
