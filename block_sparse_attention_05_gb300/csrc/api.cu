@@ -425,12 +425,17 @@ msa_status_t run_index_decode(const msa_problem_t* p, Ctx& c, const void* q_idx,
   sp.blk_off = at<int32_t>(c.ws, c.L.blk_off);
   sp.pooled = pooled;
   sp.pooled_stride = c.d.max_nb;
-  // Work units of consecutive key blocks, dealt to the CTAs in turn.  bf16 keys: about 4 units per SM in
-  // total, at least 16 blocks each.  E4M3 codes: 4 blocks (64 KB) per unit, so that the CTAs read the stream
-  // close together; it measured 5 % faster per all-fp8 decode step (decode_1m 0.1815 against 0.1913 ms,
-  // decode_128k 0.238 against 0.251), while bf16 keys moved within 1 % either way.
+  // Work units of consecutive key blocks, dealt to the CTAs in turn; every sequence gets ups units (the
+  // ones past a shorter sequence's end are skipped).  bf16 keys: about 4 units per SM in total, at least 16
+  // blocks each.  E4M3 codes: 4 blocks (64 KB) per unit, so that the CTAs read the stream close together;
+  // it measured 5 % faster per all-fp8 decode step (decode_1m 0.1815 against 0.1913 ms, decode_128k 0.238
+  // against 0.251), while bf16 keys moved within 1 % either way.  Small units only while the sequences'
+  // lengths are close (the skipped units at most about as many as the real ones): a batch of one long
+  // cache and many short ones keeps the few large units.
+  const long long key_blocks = (static_cast<long long>(c.d.N) + kBlock - 1) / kBlock;  // at most the real ones
+  const bool small_units = c.fp8_index && static_cast<long long>(c.d.S) * c.d.max_nb <= 2 * key_blocks;
   int ups, bpu;
-  if (c.fp8_index) {
+  if (small_units) {
     bpu = 4;
     ups = (c.d.max_nb + bpu - 1) / bpu;
   } else {

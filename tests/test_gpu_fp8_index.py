@@ -38,6 +38,9 @@ PREFILL = {
     "k64": dict(seqs=((700, 3000), (64, 64)), hq=64, hkv=4, topk=64, n_topics=8),
     "k1": dict(seqs=((300, 1000),), hq=64, hkv=4, topk=1, n_topics=8),
 }
+# a decode batch whose caches hold 1, 2, 128, 129, 257 and 5,000 keys (its lengths far apart, so the scan
+# keeps its few large work units instead of the small ones of the even batches below)
+MIXED_DECODE = ((1, 1), (1, 2), (1, 128), (1, 129), (1, 257), (1, 5000))
 # decode batches: (sequences, context, topk, hq, hkv)
 DECODE = [(12, 9000, 16, 64, 4), (3, 40000, 16, 64, 8), (5, 700, 64, 64, 4), (2, 200, 16, 32, 1),
           (4, 20000, 32, 32, 4)]
@@ -79,7 +82,10 @@ def _cases():
 
 
 def _make(kind, key):
-    cfg = _prefill(key) if kind == "prefill" else _decode(*DECODE[key], seed=60 + key)
+    if kind == "mixed":
+        cfg = small("fp8_dec_mixed", MIXED_DECODE, hq=64, hkv=4, d_idx=128, topk=16, n_topics=8, seed=78)
+    else:
+        cfg = _prefill(key) if kind == "prefill" else _decode(*DECODE[key], seed=60 + key)
     return cfg, workloads.generate(cfg, device="cuda")
 
 
@@ -143,7 +149,7 @@ def test_index_topk_fp8_matches_oracle(msa, kind, key, parity_report):
 
 
 @pytest.mark.parametrize("kind,key", [("prefill", "varlen_g16"), ("prefill", "g32_k8"), ("decode", 0),
-                                      ("decode", 1)])
+                                      ("decode", 1), ("mixed", 0)])
 def test_forward_fp8_index_end_to_end(msa, kind, key):
     """All-fp8 forward: selection against the oracle's Index Branch over the codes, O and LSE against the
     oracle's fp8 Main Branch on the oracle's selection (near-tie rows exempt)."""
