@@ -238,6 +238,14 @@ def ncu_traffic(workload: str, kernel_file: str, x):
     return rec["dram_bytes"] / rec["units"] * units_now
 
 
+def step_spacing(gaps_ms):
+    """Summary of the times between consecutive steps' completions (ms): a stalled step stands out against
+    the median."""
+    g = np.asarray(gaps_ms, dtype=np.float64)
+    med = float(np.median(g))
+    return {"median": med, "min": float(g.min()), "max": float(g.max()), "over_2x_median": int((g > 2 * med).sum())}
+
+
 # ------------------------------------------------------------------ CPU oracle timing (+ parity of its rows)
 def host_copy(x):
     return dict(cu_q=x.cu_q.cpu(), cu_k=x.cu_k.cpu(), q=x.q.cpu(), k=x.k.cpu(), v=x.v.cpu(),
@@ -506,11 +514,10 @@ def measure(msa, cfg, steps, warmup, args, dev, world, rank):
         e2e_ms = t0.elapsed_time(t1) / steps
         e2e_ms = max_over_ranks(e2e_ms, dev)
         # spacing of consecutive steps' compute completions: a host copy that stalls shows as one long step
-        gaps = np.array([t0.elapsed_time(done[0])] + [done[i - 1].elapsed_time(done[i]) for i in range(1, steps)])
+        gaps = [t0.elapsed_time(done[0])] + [done[i - 1].elapsed_time(done[i]) for i in range(1, steps)]
         e2e = {"value": units_per_gpu * world / (e2e_ms / 1000.0), "unit": unit, "ms_per_step": e2e_ms,
                "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "step_spacing_ms": {"median": float(np.median(gaps)), "min": float(gaps.min()),
-                                   "max": float(gaps.max()), "over_2x_median": int((gaps > 2 * np.median(gaps)).sum())},
+               "step_spacing_ms": step_spacing(gaps),
                "overlap": "two buffer sets: step n+1's inputs in and step n-1's outputs out during step n"}
         if cfg.is_decode:
             e2e["inputs"] = "q, q_idx and the new token's k, v, k_idx rows (appended on the device); KV cache resident"

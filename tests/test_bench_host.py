@@ -1,5 +1,6 @@
 """The benchmark's host-side bookkeeping on CPU: the source hash that decides
-whether a committed DRAM-traffic record still describes the kernel."""
+whether a committed DRAM-traffic record still describes the kernel, and the
+summary of the end-to-end steps' spacing."""
 import json
 import os
 
@@ -38,3 +39,10 @@ def test_committed_traffic_records_name_files_that_exist():
     for name, r in rec.items():
         assert os.path.exists(os.path.join(ROOT, "block_sparse_attention_05_gb300", "csrc", r["source"])), name
         assert r["units"] > 0 and r["dram_bytes"] > 0 and r["units_kind"] in ("total_q", "total_k")
+
+
+def test_step_spacing_flags_a_stalled_step():
+    sp = bench.step_spacing([21.0, 21.5, 118.0, 20.8, 21.2])
+    assert sp["median"] == 21.2 and sp["min"] == 20.8 and sp["max"] == 118.0
+    assert sp["over_2x_median"] == 1
+    assert bench.step_spacing([5.0, 5.0, 5.0])["over_2x_median"] == 0
